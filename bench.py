@@ -1,0 +1,550 @@
+#!/usr/bin/env python
+"""Benchmark of one paged-KV attention step on GB300.
+
+A step is the whole hot path on one synthetic batch: pa_cache_write (the new
+tokens' K/V into their slots) then pa_forward (plan + split-KV attention, and
+the multi-token path when the step has chunks).  The headline workload is the
+Llama-3-8B single-layer decode shape (batch 256, 32 q / 8 kv heads, D=128,
+bf16, lognormal contexts with median 1024, sigma 0.8, cap 8192); its KV
+(~1.4 GB) is far larger than L2, so no flush is needed between steps.  The
+mixed continuous-batching step (192 decodes + two 512-token chunks) is
+reported alongside as tokens/s per layer.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference]
+
+Prints one JSON line.  `--impl reference` times the fp64 CPU oracle on a
+bounded sample of the same workload instead (there is no other reference
+implementation of this path).
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "decode paged-attn HBM GB/s & % of GB300 peak; mixed-step tokens/s per layer"
+HEADLINE = "llama3_8b_decode"
+MIXED = "mixed_step"
+FALLBACK_HBM_GBS = 6800.0
+WORKLOAD_TEXT = {
+    "llama3_8b_decode": "Llama-3-8B single-layer decode: batch 256, 32 q / 8 kv heads, head_size 128, "
+                        "bf16, context lognormal(median 1024, sigma 0.8, cap 8192), block_size 16, "
+                        "random block tables, pool 1.2x needed",
+    "mixed_step": "mixed step, Llama-3-8B heads, bf16: 192 decodes (context U[256,4096]) + 2 chunked "
+                  "prefills of 512 (prior 0 and 1536), 1216 tokens, half the decodes share 64 prefix blocks",
+}
+
+
+# ---------------------------------------------------------------------------
+# Algorithmic work of a step (counted from the inputs, never from kernels)
+# ---------------------------------------------------------------------------
+
+def step_work(spec, meta) -> dict:
+    """Bytes the method must move and prefill flops, from the step's metadata.
+
+    decode_bytes: unique KV slots read by q_len==1 requests (a shared prefix
+    block counted once) x Hkv x D x 2 (K,V) x e, plus their q and out rows,
+    block-table entries, seq_lens and query_start_loc.
+    write_bytes: new k,v read + written into the cache, plus slot_mapping.
+    chunk_bytes/flops: the same for q_len>1 requests; flops = 4 x D x Hq x
+    (visible (query, key) pairs)."""
+    import numpy as np
+    e = 2 if spec.dtype == "bf16" else 4
+    Hq, Hkv, D, bs = spec.num_q_heads, spec.num_kv_heads, spec.head_size, spec.block_size
+    bt = meta.block_tables
+    dec_slots, chk_slots = [], []
+    table_dec = table_chk = 0
+    pairs = 0
+    for r in range(spec.num_seqs):
+        S, L = int(spec.seq_lens[r]), int(spec.q_lens[r])
+        p = np.arange(S)
+        slots = bt[r, p // bs].astype(np.int64) * bs + p % bs
+        nb = -(-S // bs)
+        if L == 1:
+            dec_slots.append(slots)
+            table_dec += nb
+        else:
+            chk_slots.append(slots)
+            table_chk += nb
+            pairs += sum(S - L + j + 1 for j in range(L))
+    row = Hkv * D * e
+    n_dec = sum(1 for L in spec.q_lens if L == 1)
+    n_chk_tok = int(sum(L for L in spec.q_lens if L > 1))
+    uniq = lambda lst: int(len(np.unique(np.concatenate(lst)))) if lst else 0  # noqa: E731
+    meta_bytes = 4 * (2 * spec.num_seqs + 1)
+    decode_bytes = (uniq(dec_slots) * row * 2 + 2 * n_dec * Hq * D * e + 4 * table_dec + meta_bytes)
+    chunk_bytes = (uniq(chk_slots) * row * 2 + 2 * n_chk_tok * Hq * D * e + 4 * table_chk)
+    T = spec.num_tokens
+    write_bytes = 2 * 2 * T * row + 8 * T
+    return dict(decode_bytes=decode_bytes, chunk_bytes=chunk_bytes, write_bytes=write_bytes,
+                step_bytes=decode_bytes + chunk_bytes + write_bytes,
+                chunk_flops=4.0 * D * Hq * pairs, tokens=T)
+
+
+def measured_peaks() -> tuple[float, str]:
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            return float(json.load(f)["hbm_gbs"]), "measured"
+    except Exception:
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+def kernel_source_hash() -> str:
+    h = hashlib.sha256()
+    for name in ("pa_attn_cc.cuh", "pa_device.cuh"):
+        with open(os.path.join(ROOT, "paged_kv_attention_04_gb300", "csrc", name), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def recorded_traffic(workload: str):
+    """DRAM bytes per launch of the decode kernel from a committed ncu summary,
+    if it was taken on the current kernel source; else None."""
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    try:
+        with open(path) as f:
+            rec = json.load(f)[workload]
+        if rec.get("kernel_hash") == kernel_source_hash():
+            return float(rec["dram_bytes_per_launch"])
+    except Exception:
+        pass
+    return None
+
+
+# ---------------------------------------------------------------------------
+# Clock sampling during the timed region
+# ---------------------------------------------------------------------------
+
+class ClockSampler:
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_uuid: str | None):
+        self.samples = []
+        self.proc = None
+        self.uuid = gpu_uuid
+        self.marks = {}
+
+    def start(self):
+        cmd = ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+               "-lms", "200"]
+        if self.uuid:
+            cmd += ["-i", self.uuid]
+        try:
+            self.proc = subprocess.Popen(cmd, stdout=subprocess.PIPE, stderr=subprocess.DEVNULL,
+                                         text=True)
+        except Exception:
+            self.proc = None
+            return
+        threading.Thread(target=self._read, daemon=True).start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.samples.append((time.time(), line.strip()))
+
+    def mark(self, name):
+        self.marks[name] = time.time()
+
+    def stop(self) -> dict:
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        time.sleep(0.45)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        t0, t1 = self.marks.get("timed_start", 0), self.marks.get("timed_end", 1e30)
+        rows = [s for t, s in self.samples if t0 - 0.25 <= t <= t1 + 0.25]
+        window = "timed"
+        if not rows:
+            w0 = self.marks.get("warm_start", 0)
+            rows = [s for t, s in self.samples if w0 <= t <= t1 + 0.3]
+            window = "warmup+timed"
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for s in rows:
+            parts = [p.strip() for p in s.split(",")]
+            if len(parts) < 8:
+                continue
+            try:
+                sm.append(float(parts[0]))
+                smax.append(float(parts[1]))
+            except ValueError:
+                continue
+            for nm, val in zip(names, parts[4:8]):
+                if val.lower().startswith("active"):
+                    reasons.add(nm)
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(smax) if smax else None,
+                "reasons": sorted(reasons), "samples": len(sm), "window": window}
+
+
+# ---------------------------------------------------------------------------
+# CPU oracle timing (runs in a child process with single-threaded BLAS)
+# ---------------------------------------------------------------------------
+
+def oracle_worker(name: str, min_seconds: float, stride: int, steps: int, warmup: int,
+                  step_budget: float) -> None:
+    """Time the fp64 oracle on a sample of workload `name`: every `stride`-th
+    request (stride 0: chosen so one pass fits `step_budget` seconds), each
+    with a private copy of its blocks; one pass = slot write + attention of the
+    sampled requests.  With steps > 0, times warmup + steps passes and reports
+    the timed ones; else repeats passes until min_seconds.  Prints JSON."""
+    import numpy as np
+
+    import oracle
+    from paged_kv_attention_04_gb300 import workloads as W
+    spec = W.CONFIGS[name]()
+    st = W.make_step(spec)
+    b = W.to_numpy_bits
+    bt = st.block_tables.numpy()
+    qsl = st.query_start_loc.numpy()
+    scale = 1.0 / np.sqrt(spec.head_size)
+
+    def prep(r):
+        S, L = int(spec.seq_lens[r]), int(spec.q_lens[r])
+        nb = -(-S // 16)
+        blocks = bt[r, :nb].astype(np.int64)
+        t0, t1 = int(qsl[r]), int(qsl[r + 1])
+        pos = np.arange(S - L, S)
+        return dict(kc=b(st.k_cache[blocks]), vc=b(st.v_cache[blocks]), q=b(st.q[t0:t1]),
+                    k=b(st.k[t0:t1]), v=b(st.v[t0:t1]), slots=(pos // 16) * 16 + pos % 16,
+                    S=S, L=L, nb=nb)
+
+    def run(samples):
+        for s in samples:
+            kc, vc = oracle.cache_write(s["k"], s["v"], s["slots"], s["kc"], s["vc"])
+            oracle.paged_attention(s["q"], kc, vc, np.arange(s["nb"])[None, :], np.array([s["S"]]),
+                                   np.array([0, s["L"]]), scale, spec.num_kv_heads)
+
+    if stride <= 0:
+        probe = [prep(r) for r in range(0, spec.num_seqs, 32)]
+        t = time.perf_counter()
+        run(probe)
+        per_req = (time.perf_counter() - t) / len(probe)
+        n = int(max(1, min(spec.num_seqs, step_budget / max(per_req, 1e-6))))
+        stride = max(1, spec.num_seqs // n)
+    reqs = list(range(0, spec.num_seqs, stride))
+    samples = [prep(r) for r in reqs]
+    sub = W.custom_spec("sample", spec.dtype, spec.num_q_heads, spec.num_kv_heads, spec.head_size,
+                        [s["L"] for s in samples], [s["S"] for s in samples])
+    work = step_work(sub, W.make_meta(sub))
+    del st
+    times = []
+    if steps > 0:
+        for i in range(warmup + steps):
+            t = time.perf_counter()
+            run(samples)
+            if i >= warmup:
+                times.append(time.perf_counter() - t)
+    else:
+        elapsed = 0.0
+        while elapsed < min_seconds or not times:
+            t = time.perf_counter()
+            run(samples)
+            times.append(time.perf_counter() - t)
+            elapsed += times[-1]
+    print(json.dumps({"seconds": sum(times), "reps": len(times), "requests": len(reqs),
+                      "stride": stride, "bytes_per_rep": work["step_bytes"],
+                      "tokens_per_rep": work["tokens"]}))
+
+
+def time_oracle(name: str, min_seconds: float = 10.0, stride: int = 1, steps: int = 0,
+                warmup: int = 0, step_budget: float = 1.0) -> dict:
+    env = dict(os.environ)
+    for k in ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS", "MKL_NUM_THREADS", "NUMEXPR_NUM_THREADS"):
+        env[k] = "1"
+    env["CUDA_VISIBLE_DEVICES"] = ""
+    for k in ("RANK", "WORLD_SIZE", "LOCAL_RANK", "MASTER_ADDR", "MASTER_PORT"):
+        env.pop(k, None)
+    cmd = [sys.executable, os.path.abspath(__file__), "--oracle-worker", name,
+           "--oracle-seconds", str(min_seconds), "--oracle-stride", str(stride),
+           "--steps", str(steps), "--warmup", str(warmup), "--oracle-budget", str(step_budget)]
+    res = subprocess.run(cmd, capture_output=True, text=True, env=env, cwd=ROOT)
+    if res.returncode != 0:
+        raise RuntimeError(f"oracle worker failed: {res.stderr[-2000:]}")
+    return json.loads(res.stdout.strip().splitlines()[-1])
+
+
+# ---------------------------------------------------------------------------
+# GPU arm
+# ---------------------------------------------------------------------------
+
+def dist_setup():
+    import torch
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    else:
+        torch.cuda.set_device(local)
+    return world, rank, local
+
+
+def dist_max(x: float, world: int) -> float:
+    if world == 1:
+        return x
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device="cuda")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def barrier(world: int):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+class StepRunner:
+    """Device-resident step of one workload through the C ABI."""
+
+    def __init__(self, name: str, seed_offset: int = 0):
+        import torch
+
+        import paged_kv_attention_04_gb300 as P
+        from paged_kv_attention_04_gb300 import workloads as W
+        self.P, self.torch = P, torch
+        fn = W.CONFIGS[name]
+        spec = fn()
+        if seed_offset:
+            spec.seed += seed_offset
+        self.spec = spec
+        self.meta = W.make_meta(spec)
+        self.st = W.make_step(spec, device="cuda")
+        st = self.st
+        self.layout = P.layout_of(st.k_cache, spec.num_q_heads)
+        self.ws = P.alloc_workspace(self.layout, spec.num_seqs, spec.num_tokens, st.max_seq_len)
+        self.out = torch.empty_like(st.q)
+        self.status = torch.zeros(1, dtype=torch.int32, device="cuda")
+        self.work = step_work(spec, self.meta)
+        self.launches_per_step = 3 + (1 if st.max_query_len > 1 else 0)
+
+    def step(self, q=None, k=None, v=None, slots=None, bt=None, sl=None, qsl=None):
+        st, P = self.st, self.P
+        q = st.q if q is None else q
+        P.pa_cache_write(st.k if k is None else k, st.v if v is None else v,
+                         st.slot_mapping if slots is None else slots, st.k_cache, st.v_cache,
+                         self.layout, self.status)
+        P.pa_forward(q, st.k_cache, st.v_cache, st.block_tables if bt is None else bt,
+                     st.seq_lens if sl is None else sl, st.query_start_loc if qsl is None else qsl,
+                     st.max_query_len, st.max_seq_len, st.scale, self.out, self.ws, self.layout,
+                     self.status)
+
+    def time_device(self, steps: int, warmup: int, world: int, clocks: ClockSampler | None = None):
+        """Inputs resident in HBM; returns (ms per step, decode-kernel ms per launch,
+        forward ms per call)."""
+        torch, P = self.torch, self.P
+        for _ in range(warmup):
+            self.step()
+        torch.cuda.synchronize()
+        evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+               for _ in range(steps)]
+        barrier(world)
+        torch.cuda.synchronize()
+        if clocks:
+            clocks.mark("timed_start")
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        for i in range(steps):
+            P.pa_set_profile_events(evs[i][0], evs[i][1])
+            self.step()
+        e1.record()
+        torch.cuda.synchronize()
+        if clocks:
+            clocks.mark("timed_end")
+        barrier(world)
+        P.pa_set_profile_events(None, None)
+        total_ms = e0.elapsed_time(e1)
+        dec_ms = statistics.mean(a.elapsed_time(b) for a, b in evs)
+        return total_ms / steps, dec_ms
+
+    def time_e2e(self, steps: int, warmup: int, world: int):
+        """Same step with this step's inputs copied from pinned host memory
+        and the output copied back, inside the timed region."""
+        torch = self.torch
+        st = self.st
+        names = ("q", "k", "v", "slot_mapping", "block_tables", "seq_lens", "query_start_loc")
+        host = {n: getattr(st, n).cpu().pin_memory() for n in names}
+        dev = {n: torch.empty_like(getattr(st, n)) for n in names}
+        out_host = torch.empty(self.out.shape, dtype=self.out.dtype).pin_memory()
+        h2d = sum(t.numel() * t.element_size() for t in host.values())
+        d2h = out_host.numel() * out_host.element_size()
+
+        def one():
+            for n in names:
+                dev[n].copy_(host[n], non_blocking=True)
+            self.step(q=dev["q"], k=dev["k"], v=dev["v"], slots=dev["slot_mapping"],
+                      bt=dev["block_tables"], sl=dev["seq_lens"], qsl=dev["query_start_loc"])
+            out_host.copy_(self.out, non_blocking=True)
+
+        for _ in range(warmup):
+            one()
+        torch.cuda.synchronize()
+        barrier(world)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        for _ in range(steps):
+            one()
+        e1.record()
+        torch.cuda.synchronize()
+        barrier(world)
+        return e0.elapsed_time(e1) / steps, h2d, d2h
+
+
+def run_gpu_arm(args):
+    import torch
+    from paged_kv_attention_04_gb300 import build
+    build.build()
+    world, rank, local = dist_setup()
+    if world != args.gpus:
+        print(f"warning: WORLD_SIZE={world} but --gpus {args.gpus}", file=sys.stderr)
+    dev_uuid = None
+    try:
+        u = str(torch.cuda.get_device_properties(local).uuid)
+        dev_uuid = u if u.startswith("GPU-") else "GPU-" + u
+    except Exception:
+        pass
+
+    runner = StepRunner(HEADLINE, seed_offset=rank * 1000 if world > 1 else 0)
+    clocks = ClockSampler(dev_uuid)
+    clocks.start()
+    time.sleep(0.3)
+    clocks.mark("warm_start")
+    ms, dec_ms = runner.time_device(args.steps, args.warmup, world, clocks)
+    clock_info = clocks.stop()
+    if int(runner.status.item()) != 0:
+        raise RuntimeError(f"device status {int(runner.status.item())}")
+    ms_max = dist_max(ms, world)
+    dec_max = dist_max(dec_ms, world)
+    w = runner.work
+    value = world * w["step_bytes"] / (ms_max * 1e-3) / 1e9
+    e2e_ms, h2d, d2h = runner.time_e2e(max(3, args.steps // 4), max(3, args.warmup), world)
+    e2e_ms = dist_max(e2e_ms, world)
+    e2e_value = world * w["step_bytes"] / (e2e_ms * 1e-3) / 1e9
+    peak, peak_src = measured_peaks()
+    achieved = w["decode_bytes"] / (dec_max * 1e-3) / 1e9
+    traffic = recorded_traffic(HEADLINE)
+    launches = runner.launches_per_step * args.steps
+    del runner
+    torch.cuda.empty_cache()
+
+    # mixed continuous-batching step
+    mixed = StepRunner(MIXED, seed_offset=rank * 1000 if world > 1 else 0)
+    mms, mdec = mixed.time_device(max(3, args.steps // 2), args.warmup, world)
+    mms, mdec = dist_max(mms, world), dist_max(mdec, world)
+    mw = mixed.work
+    rest_ms = max(mms - mdec, 1e-6)
+    mixed_info = {
+        "workload": WORKLOAD_TEXT[MIXED],
+        "tokens_per_s_per_layer": world * mw["tokens"] / (mms * 1e-3),
+        "ms_per_step": mms,
+        "decode_kernel_ms": mdec,
+        "decode_gbs": mw["decode_bytes"] / (mdec * 1e-3) / 1e9,
+        "chunk_and_write_ms": rest_ms,
+        "chunk_tflops_upper": mw["chunk_flops"] / (rest_ms * 1e-3) / 1e12,
+    }
+    if int(mixed.status.item()) != 0:
+        raise RuntimeError(f"mixed-step device status {int(mixed.status.item())}")
+    del mixed
+    torch.cuda.empty_cache()
+
+    line = {
+        "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms_max, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": WORKLOAD_TEXT[HEADLINE], "step": "pa_cache_write + pa_forward",
+                   "l2": "no flush: KV read per step (1.4 GB) > L2 (126 MB)",
+                   "parallelism": "replicas" if world > 1 else "single GPU",
+                   "algorithmic_bytes_per_step": w["step_bytes"]},
+        "roofline": {"bound": "hbm", "kernel": "attn_cc_kernel<bf16,128,4,1> (decode)",
+                     "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
+                     "peak_source": peak_src, "traffic": traffic,
+                     "algorithmic_bytes_per_launch": w["decode_bytes"], "kernel_ms": dec_max},
+        "e2e": {"value": e2e_value, "unit": "GB/s", "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms},
+        "gpu_launches": launches,
+        "clocks": clock_info,
+        "mixed": mixed_info,
+    }
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        o = time_oracle(HEADLINE, min_seconds=args.oracle_seconds, stride=args.oracle_stride)
+        line["cpu_baseline"] = {
+            "value": o["bytes_per_rep"] * o["reps"] / o["seconds"] / 1e9, "unit": "GB/s",
+            "cores": 1, "kind": "oracle",
+            "sample": f"{o['requests']} of 256 requests (every {o['stride']}th), each with its own "
+                      f"blocks: fp64 slot write + attention, {o['reps']} passes, "
+                      f"{o['seconds']:.1f} s on 1 core"}
+    if rank == 0:
+        print(json.dumps(line))
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+def run_reference_arm(args):
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return
+    # each step is one oracle pass over a sample sized so the run takes ~2 minutes
+    budget = 120.0 / max(1, args.steps + args.warmup)
+    o = time_oracle(HEADLINE, stride=0, steps=args.steps, warmup=args.warmup, step_budget=budget)
+    value = o["bytes_per_rep"] * o["reps"] / o["seconds"] / 1e9
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": 1,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * o["seconds"] / o["reps"],
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic",
+        "config": {"workload": WORKLOAD_TEXT[HEADLINE], "step": "oracle slot write + attention",
+                   "parallelism": "single CPU core"},
+        "cpu_baseline": {"value": value, "unit": "GB/s", "cores": 1, "kind": "oracle",
+                         "sample": f"{o['requests']} of 256 requests per step (every "
+                                   f"{o['stride']}th), each with its own blocks"},
+        "e2e": {"value": value, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+        "gpu_launches": 0,
+    }
+    print(json.dumps(line))
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", default="gpu", choices=["gpu", "reference"])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--oracle-seconds", type=float, default=10.0)
+    ap.add_argument("--oracle-stride", type=int, default=1)
+    ap.add_argument("--oracle-budget", type=float, default=1.0, help=argparse.SUPPRESS)
+    ap.add_argument("--oracle-worker", default=None, help=argparse.SUPPRESS)
+    args = ap.parse_args()
+    if args.oracle_worker:
+        oracle_worker(args.oracle_worker, args.oracle_seconds, args.oracle_stride, args.steps,
+                      args.warmup, args.oracle_budget)
+        return
+    if args.warmup < 3:
+        args.warmup = 3
+    if args.impl == "reference":
+        run_reference_arm(args)
+    else:
+        run_gpu_arm(args)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,301 @@
+// Host side of the libpa C ABI: argument checks, workspace layout, launch
+// order.  Nothing here touches tensor data; every step of the attention runs
+// in the kernels.
+#include <cmath>
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+#include <string>
+
+#include "pa_internal.h"
+
+namespace pa {
+cudaError_t launch_attn_cc_bf16(const AttnParams& p, int head_size, int group, int positions,
+                                int num_sms, cudaStream_t stream);
+cudaError_t launch_attn_cc_f32(const AttnParams& p, int head_size, int group, int positions,
+                               int num_sms, cudaStream_t stream);
+
+cudaError_t launch_attn_cuda_core(const AttnParams& p, pa_dtype dtype, int head_size, int group,
+                                  int positions, int num_sms, cudaStream_t stream) {
+  return dtype == PA_BF16 ? launch_attn_cc_bf16(p, head_size, group, positions, num_sms, stream)
+                          : launch_attn_cc_f32(p, head_size, group, positions, num_sms, stream);
+}
+
+namespace {
+
+thread_local std::string g_last_error;
+thread_local cudaEvent_t g_prof_start = nullptr;
+thread_local cudaEvent_t g_prof_stop = nullptr;
+
+int fail(int code, const char* fmt, ...) {
+  char buf[512];
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(buf, sizeof(buf), fmt, ap);
+  va_end(ap);
+  g_last_error = buf;
+  return code;
+}
+
+int fail_cuda(cudaError_t e, const char* what) {
+  return fail(PA_ERR_CUDA, "%s: %s", what, cudaGetErrorString(e));
+}
+
+int elem_bytes(pa_dtype t) { return t == PA_BF16 ? 2 : 4; }
+
+bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+long long cdiv(long long a, long long b) { return (a + b - 1) / b; }
+
+int check_layout(const pa_layout* L) {
+  if (!L) return fail(PA_ERR_INVALID, "layout is NULL");
+  if (L->dtype != PA_F32 && L->dtype != PA_BF16)
+    return fail(PA_ERR_INVALID, "dtype %d is not PA_F32 or PA_BF16", static_cast<int>(L->dtype));
+  if (L->num_q_heads <= 0 || L->num_kv_heads <= 0 || L->head_size <= 0 || L->num_blocks <= 0)
+    return fail(PA_ERR_INVALID, "heads, head_size and num_blocks must be positive");
+  if (L->num_q_heads % L->num_kv_heads)
+    return fail(PA_ERR_INVALID, "num_q_heads %d is not a multiple of num_kv_heads %d",
+                L->num_q_heads, L->num_kv_heads);
+  if (L->block_size != kBlockSize)
+    return fail(PA_ERR_UNSUPPORTED, "block_size %d (built for 16)", L->block_size);
+  if (L->head_size != 64 && L->head_size != 128)
+    return fail(PA_ERR_UNSUPPORTED, "head_size %d (built for 64 and 128)", L->head_size);
+  const int g = L->num_q_heads / L->num_kv_heads;
+  if (g != 1 && g != 2 && g != 4 && g != 8)
+    return fail(PA_ERR_UNSUPPORTED, "GQA group %d (built for 1, 2, 4, 8)", g);
+  if (static_cast<long long>(L->num_blocks) * kBlockSize > (1LL << 40))
+    return fail(PA_ERR_INVALID, "num_blocks %d too large", L->num_blocks);
+  return PA_OK;
+}
+
+// KV blocks per split: about 128 KiB of K+V per work unit.
+int blocks_per_split(const pa_layout* L) {
+  const int block_kv_bytes = 2 * kBlockSize * L->head_size * elem_bytes(L->dtype);
+  int b = (128 * 1024) / block_kv_bytes;
+  return b < 1 ? 1 : b;
+}
+
+int small_positions(const pa_layout* L) { return kSmallRows / (L->num_q_heads / L->num_kv_heads); }
+
+Capacity capacity(const pa_layout* L, int B, int T, int max_seq_len) {
+  Capacity c{};
+  const long long max_nb = cdiv(max_seq_len, kBlockSize);
+  const long long splits = cdiv(max_nb, blocks_per_split(L));
+  const long long multi = T > B ? (T - B < B ? T - B : B) : 0;  // requests with q_len >= 2
+  c.decode_tiles = B;
+  c.decode_items = static_cast<long long>(B) * splits;
+  c.small_tiles = (T > B ? cdiv(T - B, small_positions(L)) : 0) + multi;
+  c.small_items = c.small_tiles * splits;
+  c.prefill_tiles = 0;
+  return c;
+}
+
+size_t align256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
+
+int num_sms_of_current_device(int* out) {
+  static int cache[64] = {0};
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return fail_cuda(e, "cudaGetDevice");
+  if (dev < 0 || dev >= 64) return fail(PA_ERR_CUDA, "device ordinal %d", dev);
+  if (!cache[dev]) {
+    int n = 0;
+    e = cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
+    if (e != cudaSuccess) return fail_cuda(e, "cudaDeviceGetAttribute");
+    cache[dev] = n;
+  }
+  *out = cache[dev];
+  return PA_OK;
+}
+
+}  // namespace
+
+WsLayout ws_layout(const Capacity& cap, int B, int Hkv, int D, int group) {
+  WsLayout w{};
+  size_t off = 0;
+  auto take = [&](size_t bytes) { size_t o = off; off = align256(off + bytes); return o; };
+  const size_t rows_d = static_cast<size_t>(group);
+  const size_t rows_s = static_cast<size_t>(kSmallRows);
+  w.hdr = take(kHdrWords * sizeof(int));
+  w.req_class = take(sizeof(int) * B);
+  w.pfx_d_items = take(sizeof(int) * (B + 1));
+  w.pfx_d_tiles = take(sizeof(int) * (B + 1));
+  w.pfx_s_items = take(sizeof(int) * (B + 1));
+  w.pfx_s_tiles = take(sizeof(int) * (B + 1));
+  w.pfx_p_tiles = take(sizeof(int) * (B + 1));
+  w.items_d = take(sizeof(int4) * cap.decode_items);
+  w.tiles_d = take(sizeof(int2) * cap.decode_tiles);
+  w.items_s = take(sizeof(int4) * cap.small_items);
+  w.tiles_s = take(sizeof(int2) * cap.small_tiles);
+  w.tiles_p = take(sizeof(int4) * cap.prefill_tiles);
+  w.cnt_d = take(sizeof(int) * cap.decode_tiles * Hkv);
+  w.cnt_s = take(sizeof(int) * cap.small_tiles * Hkv);
+  w.part_acc_d = take(sizeof(float) * cap.decode_items * Hkv * rows_d * D);
+  w.part_ml_d = take(sizeof(float) * cap.decode_items * Hkv * rows_d * 2);
+  w.part_acc_s = take(sizeof(float) * cap.small_items * Hkv * rows_s * D);
+  w.part_ml_s = take(sizeof(float) * cap.small_items * Hkv * rows_s * 2);
+  w.total = off;
+  return w;
+}
+
+}  // namespace pa
+
+using namespace pa;
+
+extern "C" {
+
+const char* pa_last_error(void) { return g_last_error.c_str(); }
+
+int pa_version(void) { return 100; }
+
+int pa_set_profile_events(void* start, void* stop) {
+  g_prof_start = static_cast<cudaEvent_t>(start);
+  g_prof_stop = static_cast<cudaEvent_t>(stop);
+  return PA_OK;
+}
+
+int pa_cache_write(const void* k, const void* v, const int64_t* slot_mapping, int num_tokens,
+                   void* k_cache, void* v_cache, const pa_layout* layout, int32_t* status,
+                   void* stream) {
+  g_last_error.clear();
+  if (int rc = check_layout(layout)) return rc;
+  if (num_tokens < 0) return fail(PA_ERR_INVALID, "num_tokens %d < 0", num_tokens);
+  if (num_tokens == 0) return PA_OK;
+  if (!k || !v || !slot_mapping || !k_cache || !v_cache)
+    return fail(PA_ERR_INVALID, "null tensor pointer");
+  if (!aligned(k, 16) || !aligned(v, 16) || !aligned(k_cache, 16) || !aligned(v_cache, 16))
+    return fail(PA_ERR_INVALID, "k, v, k_cache and v_cache must be 16-byte aligned");
+  if (!aligned(slot_mapping, 8)) return fail(PA_ERR_INVALID, "slot_mapping must be 8-byte aligned");
+  if (status && !aligned(status, 4)) return fail(PA_ERR_INVALID, "status must be 4-byte aligned");
+  const int row_bytes = layout->num_kv_heads * layout->head_size * elem_bytes(layout->dtype);
+  const long long num_slots = static_cast<long long>(layout->num_blocks) * kBlockSize;
+  cudaError_t e = launch_cache_write(k, v, slot_mapping, num_tokens, k_cache, v_cache, row_bytes,
+                                     num_slots, status, static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return fail_cuda(e, "cache write launch");
+  return PA_OK;
+}
+
+size_t pa_forward_workspace_size(const pa_layout* layout, int num_seqs, int num_tokens,
+                                 int max_seq_len) {
+  g_last_error.clear();
+  if (check_layout(layout)) return 0;
+  if (num_seqs < 0 || num_tokens < 0 || max_seq_len < 0) {
+    fail(PA_ERR_INVALID, "negative size");
+    return 0;
+  }
+  const Capacity cap = capacity(layout, num_seqs, num_tokens, max_seq_len);
+  return ws_layout(cap, num_seqs, layout->num_kv_heads, layout->head_size,
+                   layout->num_q_heads / layout->num_kv_heads)
+      .total;
+}
+
+int pa_forward(const void* q, const void* k_cache, const void* v_cache,
+               const int32_t* block_tables, int max_blocks_per_seq, const int32_t* seq_lens,
+               const int32_t* query_start_loc, int num_seqs, int num_tokens, int max_query_len,
+               int max_seq_len, float scale, void* out, void* workspace, size_t workspace_bytes,
+               const pa_layout* layout, int32_t* status, void* stream) {
+  g_last_error.clear();
+  if (int rc = check_layout(layout)) return rc;
+  if (num_seqs < 0 || num_tokens < 0 || max_query_len < 0 || max_seq_len < 0 ||
+      max_blocks_per_seq < 0)
+    return fail(PA_ERR_INVALID, "negative size argument");
+  if (num_seqs == 0 || num_tokens == 0) return PA_OK;
+  if (!q || !k_cache || !v_cache || !block_tables || !seq_lens || !query_start_loc || !out ||
+      !workspace)
+    return fail(PA_ERR_INVALID, "null pointer argument");
+  if (!aligned(q, 16) || !aligned(out, 16) || !aligned(k_cache, 16) || !aligned(v_cache, 16))
+    return fail(PA_ERR_INVALID, "q, out, k_cache and v_cache must be 16-byte aligned");
+  if (!aligned(block_tables, 4) || !aligned(seq_lens, 4) || !aligned(query_start_loc, 4))
+    return fail(PA_ERR_INVALID, "int32 arrays must be 4-byte aligned");
+  if (!aligned(workspace, 256)) return fail(PA_ERR_INVALID, "workspace must be 256-byte aligned");
+  if (status && !aligned(status, 4)) return fail(PA_ERR_INVALID, "status must be 4-byte aligned");
+  if (!std::isfinite(scale)) return fail(PA_ERR_INVALID, "scale is not finite");
+  if (max_query_len < 1 || max_seq_len < 1)
+    return fail(PA_ERR_INVALID, "max_query_len and max_seq_len must be >= 1");
+  if (cdiv(max_seq_len, kBlockSize) > max_blocks_per_seq)
+    return fail(PA_ERR_INVALID, "max_blocks_per_seq %d < ceil(max_seq_len / 16) = %lld",
+                max_blocks_per_seq, cdiv(max_seq_len, kBlockSize));
+  if (num_tokens < num_seqs)
+    return fail(PA_ERR_INVALID, "num_tokens %d < num_seqs %d: every request needs a new token",
+                num_tokens, num_seqs);
+  const int group = layout->num_q_heads / layout->num_kv_heads;
+  const Capacity cap = capacity(layout, num_seqs, num_tokens, max_seq_len);
+  if (cap.decode_items > (1LL << 30) || cap.small_items > (1LL << 30))
+    return fail(PA_ERR_INVALID, "step too large for one call");
+  const WsLayout lay = ws_layout(cap, num_seqs, layout->num_kv_heads, layout->head_size, group);
+  if (workspace_bytes < lay.total)
+    return fail(PA_ERR_INVALID, "workspace of %zu bytes < %zu needed", workspace_bytes, lay.total);
+  int num_sms = 0;
+  if (int rc = num_sms_of_current_device(&num_sms)) return rc;
+
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  char* ws = static_cast<char*>(workspace);
+  int* hdr = reinterpret_cast<int*>(ws + lay.hdr);
+
+  PlanParams pp{};
+  pp.seq_lens = seq_lens;
+  pp.qsl = query_start_loc;
+  pp.num_seqs = num_seqs;
+  pp.num_tokens = num_tokens;
+  pp.max_query_len = max_query_len;
+  pp.max_seq_len = max_seq_len;
+  pp.max_blocks_per_seq = max_blocks_per_seq;
+  pp.bps = blocks_per_split(layout);
+  pp.small_positions = small_positions(layout);
+  pp.prefill_min_qlen = 0x7fffffff;
+  pp.prefill_rows = 128;
+  pp.group = group;
+  pp.num_kv_heads = layout->num_kv_heads;
+  pp.cap = cap;
+  pp.ws = ws;
+  pp.lay = lay;
+  pp.status = status;
+  cudaError_t e = launch_plan(pp, st);
+  if (e != cudaSuccess) return fail_cuda(e, "plan launch");
+
+  AttnParams ap{};
+  ap.q = q;
+  ap.k_cache = k_cache;
+  ap.v_cache = v_cache;
+  ap.block_tables = block_tables;
+  ap.seq_lens = seq_lens;
+  ap.qsl = query_start_loc;
+  ap.out = out;
+  ap.max_blocks_per_seq = max_blocks_per_seq;
+  ap.num_q_heads = layout->num_q_heads;
+  ap.num_kv_heads = layout->num_kv_heads;
+  ap.num_blocks = layout->num_blocks;
+  ap.num_tokens = num_tokens;
+  ap.bps = pp.bps;
+  ap.scale_log2 = scale * 1.4426950408889634f;
+  ap.status = status;
+
+  // decode rows (q_len == 1)
+  ap.n_items = hdr + kHdrDecodeItems;
+  ap.next = hdr + kHdrDecodeNext;
+  ap.items = reinterpret_cast<const int4*>(ws + lay.items_d);
+  ap.tiles = reinterpret_cast<const int2*>(ws + lay.tiles_d);
+  ap.merge_cnt = reinterpret_cast<int*>(ws + lay.cnt_d);
+  ap.part_acc = reinterpret_cast<float*>(ws + lay.part_acc_d);
+  ap.part_ml = reinterpret_cast<float*>(ws + lay.part_ml_d);
+  if (g_prof_start) cudaEventRecord(g_prof_start, st);
+  e = launch_attn_cuda_core(ap, layout->dtype, layout->head_size, group, 1, num_sms, st);
+  if (e != cudaSuccess) return fail_cuda(e, "decode attention launch");
+  if (g_prof_stop) cudaEventRecord(g_prof_stop, st);
+
+  if (max_query_len > 1) {
+    ap.n_items = hdr + kHdrSmallItems;
+    ap.next = hdr + kHdrSmallNext;
+    ap.items = reinterpret_cast<const int4*>(ws + lay.items_s);
+    ap.tiles = reinterpret_cast<const int2*>(ws + lay.tiles_s);
+    ap.merge_cnt = reinterpret_cast<int*>(ws + lay.cnt_s);
+    ap.part_acc = reinterpret_cast<float*>(ws + lay.part_acc_s);
+    ap.part_ml = reinterpret_cast<float*>(ws + lay.part_ml_s);
+    e = launch_attn_cuda_core(ap, layout->dtype, layout->head_size, group, small_positions(layout),
+                              num_sms, st);
+    if (e != cudaSuccess) return fail_cuda(e, "small-q attention launch");
+  }
+  return PA_OK;
+}
+
+}  // extern "C"

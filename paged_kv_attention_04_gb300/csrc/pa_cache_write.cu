@@ -1,0 +1,54 @@
+// reshape_and_cache: scatter each new token's K and V row into its paged slot.
+//
+// "Inside vLLM: Anatomy of a High-Throughput LLM Inference System", section
+// Run forward pass: slot_mapping is built with the inputs, and section Prefix
+// Caching: the forward pass fills the allocated blocks with the new KVs.
+//
+// With the cache laid out [num_blocks][16][Hkv][D], slot s = block*16 + row
+// names one contiguous row of Hkv*D elements, so the write is a row copy:
+// every thread moves one 16-byte chunk of K and the same chunk of V with
+// 128-bit loads and stores.  Bits are copied unchanged.
+#include "pa_device.cuh"
+#include "pa_internal.h"
+
+namespace pa {
+
+__global__ void __launch_bounds__(256) cache_write_kernel(
+    const uint4* __restrict__ k, const uint4* __restrict__ v, const int64_t* __restrict__ slots,
+    int num_tokens, uint4* __restrict__ k_cache, uint4* __restrict__ v_cache, int row_chunks,
+    long long num_slots, int32_t* status) {
+  const long long total = static_cast<long long>(num_tokens) * row_chunks;
+  for (long long i = blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x; i < total;
+       i += static_cast<long long>(gridDim.x) * blockDim.x) {
+    const int t = static_cast<int>(i / row_chunks);
+    const int c = static_cast<int>(i - static_cast<long long>(t) * row_chunks);
+    const int64_t s = __ldg(slots + t);
+    if (s < 0) continue;
+    if (s >= num_slots) {
+      if (c == 0) flag_error(status, PA_DEV_SLOT_RANGE);
+      continue;
+    }
+    const long long src = static_cast<long long>(t) * row_chunks + c;
+    const long long dst = s * row_chunks + c;
+    const uint4 kk = __ldg(k + src);
+    const uint4 vv = __ldg(v + src);
+    k_cache[dst] = kk;
+    v_cache[dst] = vv;
+  }
+}
+
+cudaError_t launch_cache_write(const void* k, const void* v, const int64_t* slot_mapping,
+                               int num_tokens, void* k_cache, void* v_cache, int row_bytes,
+                               long long num_slots, int32_t* status, cudaStream_t stream) {
+  const int row_chunks = row_bytes / 16;
+  const long long total = static_cast<long long>(num_tokens) * row_chunks;
+  const int threads = 256;
+  long long blocks = (total + threads - 1) / threads;
+  if (blocks > 65535LL * 64) blocks = 65535LL * 64;
+  cache_write_kernel<<<static_cast<unsigned>(blocks), threads, 0, stream>>>(
+      static_cast<const uint4*>(k), static_cast<const uint4*>(v), slot_mapping, num_tokens,
+      static_cast<uint4*>(k_cache), static_cast<uint4*>(v_cache), row_chunks, num_slots, status);
+  return cudaGetLastError();
+}
+
+}  // namespace pa

@@ -1,0 +1,94 @@
+// Internal declarations shared by the host API and the kernels of libpa.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "../../include/pa.h"
+
+namespace pa {
+
+constexpr int kBlockSize = 16;        // tokens per KV block
+constexpr int kSmallRows = 16;        // query rows (positions x grouped heads) per CUDA-core tile
+
+// Work-list classes written by the plan kernel.
+enum ReqClass : int { kClassNone = 0, kClassDecode = 1, kClassSmall = 2, kClassPrefill = 3 };
+
+// Header words at the start of the workspace.
+enum Hdr : int {
+  kHdrDecodeItems = 0, kHdrDecodeTiles, kHdrDecodeNext,
+  kHdrSmallItems, kHdrSmallTiles, kHdrSmallNext,
+  kHdrPrefillTiles, kHdrPrefillNext,
+  kHdrWords = 16
+};
+
+// Capacities (host upper bounds) for one step.
+struct Capacity {
+  long long decode_items, decode_tiles;
+  long long small_items, small_tiles;
+  long long prefill_tiles;
+};
+
+// Byte offsets of every workspace region (all 256-byte aligned).
+struct WsLayout {
+  size_t hdr, req_class, pfx_d_items, pfx_d_tiles, pfx_s_items, pfx_s_tiles, pfx_p_tiles;
+  size_t items_d, tiles_d, items_s, tiles_s, tiles_p;
+  size_t cnt_d, cnt_s;
+  size_t part_acc_d, part_ml_d, part_acc_s, part_ml_s;
+  size_t total;
+};
+
+struct PlanParams {
+  const int32_t* seq_lens;
+  const int32_t* qsl;
+  int num_seqs, num_tokens, max_query_len, max_seq_len, max_blocks_per_seq;
+  int bps;              // KV blocks per split
+  int small_positions;  // query positions per small-q tile
+  int prefill_min_qlen; // requests with q_len >= this go to the tensor-core kernel
+  int prefill_rows;     // query rows (positions x group) per prefill tile
+  int group;            // num_q_heads / num_kv_heads
+  int num_kv_heads;
+  Capacity cap;
+  char* ws;
+  WsLayout lay;
+  int32_t* status;
+};
+
+// One unit of CUDA-core attention work: request r, query tile m, KV split s,
+// and the tile's global index (for the split merge).
+struct AttnParams {
+  const void* q;
+  const void* k_cache;
+  const void* v_cache;
+  const int32_t* block_tables;
+  const int32_t* seq_lens;
+  const int32_t* qsl;
+  void* out;
+  int max_blocks_per_seq;
+  int num_q_heads, num_kv_heads, num_blocks, num_tokens;
+  int bps;
+  float scale_log2;      // softmax scale * log2(e)
+  const int* n_items;    // device count of work items (x num_kv_heads units)
+  int* next;             // device work counter (zeroed by the plan kernel)
+  const int4* items;     // {r, m, s, tile}
+  const int2* tiles;     // {first item, number of splits}
+  int* merge_cnt;        // [tiles][num_kv_heads]
+  float* part_acc;       // [items][num_kv_heads][rows][D]
+  float* part_ml;        // [items][num_kv_heads][rows][2]
+  int32_t* status;
+};
+
+WsLayout ws_layout(const Capacity& cap, int num_seqs, int num_kv_heads, int head_size,
+                   int group);
+
+// Kernel launchers (return cudaError_t of the launch).
+cudaError_t launch_cache_write(const void* k, const void* v, const int64_t* slot_mapping,
+                               int num_tokens, void* k_cache, void* v_cache, int row_bytes,
+                               long long num_slots, int32_t* status, cudaStream_t stream);
+cudaError_t launch_plan(const PlanParams& p, cudaStream_t stream);
+// CUDA-core split-KV attention.  positions: 1 (decode list) or the small-q
+// tile height.  Returns cudaErrorInvalidValue for an unbuilt combination.
+cudaError_t launch_attn_cuda_core(const AttnParams& p, pa_dtype dtype, int head_size, int group,
+                                  int positions, int num_sms, cudaStream_t stream);
+
+}  // namespace pa

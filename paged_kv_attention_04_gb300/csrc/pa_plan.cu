@@ -1,0 +1,210 @@
+// Step planning on the device: no host<->device copy is needed to split the
+// step's requests into work.
+//
+// The step is one flattened super-sequence: decodes first, then prefill
+// chunks ("Serving models at scale with vLLM", section Chunked prefill;
+// "Inside vLLM", section Run forward pass).  One CTA reads seq_lens and
+// query_start_loc, checks them, sorts every request into a class
+//   decode   q_len == 1
+//   small    1 < q_len < prefill_min_qlen (CUDA-core tiles of a few positions)
+//   prefill  q_len >= prefill_min_qlen   (tensor-core tiles)
+// and writes the work lists the attention kernels consume, plus zeroed
+// per-tile split counters.  A decode or small tile whose KV is longer than
+// `bps` blocks is split into several items whose partial softmax states are
+// merged by the last item to finish.
+#include <climits>
+
+#include "pa_device.cuh"
+#include "pa_internal.h"
+
+namespace pa {
+
+namespace {
+
+constexpr int kPlanThreads = 1024;
+
+// Exclusive scan of one int per thread across the CTA; returns the CTA total.
+__device__ int block_exclusive_scan(int v, int* warp_sums, int& total) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  int x = v;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int y = __shfl_up_sync(0xffffffffu, x, o);
+    if (lane >= o) x += y;
+  }
+  if (lane == 31) warp_sums[warp] = x;
+  __syncthreads();
+  if (warp == 0) {
+    int w = (lane < (kPlanThreads / 32)) ? warp_sums[lane] : 0;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int y = __shfl_up_sync(0xffffffffu, w, o);
+      if (lane >= o) w += y;
+    }
+    warp_sums[lane] = w;  // inclusive
+  }
+  __syncthreads();
+  const int before = (warp > 0 ? warp_sums[warp - 1] : 0) + x - v;
+  total = warp_sums[kPlanThreads / 32 - 1];
+  __syncthreads();
+  return before;
+}
+
+__device__ __forceinline__ int ceil_div(int a, int b) { return (a + b - 1) / b; }
+
+// Number of KV splits of a tile whose last query row sits at position pos_last.
+__device__ __forceinline__ int splits_for(int pos_last, int bps) {
+  return ceil_div(ceil_div(pos_last + 1, kBlockSize), bps);
+}
+
+// Largest r with pfx[r] <= i (pfx nondecreasing, pfx[0] = 0).
+__device__ int find_owner(const int* pfx, int n, int i) {
+  int lo = 0, hi = n - 1;
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) >> 1;
+    if (pfx[mid] <= i) lo = mid; else hi = mid - 1;
+  }
+  return lo;
+}
+
+}  // namespace
+
+__global__ void __launch_bounds__(kPlanThreads, 1) plan_kernel(PlanParams p) {
+  __shared__ int warp_sums[32];
+  __shared__ int carry[5];
+  __shared__ int err;
+  const int B = p.num_seqs;
+  char* ws = p.ws;
+  int* hdr = reinterpret_cast<int*>(ws + p.lay.hdr);
+  int* cls = reinterpret_cast<int*>(ws + p.lay.req_class);
+  int* pfx_di = reinterpret_cast<int*>(ws + p.lay.pfx_d_items);
+  int* pfx_dt = reinterpret_cast<int*>(ws + p.lay.pfx_d_tiles);
+  int* pfx_si = reinterpret_cast<int*>(ws + p.lay.pfx_s_items);
+  int* pfx_st = reinterpret_cast<int*>(ws + p.lay.pfx_s_tiles);
+  int* pfx_pt = reinterpret_cast<int*>(ws + p.lay.pfx_p_tiles);
+  int4* items_d = reinterpret_cast<int4*>(ws + p.lay.items_d);
+  int2* tiles_d = reinterpret_cast<int2*>(ws + p.lay.tiles_d);
+  int4* items_s = reinterpret_cast<int4*>(ws + p.lay.items_s);
+  int2* tiles_s = reinterpret_cast<int2*>(ws + p.lay.tiles_s);
+  int* cnt_d = reinterpret_cast<int*>(ws + p.lay.cnt_d);
+  int* cnt_s = reinterpret_cast<int*>(ws + p.lay.cnt_s);
+
+  if (threadIdx.x == 0) {
+    err = 0;
+    for (int i = 0; i < 5; ++i) carry[i] = 0;
+    const int q0 = __ldg(p.qsl), qB = __ldg(p.qsl + B);
+    if (q0 != 0 || qB != p.num_tokens) err |= PA_DEV_QSL;
+  }
+  __syncthreads();
+
+  // Pass 1: classify and count, with a running exclusive scan per list.
+  for (int base = 0; base < B; base += kPlanThreads) {
+    const int r = base + threadIdx.x;
+    int c = kClassNone, nd_items = 0, nd_tiles = 0, ns_items = 0, ns_tiles = 0, np_tiles = 0;
+    if (r < B) {
+      const int S = __ldg(p.seq_lens + r);
+      const int a = __ldg(p.qsl + r), b = __ldg(p.qsl + r + 1);
+      const int L = b - a;
+      int e = 0;
+      if (L < 0 || a < 0 || b > p.num_tokens) e |= PA_DEV_QSL;
+      else if (L < 1 || L > S || S > p.max_seq_len || L > p.max_query_len ||
+               ceil_div(S, kBlockSize) > p.max_blocks_per_seq)
+        e |= PA_DEV_LENGTHS;
+      if (e) {
+        atomicOr(&err, e);
+      } else if (L == 1) {
+        c = kClassDecode;
+        nd_tiles = 1;
+        nd_items = splits_for(S - 1, p.bps);
+      } else if (L >= p.prefill_min_qlen) {
+        c = kClassPrefill;
+        np_tiles = ceil_div(L * p.group, p.prefill_rows);
+      } else {
+        c = kClassSmall;
+        ns_tiles = ceil_div(L, p.small_positions);
+        for (int m = 0; m < ns_tiles; ++m) {
+          const int last = min(L, (m + 1) * p.small_positions) - 1;
+          ns_items += splits_for(S - L + last, p.bps);
+        }
+      }
+      cls[r] = c;
+    }
+    int tot;
+    const int o_di = block_exclusive_scan(nd_items, warp_sums, tot);
+    const int c_di = carry[0]; __syncthreads(); if (threadIdx.x == 0) carry[0] += tot;
+    const int o_dt = block_exclusive_scan(nd_tiles, warp_sums, tot);
+    const int c_dt = carry[1]; __syncthreads(); if (threadIdx.x == 0) carry[1] += tot;
+    const int o_si = block_exclusive_scan(ns_items, warp_sums, tot);
+    const int c_si = carry[2]; __syncthreads(); if (threadIdx.x == 0) carry[2] += tot;
+    const int o_st = block_exclusive_scan(ns_tiles, warp_sums, tot);
+    const int c_st = carry[3]; __syncthreads(); if (threadIdx.x == 0) carry[3] += tot;
+    const int o_pt = block_exclusive_scan(np_tiles, warp_sums, tot);
+    const int c_pt = carry[4]; __syncthreads(); if (threadIdx.x == 0) carry[4] += tot;
+    if (r < B) {
+      pfx_di[r] = c_di + o_di; pfx_dt[r] = c_dt + o_dt;
+      pfx_si[r] = c_si + o_si; pfx_st[r] = c_st + o_st;
+      pfx_pt[r] = c_pt + o_pt;
+    }
+    __syncthreads();
+  }
+  if (threadIdx.x == 0) {
+    pfx_di[B] = carry[0]; pfx_dt[B] = carry[1]; pfx_si[B] = carry[2];
+    pfx_st[B] = carry[3]; pfx_pt[B] = carry[4];
+    if (carry[0] > p.cap.decode_items || carry[1] > p.cap.decode_tiles ||
+        carry[2] > p.cap.small_items || carry[3] > p.cap.small_tiles ||
+        carry[4] > p.cap.prefill_tiles)
+      err |= PA_DEV_CAPACITY;
+  }
+  __syncthreads();
+  if (err & (PA_DEV_CAPACITY | PA_DEV_QSL)) {
+    // Nothing is safe to schedule: publish empty lists.
+    if (threadIdx.x == 0) {
+      for (int i = 0; i < kHdrWords; ++i) hdr[i] = 0;
+      flag_error(p.status, err);
+    }
+    return;
+  }
+  const int n_di = carry[0], n_dt = carry[1], n_si = carry[2], n_st = carry[3], n_pt = carry[4];
+
+  // Pass 2: decode items, one split of one request each.
+  for (int i = threadIdx.x; i < n_di; i += kPlanThreads) {
+    const int r = find_owner(pfx_di, B, i);
+    const int s = i - pfx_di[r];
+    const int tile = pfx_dt[r];
+    items_d[i] = make_int4(r, 0, s, tile);
+    if (s == 0) tiles_d[tile] = make_int2(i, pfx_di[r + 1] - pfx_di[r]);
+  }
+  // Small-q tiles: each thread expands one tile into its splits.
+  for (int tile = threadIdx.x; tile < n_st; tile += kPlanThreads) {
+    const int r = find_owner(pfx_st, B, tile);
+    const int m = tile - pfx_st[r];
+    const int S = __ldg(p.seq_lens + r);
+    const int L = __ldg(p.qsl + r + 1) - __ldg(p.qsl + r);
+    int first = pfx_si[r];
+    for (int mm = 0; mm < m; ++mm)
+      first += splits_for(S - L + min(L, (mm + 1) * p.small_positions) - 1, p.bps);
+    const int ns = splits_for(S - L + min(L, (m + 1) * p.small_positions) - 1, p.bps);
+    for (int s = 0; s < ns; ++s) items_s[first + s] = make_int4(r, m, s, tile);
+    tiles_s[tile] = make_int2(first, ns);
+  }
+  for (int i = threadIdx.x; i < n_dt * p.num_kv_heads; i += kPlanThreads) cnt_d[i] = 0;
+  for (int i = threadIdx.x; i < n_st * p.num_kv_heads; i += kPlanThreads) cnt_s[i] = 0;
+  if (threadIdx.x == 0) {
+    hdr[kHdrDecodeItems] = n_di;
+    hdr[kHdrDecodeTiles] = n_dt;
+    hdr[kHdrDecodeNext] = 0;
+    hdr[kHdrSmallItems] = n_si;
+    hdr[kHdrSmallTiles] = n_st;
+    hdr[kHdrSmallNext] = 0;
+    hdr[kHdrPrefillTiles] = n_pt;
+    hdr[kHdrPrefillNext] = 0;
+    if (err) flag_error(p.status, err);
+  }
+}
+
+cudaError_t launch_plan(const PlanParams& p, cudaStream_t stream) {
+  plan_kernel<<<1, kPlanThreads, 0, stream>>>(p);
+  return cudaGetLastError();
+}
+
+}  // namespace pa

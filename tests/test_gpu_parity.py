@@ -1,0 +1,175 @@
+"""GPU parity: libpa against the fp64 oracle on the same seeded inputs.
+
+Cache writes must match bit for bit (the whole cache, so untouched slots are
+checked too); attention must satisfy |gpu - oracle| <= atol + rtol*|oracle|
+elementwise with (atol, rtol) = (1e-2, 2e-2) for bf16 and (1e-5, 1e-5) for
+fp32.  Every launch goes through the C ABI."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import paged_kv_attention_04_gb300 as P
+from paged_kv_attention_04_gb300 import workloads as W
+
+from helpers import assert_close, bits, raw_bits, run_gpu, run_oracle
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    from paged_kv_attention_04_gb300 import build
+    build.build()
+    P.lib()
+
+
+def _full_parity(step_cpu):
+    step = step_cpu.to("cuda")
+    out, kc, vc, status = run_gpu(step)
+    assert status == 0
+    ref, rkc, rvc = run_oracle(step_cpu)
+    assert np.array_equal(raw_bits(kc), rkc.view(np.uint32) if rkc.dtype == np.float32 else rkc)
+    assert np.array_equal(raw_bits(vc), rvc.view(np.uint32) if rvc.dtype == np.float32 else rvc)
+    return assert_close(out, ref, step_cpu.spec.dtype, step_cpu.spec.name)
+
+
+@pytest.mark.parametrize("name", ["tiny_decode_f32", "tinyllama_decode", "llama3_8b_decode",
+                                  "mixed_step"])
+def test_config_full_parity(name):
+    _full_parity(W.make_config(name))
+
+
+def test_long_context_sampled_parity():
+    """Long-context decode at full size (a ~9 GB pool): the whole cache write
+    is checked, attention on sampled rows the oracle evaluates one by one."""
+    spec = W.spec_long_context_decode()
+    step = W.make_step(spec, device="cuda")
+    out, kc, vc, status = run_gpu(step)
+    assert status == 0
+    slots = step.slot_mapping
+    # written rows hold the new tokens' bits; every other row is unchanged
+    NBS = step.num_blocks * 16
+    for cache, orig, new in ((kc, step.k_cache, step.k), (vc, step.v_cache, step.v)):
+        flat = cache.view(NBS, -1).view(torch.int16)
+        assert torch.equal(flat[slots], new.reshape(len(slots), -1).view(torch.int16))
+        restored = flat.clone()
+        restored[slots] = orig.view(NBS, -1).view(torch.int16)[slots]
+        assert torch.equal(restored, orig.view(NBS, -1).view(torch.int16))
+        del restored
+    # oracle on sampled rows, over a private copy of each request's blocks
+    bt = step.block_tables.cpu().numpy()
+    S_all = spec.seq_lens
+    for r, h in ((int(np.argmin(S_all)), 0), (int(np.argmax(S_all)), 31), (5, 13)):
+        S = int(S_all[r])
+        nb = oracle.blocks_needed(S)
+        blocks = torch.from_numpy(bt[r, :nb].astype(np.int64)).cuda()
+        mk = bits(step.k_cache[blocks])
+        mv = bits(step.v_cache[blocks])
+        pos = S - 1
+        slot = (pos // 16) * 16 + pos % 16
+        mk, mv = oracle.cache_write(bits(step.k[r:r + 1]), bits(step.v[r:r + 1]),
+                                    np.array([slot]), mk, mv)
+        ref = oracle.paged_attention_rows(bits(step.q[r:r + 1]), mk, mv, np.arange(nb)[None, :],
+                                          np.array([S]), np.array([0, 1]), step.scale,
+                                          spec.num_kv_heads, [(0, h)])
+        assert_close(out[r, h], ref[0], "bf16", f"long-context r={r} h={h}")
+        del mk, mv
+
+
+SHAPES = [
+    # (q_lens, seq_lens): decode lengths at block edges, splits, chunks, a 1-token prompt
+    ([1, 1, 1, 1, 1, 1], [1, 15, 16, 17, 300, 1000]),
+    ([3, 1, 16, 40, 1], [17, 33, 40, 300, 2]),
+    ([7, 1, 25], [500, 257, 25]),
+]
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "f32"])
+@pytest.mark.parametrize("D", [64, 128])
+@pytest.mark.parametrize("G", [1, 2, 4, 8])
+@pytest.mark.parametrize("shape", range(len(SHAPES)))
+def test_random_shapes(dtype, D, G, shape):
+    q_lens, seq_lens = SHAPES[shape]
+    Hkv = 2
+    spec = W.custom_spec(f"rand-{dtype}-{D}-{G}-{shape}", dtype, Hkv * G, Hkv, D, q_lens, seq_lens,
+                         seed=100 + shape * 17 + D + G)
+    _full_parity(W.make_step(spec))
+
+
+def test_prefix_sharing_and_permutation_invariance():
+    """Outputs are bit-identical when the physical blocks are renumbered (data
+    moved with them), including blocks shared by several tables."""
+    spec = W.custom_spec("perm", "bf16", 8, 2, 128, [1, 1, 1, 4], [40, 90, 200, 64],
+                         shared_prefix_blocks=2, sharing=[True, True, True, False], seed=9)
+    st = W.make_step(spec, device="cuda")
+    out1, *_ = run_gpu(st)
+    NB = st.num_blocks
+    perm = torch.randperm(NB, generator=torch.Generator().manual_seed(4)).cuda()
+    st2 = W.make_step(spec, device="cuda")
+    st2.k_cache = torch.empty_like(st.k_cache)
+    st2.v_cache = torch.empty_like(st.v_cache)
+    st2.k_cache[perm] = st.k_cache
+    st2.v_cache[perm] = st.v_cache
+    bt = st.block_tables.long()
+    st2.block_tables = torch.where(bt >= 0, perm[bt.clamp(min=0)], bt).int()
+    st2.slot_mapping = perm[st.slot_mapping // 16] * 16 + st.slot_mapping % 16
+    out2, *_ = run_gpu(st2)
+    assert torch.equal(out1.view(torch.int16), out2.view(torch.int16))
+
+
+def test_batch_invariance_and_determinism():
+    spec = W.custom_spec("batch", "bf16", 32, 8, 128, [1, 5, 1, 1], [700, 64, 3000, 16], seed=21)
+    st = W.make_step(spec, device="cuda")
+    out, *_ = run_gpu(st)
+    again, *_ = run_gpu(st)
+    assert torch.equal(out.view(torch.int16), again.view(torch.int16))
+    qsl = st.query_start_loc.tolist()
+    for r in range(4):
+        solo = W.custom_spec("solo", "bf16", 32, 8, 128, [spec.q_lens[r]], [spec.seq_lens[r]], seed=21)
+        s1 = W.make_step(solo, device="cuda")
+        s1.k_cache, s1.v_cache = st.k_cache, st.v_cache
+        s1.block_tables = st.block_tables[r:r + 1].contiguous()
+        s1.q = st.q[qsl[r]:qsl[r + 1]].contiguous()
+        s1.k = st.k[qsl[r]:qsl[r + 1]].contiguous()
+        s1.v = st.v[qsl[r]:qsl[r + 1]].contiguous()
+        s1.slot_mapping = st.slot_mapping[qsl[r]:qsl[r + 1]].contiguous()
+        o1, *_ = run_gpu(s1)
+        assert torch.equal(o1.view(torch.int16), out[qsl[r]:qsl[r + 1]].view(torch.int16))
+
+
+def test_chunked_prefill_matches_whole_prompt():
+    """A prompt run as chunks (each written, then attended) matches the whole
+    prompt run at once, within tolerance of the oracle."""
+    n, chunks = 600, (256, 256, 88)
+    spec = W.custom_spec("whole", "bf16", 16, 4, 128, [n], [n], seed=31)
+    st = W.make_step(spec, device="cuda")
+    whole, *_ = run_gpu(st)
+    kc, vc = st.k_cache.clone(), st.v_cache.clone()
+    lay = P.layout_of(kc, 16)
+    done, parts = 0, []
+    for c in chunks:
+        sl = slice(done, done + c)
+        P.pa_cache_write(st.k[sl], st.v[sl], st.slot_mapping[sl], kc, vc, lay)
+        sq = torch.tensor([done + c], dtype=torch.int32, device="cuda")
+        qsl = torch.tensor([0, c], dtype=torch.int32, device="cuda")
+        ws = P.alloc_workspace(lay, 1, c, done + c)
+        o = torch.empty_like(st.q[sl])
+        P.pa_forward(st.q[sl].contiguous(), kc, vc, st.block_tables, sq, qsl, c, done + c, st.scale,
+                     o, ws, lay)
+        parts.append(o)
+        done += c
+    chunked = torch.cat(parts)
+    torch.cuda.synchronize()
+    ref, _, _ = run_oracle(st.to("cpu"))
+    assert_close(chunked, ref, "bf16", "chunked")
+    assert_close(whole, ref, "bf16", "whole")
+
+
+def test_empty_step_is_a_noop():
+    lay = P.make_layout(8, 2, 64, 4, torch.bfloat16)
+    kc = torch.zeros(4, 16, 2, 64, dtype=torch.bfloat16, device="cuda")
+    e = torch.empty(0, 2, 64, dtype=torch.bfloat16, device="cuda")
+    P.pa_cache_write(e, e, torch.empty(0, dtype=torch.int64, device="cuda"), kc, kc, lay)
+    torch.cuda.synchronize()
+    assert int(kc.abs().sum()) == 0
