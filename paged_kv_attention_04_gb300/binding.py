@@ -126,9 +126,18 @@ def pa_forward(q, k_cache, v_cache, block_tables, seq_lens, query_start_loc,
 
 def pa_set_profile_events(start: "torch.cuda.Event | None", stop: "torch.cuda.Event | None") -> None:
     """Record `start`/`stop` around the decode-attention kernel of later
-    pa_forward calls on this thread (None, None turns it off)."""
-    _check(lib().pa_set_profile_events(None if start is None else start.cuda_event,
-                                       None if stop is None else stop.cuda_event))
+    pa_forward calls on this thread (None, None turns it off).  torch creates
+    an event's CUDA handle on its first record, so unrecorded events are
+    recorded once here first."""
+    handles = []
+    for ev in (start, stop):
+        if ev is None:
+            handles.append(None)
+            continue
+        if not ev.cuda_event:
+            ev.record()
+        handles.append(ev.cuda_event)
+    _check(lib().pa_set_profile_events(handles[0], handles[1]))
 
 
 def alloc_workspace(layout: pa_layout, num_seqs: int, num_tokens: int, max_seq_len: int,
