@@ -147,6 +147,36 @@ int pa_forward(const void* q, const void* k_cache, const void* v_cache,
  */
 int pa_set_profile_events(void* start, void* stop);
 
+/*
+ * pa_forward without a caller-provided workspace, for callers that cannot
+ * allocate device memory.  The pages have no counterpart; this is a
+ * convenience of this library.  Who needs it: a serving engine that, at
+ * start-up, claimed nearly all free GPU memory for its KV-block pool (so a
+ * later cudaMalloc may fail), a plugin whose host framework owns all device
+ * memory and hands it no allocator, or a step loop that cannot afford the
+ * device synchronisation cudaMalloc/cudaFree may cause.
+ *
+ * Same arguments and results as pa_forward, minus workspace/workspace_bytes.
+ * The scratch is one file-scope device array of PA_STATIC_SCRATCH_BYTES
+ * inside the library: every GPU that loads the library holds it until the
+ * process exits.  A step whose pa_forward_workspace_size exceeds that is
+ * rejected with PA_ERR_INVALID before anything is launched.  The call makes
+ * no cudaMalloc/cudaFree or other allocation.
+ *
+ * The first call on each device looks up the array's device address
+ * (cudaGetSymbolAddress, with that device current); make that first call
+ * before any stream capture starts on the device.  All calls share the one
+ * array and each call re-initialises what it needs, but calls whose work
+ * overlaps on the GPU (other streams, other threads) race on it: order them.
+ */
+#define PA_STATIC_SCRATCH_BYTES ((size_t)32 << 20)
+int pa_forward_noalloc(const void* q, const void* k_cache, const void* v_cache,
+                       const int32_t* block_tables, int max_blocks_per_seq,
+                       const int32_t* seq_lens, const int32_t* query_start_loc,
+                       int num_seqs, int num_tokens, int max_query_len, int max_seq_len,
+                       float scale, void* out, const pa_layout* layout, int32_t* status,
+                       void* stream);
+
 /* Message of the last failing call on this thread ("" if none). */
 const char* pa_last_error(void);
 

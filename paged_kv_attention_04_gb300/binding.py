@@ -54,6 +54,9 @@ def lib() -> ctypes.CDLL:
         L.pa_forward.restype = i32
         L.pa_last_error.argtypes = []
         L.pa_last_error.restype = ctypes.c_char_p
+        L.pa_forward_noalloc.argtypes = [vp, vp, vp, vp, i32, vp, vp, i32, i32, i32, i32,
+                                         ctypes.c_float, vp, lp, vp, vp]
+        L.pa_forward_noalloc.restype = i32
         L.pa_set_profile_events.argtypes = [vp, vp]
         L.pa_set_profile_events.restype = i32
         L.pa_version.argtypes = []
@@ -122,6 +125,18 @@ def pa_forward(q, k_cache, v_cache, block_tables, seq_lens, query_start_loc,
                             int(max_seq_len), float(scale), _ptr(out), _ptr(workspace),
                             int(workspace.numel() * workspace.element_size()),
                             ctypes.byref(layout), _ptr(status), _stream(stream)))
+
+
+def pa_forward_noalloc(q, k_cache, v_cache, block_tables, seq_lens, query_start_loc,
+                       max_query_len: int, max_seq_len: int, scale: float, out,
+                       layout: pa_layout, status: torch.Tensor | None = None, stream=None) -> None:
+    """pa_forward using the library's built-in device scratch instead of a
+    caller workspace (for callers that cannot allocate device memory)."""
+    _check(lib().pa_forward_noalloc(_ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(block_tables),
+                                    int(block_tables.shape[1]), _ptr(seq_lens),
+                                    _ptr(query_start_loc), int(seq_lens.shape[0]), int(q.shape[0]),
+                                    int(max_query_len), int(max_seq_len), float(scale), _ptr(out),
+                                    ctypes.byref(layout), _ptr(status), _stream(stream)))
 
 
 def pa_set_profile_events(start: "torch.cuda.Event | None", stop: "torch.cuda.Event | None") -> None:

@@ -110,6 +110,11 @@ int num_sms_of_current_device(int* out) {
 
 }  // namespace
 
+int set_last_error(int code, const char* msg) {
+  g_last_error = msg;
+  return code;
+}
+
 WsLayout ws_layout(const Capacity& cap, int B, int Hkv, int D, int group) {
   WsLayout w{};
   size_t off = 0;

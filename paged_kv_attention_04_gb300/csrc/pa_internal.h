@@ -78,6 +78,9 @@ struct AttnParams {
   int32_t* status;
 };
 
+// Sets the message pa_last_error() returns on this thread; returns code.
+int set_last_error(int code, const char* msg);
+
 WsLayout ws_layout(const Capacity& cap, int num_seqs, int num_kv_heads, int head_size,
                    int group);
 
