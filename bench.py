@@ -101,22 +101,24 @@ def measured_peaks() -> tuple[float, str]:
 
 def kernel_source_hash() -> str:
     h = hashlib.sha256()
-    for name in ("pa_attn_cc.cuh", "pa_device.cuh"):
+    for name in ("pa_attn_mma.cuh", "pa_attn_cc_bf16.cu", "pa_device.cuh"):
         with open(os.path.join(ROOT, "paged_kv_attention_04_gb300", "csrc", name), "rb") as f:
             h.update(f.read())
     return h.hexdigest()[:16]
 
 
 def recorded_traffic(workload: str):
-    """DRAM bytes per launch of the decode kernel from a committed ncu summary,
-    if it was taken on the current kernel source; else None."""
-    path = os.path.join(ROOT, "profiles", "traffic.json")
+    """DRAM bytes per launch of the decode kernel from the committed ncu summary
+    (profiles/traffic.txt), if it was taken on the current kernel source; else None."""
+    path = os.path.join(ROOT, "profiles", "traffic.txt")
     try:
         with open(path) as f:
-            rec = json.load(f)[workload]
-        if rec.get("kernel_hash") == kernel_source_hash():
-            return float(rec["dram_bytes_per_launch"])
-    except Exception:
+            for line in f:
+                parts = line.split()
+                if parts and not parts[0].startswith("#") and parts[0] == workload:
+                    if parts[1] == kernel_source_hash():
+                        return float(parts[2])
+    except OSError:
         pass
     return None
 
@@ -473,7 +475,7 @@ def run_gpu_arm(args):
                    "l2": "no flush: KV read per step (1.4 GB) > L2 (126 MB)",
                    "parallelism": "replicas" if world > 1 else "single GPU",
                    "algorithmic_bytes_per_step": w["step_bytes"]},
-        "roofline": {"bound": "hbm", "kernel": "attn_cc_kernel<bf16,128,4,1> (decode)",
+        "roofline": {"bound": "hbm", "kernel": "attn_mma_kernel<128,4,1,4,2> (decode)",
                      "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
                      "peak_source": peak_src, "traffic": traffic,
                      "algorithmic_bytes_per_launch": w["decode_bytes"], "kernel_ms": dec_max},
@@ -522,6 +524,38 @@ def run_reference_arm(args):
     print(json.dumps(line))
 
 
+def run_ncu_case(spec_arg: str, iters: int = 3) -> None:
+    """A small step for profilers: `NAME` or `NAME:N` (the first N requests of
+    workload NAME); runs pa_cache_write + pa_forward `iters` times."""
+    import torch
+
+    import paged_kv_attention_04_gb300 as P
+    from paged_kv_attention_04_gb300 import build
+    from paged_kv_attention_04_gb300 import workloads as W
+    build.build()
+    name, _, n = spec_arg.partition(":")
+    spec = W.CONFIGS[name]()
+    if n:
+        spec.seq_lens = spec.seq_lens[:int(n)]
+        spec.q_lens = spec.q_lens[:int(n)]
+        if spec.sharing is not None:
+            spec.sharing = spec.sharing[:int(n)]
+    st = W.make_step(spec, device="cuda")
+    lay = P.layout_of(st.k_cache, spec.num_q_heads)
+    ws = P.alloc_workspace(lay, spec.num_seqs, spec.num_tokens, st.max_seq_len)
+    out = torch.empty_like(st.q)
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    for _ in range(iters):
+        P.pa_cache_write(st.k, st.v, st.slot_mapping, st.k_cache, st.v_cache, lay, status)
+        P.pa_forward(st.q, st.k_cache, st.v_cache, st.block_tables, st.seq_lens,
+                     st.query_start_loc, st.max_query_len, st.max_seq_len, st.scale, out, ws, lay,
+                     status)
+    torch.cuda.synchronize()
+    if int(status.item()) != 0:
+        raise RuntimeError(f"device status {int(status.item())}")
+    print(json.dumps({"ncu_case": spec_arg, "tokens": spec.num_tokens, "ok": True}))
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -531,9 +565,14 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--oracle-seconds", type=float, default=10.0)
     ap.add_argument("--oracle-stride", type=int, default=1)
+    ap.add_argument("--ncu-case", default=None,
+                    help="run a small step for a profiler: NAME or NAME:N (first N requests)")
     ap.add_argument("--oracle-budget", type=float, default=1.0, help=argparse.SUPPRESS)
     ap.add_argument("--oracle-worker", default=None, help=argparse.SUPPRESS)
     args = ap.parse_args()
+    if args.ncu_case:
+        run_ncu_case(args.ncu_case)
+        return
     if args.oracle_worker:
         oracle_worker(args.oracle_worker, args.oracle_seconds, args.oracle_stride, args.steps,
                       args.warmup, args.oracle_budget)

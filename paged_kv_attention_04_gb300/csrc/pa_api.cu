@@ -68,10 +68,15 @@ int check_layout(const pa_layout* L) {
   return PA_OK;
 }
 
-// KV blocks per split: about 128 KiB of K+V per work unit.
+#ifndef PA_SPLIT_KV_BYTES
+#define PA_SPLIT_KV_BYTES (512 * 1024)
+#endif
+
+// Smallest KV split, in blocks: about PA_SPLIT_KV_BYTES of K+V per work unit.
 int blocks_per_split(const pa_layout* L) {
   const int block_kv_bytes = 2 * kBlockSize * L->head_size * elem_bytes(L->dtype);
-  int b = (128 * 1024) / block_kv_bytes;
+  int b = PA_SPLIT_KV_BYTES / block_kv_bytes;
+  if (b > kMaxUnitBlocks) b = kMaxUnitBlocks;
   return b < 1 ? 1 : b;
 }
 
@@ -80,7 +85,10 @@ int small_positions(const pa_layout* L) { return kSmallRows / (L->num_q_heads / 
 Capacity capacity(const pa_layout* L, int B, int T, int max_seq_len) {
   Capacity c{};
   const long long max_nb = cdiv(max_seq_len, kBlockSize);
-  const long long splits = cdiv(max_nb, blocks_per_split(L));
+  // most splits any tile gets (see the plan kernel's per-request split size)
+  long long splits = cdiv(max_nb, blocks_per_split(L));
+  if (splits > kMaxSplits) splits = kMaxSplits;
+  if (cdiv(max_nb, kMaxUnitBlocks) > splits) splits = cdiv(max_nb, kMaxUnitBlocks);
   const long long multi = T > B ? (T - B < B ? T - B : B) : 0;  // requests with q_len >= 2
   c.decode_tiles = B;
   c.decode_items = static_cast<long long>(B) * splits;
@@ -129,9 +137,9 @@ WsLayout ws_layout(const Capacity& cap, int B, int Hkv, int D, int group) {
   w.pfx_s_tiles = take(sizeof(int) * (B + 1));
   w.pfx_p_tiles = take(sizeof(int) * (B + 1));
   w.items_d = take(sizeof(int4) * cap.decode_items);
-  w.tiles_d = take(sizeof(int2) * cap.decode_tiles);
+  w.tiles_d = take(sizeof(int4) * cap.decode_tiles);
   w.items_s = take(sizeof(int4) * cap.small_items);
-  w.tiles_s = take(sizeof(int2) * cap.small_tiles);
+  w.tiles_s = take(sizeof(int4) * cap.small_tiles);
   w.tiles_p = take(sizeof(int4) * cap.prefill_tiles);
   w.cnt_d = take(sizeof(int) * cap.decode_tiles * Hkv);
   w.cnt_s = take(sizeof(int) * cap.small_tiles * Hkv);
@@ -271,7 +279,6 @@ int pa_forward(const void* q, const void* k_cache, const void* v_cache,
   ap.num_kv_heads = layout->num_kv_heads;
   ap.num_blocks = layout->num_blocks;
   ap.num_tokens = num_tokens;
-  ap.bps = pp.bps;
   ap.scale_log2 = scale * 1.4426950408889634f;
   ap.status = status;
 
@@ -279,7 +286,7 @@ int pa_forward(const void* q, const void* k_cache, const void* v_cache,
   ap.n_items = hdr + kHdrDecodeItems;
   ap.next = hdr + kHdrDecodeNext;
   ap.items = reinterpret_cast<const int4*>(ws + lay.items_d);
-  ap.tiles = reinterpret_cast<const int2*>(ws + lay.tiles_d);
+  ap.tiles = reinterpret_cast<const int4*>(ws + lay.tiles_d);
   ap.merge_cnt = reinterpret_cast<int*>(ws + lay.cnt_d);
   ap.part_acc = reinterpret_cast<float*>(ws + lay.part_acc_d);
   ap.part_ml = reinterpret_cast<float*>(ws + lay.part_ml_d);
@@ -292,7 +299,7 @@ int pa_forward(const void* q, const void* k_cache, const void* v_cache,
     ap.n_items = hdr + kHdrSmallItems;
     ap.next = hdr + kHdrSmallNext;
     ap.items = reinterpret_cast<const int4*>(ws + lay.items_s);
-    ap.tiles = reinterpret_cast<const int2*>(ws + lay.tiles_s);
+    ap.tiles = reinterpret_cast<const int4*>(ws + lay.tiles_s);
     ap.merge_cnt = reinterpret_cast<int*>(ws + lay.cnt_s);
     ap.part_acc = reinterpret_cast<float*>(ws + lay.part_acc_s);
     ap.part_ml = reinterpret_cast<float*>(ws + lay.part_ml_s);

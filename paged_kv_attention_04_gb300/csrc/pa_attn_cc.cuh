@@ -103,8 +103,8 @@ __global__ void __launch_bounds__(CcCfg<T, D, G, P>::kThreads)
     const int item = unit / Hkv;
     const int g = unit - item * Hkv;
     const int4 it = __ldg(p.items + item);
-    const int r = it.x, m = it.y, s = it.z, tile = it.w;
-    const int2 tinfo = __ldg(p.tiles + tile);
+    const int r = it.x, m = it.y, tile = it.w;
+    const int4 tinfo = __ldg(p.tiles + tile);
     const int nsplit = tinfo.y;
     const int S = __ldg(p.seq_lens + r);
     const int a = __ldg(p.qsl + r);
@@ -114,8 +114,8 @@ __global__ void __launch_bounds__(CcCfg<T, D, G, P>::kThreads)
     const int pos0 = S - L + j0;                 // position of tile row 0
     const int kv_end = pos0 + npos;              // one past the last visible key
     const int nblk = (kv_end + kBlockSize - 1) / kBlockSize;
-    const int b0 = s * p.bps;
-    const int b1 = min(b0 + p.bps, nblk);
+    const int b0 = it.z;
+    const int b1 = min(b0 + tinfo.z, nblk);
     const int kv_hi = min(b1 * kBlockSize, kv_end);
     const int32_t* bt_row = p.block_tables + static_cast<long long>(r) * p.max_blocks_per_seq;
 

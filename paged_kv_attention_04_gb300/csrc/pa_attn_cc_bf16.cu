@@ -1,9 +1,45 @@
-// bf16 instantiations of the CUDA-core split-KV attention kernel.
-#include "pa_attn_cc.cuh"
+// bf16 attention dispatch: the tensor-core (mma.sync) split-KV kernel for
+// decode tiles (one position) and few-position tiles.
+#include "pa_attn_mma.cuh"
+
+#ifndef PA_MMA_WARPS
+#define PA_MMA_WARPS 4
+#endif
+#ifndef PA_MMA_STAGES
+#define PA_MMA_STAGES 2
+#endif
 
 namespace pa {
+
+namespace {
+template <int D, int G>
+cudaError_t dispatch_positions(const AttnParams& p, int positions, int num_sms,
+                               cudaStream_t stream) {
+  if (positions == 1)
+    return launch_mma<D, G, 1, PA_MMA_WARPS, PA_MMA_STAGES>(p, num_sms, stream);
+  return launch_mma<D, G, kSmallRows / G, PA_MMA_WARPS, PA_MMA_STAGES>(p, num_sms, stream);
+}
+
+template <int D>
+cudaError_t dispatch_group(const AttnParams& p, int group, int positions, int num_sms,
+                           cudaStream_t stream) {
+  switch (group) {
+    case 1: return dispatch_positions<D, 1>(p, positions, num_sms, stream);
+    case 2: return dispatch_positions<D, 2>(p, positions, num_sms, stream);
+    case 4: return dispatch_positions<D, 4>(p, positions, num_sms, stream);
+    case 8: return dispatch_positions<D, 8>(p, positions, num_sms, stream);
+    default: return cudaErrorInvalidValue;
+  }
+}
+}  // namespace
+
 cudaError_t launch_attn_cc_bf16(const AttnParams& p, int head_size, int group, int positions,
                                 int num_sms, cudaStream_t stream) {
-  return dispatch_cc<__nv_bfloat16>(p, head_size, group, positions, num_sms, stream);
+  switch (head_size) {
+    case 64: return dispatch_group<64>(p, group, positions, num_sms, stream);
+    case 128: return dispatch_group<128>(p, group, positions, num_sms, stream);
+    default: return cudaErrorInvalidValue;
+  }
 }
+
 }  // namespace pa

@@ -1,0 +1,545 @@
+// bf16 paged attention for decode and few-token tiles: warp-level tensor-core
+// products, a continuous per-warp KV stream, split-KV with a fused
+// log-sum-exp merge.
+//
+// Decode is bound by HBM bandwidth ("Inside vLLM", section Scheduler).  On
+// GB300 an SM must consume ~23 bytes of KV per clock to keep up with HBM;
+// doing the grouped-query dot products on CUDA cores costs ~1400 warp
+// instructions per 8 KB KV block (unpack, FMA, shuffles), which makes the
+// kernel issue-bound.  The R = P x G query rows of a tile against a 16-token
+// block are two tiny dense products (R x D by D x 16 and R x 16 by 16 x D),
+// so each warp runs them as m16n8k16 bf16 MMAs with fp32 accumulation
+// (rows padded to 16): ~32 MMAs and 16 ldmatrix per block.  The softmax
+// stays on CUDA cores (fp32, base 2, quad shuffles).
+//
+// Work: units (request r, query tile m, KV split s, kv head g) fetched with
+// an atomic counter.  A CTA has NW compute warps and one scheduler warp.
+// The scheduler warp claims units two ahead, decodes them, copies the
+// unit's block-table slice and stages the next unit's q rows, so the
+// compute warps never wait on a dependent global load.  Compute warp w
+// takes blocks w, w+NW, ... of a unit; its cp.async ring (NS stages of one
+// K+V block, rows XOR-swizzled so ldmatrix is conflict-free) keeps issuing
+// into the next unit's blocks while the current unit is finished, so the KV
+// stream does not drain at unit boundaries.  Warps are joined through
+// shared memory; a split unit writes (max, sum, acc) partials and the last
+// split to finish merges them (atomic counter, no waiting).
+//
+// Causal limits: row j of a chunk of length L in a request of S tokens sits
+// at position S - L + j ("Serving models at scale with vLLM", section
+// Chunked prefill).  V rows past the last visible key are zero-filled so a
+// masked (p = 0) key never meets unwritten (NaN) cache slots in the MMA.
+#pragma once
+
+#include <cuda_bf16.h>
+#include <math_constants.h>
+
+#include "pa_device.cuh"
+#include "pa_internal.h"
+
+namespace pa {
+
+struct UnitMeta {
+  int valid;
+  int item, g, r, a, j0, npos, pos0, kv_hi, b0, b1, tile, nsplit, first;
+  int bt[kMaxUnitBlocks];  // the unit's block-table slice
+};
+
+// What the scheduler warp keeps of a unit to finish it after the compute
+// warps have moved on.
+struct UnitTail {
+  int valid, item, g, a, j0, npos, tile, nsplit, first;
+};
+
+__device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2,
+                                        uint32_t& r3) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];\n"
+               : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
+               : "r"(addr));
+}
+__device__ __forceinline__ void ldsm_x4_t(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2,
+                                          uint32_t& r3) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];\n"
+               : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
+               : "r"(addr));
+}
+// D = A(16x16, row) * B(16x8, col) + D, bf16 inputs, fp32 accumulators.
+__device__ __forceinline__ void mma_bf16(float* d, const uint32_t* a, uint32_t b0, uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
+      "{%8,%9}, {%0,%1,%2,%3};\n"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+// Two floats -> packed bf16 pair (lo in the low half), round to nearest even.
+__device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
+  uint32_t r;
+  asm("cvt.rn.bf16x2.f32 %0, %1, %2;\n" : "=r"(r) : "f"(hi), "f"(lo));
+  return r;
+}
+
+template <int D, int G, int P, int NW, int NS>
+struct MmaCfg {
+  static constexpr int kR = P * G;                 // real query rows (<= 16)
+  static constexpr int kRowBytes = D * 2;
+  static constexpr int kChunks = kRowBytes / 16;   // 16-byte chunks per row
+  static constexpr int kTileBytes = kBlockSize * kRowBytes;
+  static constexpr int kStageBytes = 2 * kTileBytes;  // K then V
+  static constexpr int kKSteps = D / 16;
+  static constexpr int kNTiles = D / 8;
+  static constexpr int kThreads = (NW + 1) * 32;
+  static constexpr int kRingOff = 0;
+  static constexpr int kRingBytes = NW * NS * kStageBytes;
+  static constexpr int kQOff = kRingOff + kRingBytes;
+  static constexpr int kQBytes = 2 * 16 * kRowBytes;
+  static constexpr int kCombOff = kQOff + kQBytes;
+  static constexpr int kCombBytes = 2 * NW * kR * D * 4;   // two units in flight
+  static constexpr int kMlOff = kCombOff + kCombBytes;
+  static constexpr int kMlBytes = 2 * NW * kR * 2 * 4;
+  static constexpr int kMetaOff = (kMlOff + kMlBytes + 15) / 16 * 16;
+  static constexpr int kSmemBytes = kMetaOff + 3 * static_cast<int>(sizeof(UnitMeta));
+  // two CTAs per SM when their shared memory fits (228 KB per SM, 1 KB reserved per CTA)
+  static constexpr int kMinCtas = 2 * (kSmemBytes + 1024 + 64) <= 228 * 1024 ? 2 : 1;
+  static_assert(kSmemBytes <= 227 * 1024, "shared memory per CTA exceeds 227 KB");
+  static_assert(kR <= 16, "at most 16 query rows per tile");
+  static_assert(NS >= 2 && NS <= 8, "2 to 8 pipeline stages");
+  static_assert(kChunks % 8 == 0, "rows must be a multiple of 128 bytes");
+  static_assert((kBlockSize * kChunks) % 32 == 0, "tile chunks must split over a warp");
+};
+
+// Swizzled byte offset of 16-byte chunk c of row t in a tile.
+template <int RowBytes>
+__device__ __forceinline__ uint32_t swz(int t, int c) {
+  return static_cast<uint32_t>(t * RowBytes + ((c ^ (t & 7)) << 4));
+}
+
+template <int D, int G, int P, int NW, int NS>
+__global__ void __launch_bounds__(MmaCfg<D, G, P, NW, NS>::kThreads,
+                                  MmaCfg<D, G, P, NW, NS>::kMinCtas)
+    attn_mma_kernel(const AttnParams p) {
+  using C = MmaCfg<D, G, P, NW, NS>;
+  constexpr int R = C::kR;
+  extern __shared__ __align__(128) unsigned char smem[];
+
+  const int tid = threadIdx.x;
+  const int lane = tid & 31;
+  const int warp = tid >> 5;
+  const bool sched = warp == NW;
+  const int Hkv = p.num_kv_heads, Hq = p.num_q_heads;
+  UnitMeta* meta = reinterpret_cast<UnitMeta*>(smem + C::kMetaOff);
+  float* comb = reinterpret_cast<float*>(smem + C::kCombOff);
+  float* comb_ml = reinterpret_cast<float*>(smem + C::kMlOff);
+  const uint32_t ring_u32 = smem_u32(smem + C::kRingOff) + warp * NS * C::kStageBytes;
+  const uint32_t q_u32 = smem_u32(smem + C::kQOff);
+  const unsigned char* kc = static_cast<const unsigned char*>(p.k_cache);
+  const unsigned char* vc = static_cast<const unsigned char*>(p.v_cache);
+  const __nv_bfloat16* q = static_cast<const __nv_bfloat16*>(p.q);
+  __nv_bfloat16* out = static_cast<__nv_bfloat16*>(p.out);
+  const int n_units = __ldg(p.n_items) * Hkv;
+
+  // ---- scheduler-warp helpers -------------------------------------------
+  auto fetch_unit = [&](UnitMeta& m) {  // whole scheduler warp
+    int u = 0;
+    if (lane == 0) u = atomicAdd(p.next, 1);
+    u = __shfl_sync(0xffffffffu, u, 0);
+    if (u >= n_units) {
+      if (lane == 0) m.valid = 0;
+      return;
+    }
+    const int item = u / Hkv;
+    const int g = u - item * Hkv;
+    const int4 it = __ldg(p.items + item);
+    const int4 ti = __ldg(p.tiles + it.w);
+    const int S = __ldg(p.seq_lens + it.x);
+    const int a = __ldg(p.qsl + it.x);
+    const int L = __ldg(p.qsl + it.x + 1) - a;
+    const int j0 = it.y * P;
+    const int npos = min(P, L - j0);
+    const int pos0 = S - L + j0;
+    const int kv_end = pos0 + npos;
+    const int nblk = (kv_end + kBlockSize - 1) / kBlockSize;
+    const int b0 = it.z;
+    const int b1 = min(b0 + ti.z, nblk);
+    const int32_t* row = p.block_tables + static_cast<long long>(it.x) * p.max_blocks_per_seq;
+    for (int i = lane; i < b1 - b0; i += 32) m.bt[i] = __ldg(row + b0 + i);
+    if (lane == 0) {
+      m.valid = 1; m.item = item; m.g = g; m.r = it.x; m.a = a; m.j0 = j0; m.npos = npos;
+      m.pos0 = pos0; m.kv_hi = min(b1 * kBlockSize, kv_end); m.b0 = b0; m.b1 = b1;
+      m.tile = it.w; m.nsplit = ti.y; m.first = ti.x;
+    }
+  };
+  auto stage_q = [&](const UnitMeta& m, int buf) {  // whole scheduler warp
+    // rows: (position jj, grouped head hh) = (row / G, row % G); rows >= R are zero
+    for (int idx = lane; idx < 16 * C::kChunks; idx += 32) {
+      const int row = idx / C::kChunks, c = idx - row * C::kChunks;
+      uint4 v = make_uint4(0, 0, 0, 0);
+      if (m.valid && row < R) {
+        const int jj = row / G, hh = row - jj * G;
+        if (jj < m.npos) {
+          const long long tok = m.a + m.j0 + jj;
+          v = __ldg(reinterpret_cast<const uint4*>(q + (tok * Hq + m.g * G + hh) * D) + c);
+        }
+      }
+      *reinterpret_cast<uint4*>(smem + C::kQOff + buf * 16 * C::kRowBytes +
+                                swz<C::kRowBytes>(row, c)) = v;
+    }
+  };
+
+  if (sched) {
+    fetch_unit(meta[0]);
+    __syncwarp();
+    fetch_unit(meta[1]);
+    __syncwarp();
+    stage_q(meta[0], 0);
+  }
+  __syncthreads();
+
+  // ---- compute-warp stream state ----------------------------------------
+  // The warp's KV stream is its share of unit k's blocks, then of unit k+1's.
+  int iss_unit = 0, iss_i = 0;  // next block to issue: (unit sequence, index in warp share)
+  int issued = 0, computed = 0;
+
+  auto share = [&](const UnitMeta& m) -> int {
+    const int n = m.b1 - m.b0 - warp;
+    return (m.valid && n > 0) ? (n + NW - 1) / NW : 0;
+  };
+  // Issue the next block of the stream if it lies in unit `limit` or earlier.
+  auto issue_one = [&](int limit) -> bool {
+    while (iss_unit <= limit) {
+      const UnitMeta& m = meta[iss_unit % 3];
+      if (iss_i < share(m)) break;
+      ++iss_unit;
+      iss_i = 0;
+    }
+    if (iss_unit > limit) return false;
+    const UnitMeta& m = meta[iss_unit % 3];
+    const int bl = warp + iss_i * NW;  // block index within the unit
+    const int b = m.b0 + bl;
+    int phys = m.bt[bl];
+    int kbytes = 16;
+    if (phys < 0 || phys >= p.num_blocks) {
+      if (lane == 0) flag_error(p.status, PA_DEV_BLOCK_RANGE);
+      phys = 0;
+      kbytes = 0;
+    }
+    const int valid_rows = min(kBlockSize, m.kv_hi - b * kBlockSize);
+    const uint32_t st = ring_u32 + (issued % NS) * C::kStageBytes;
+    const long long row_stride = static_cast<long long>(Hkv) * C::kRowBytes;
+    const long long base = static_cast<long long>(phys) * kBlockSize * row_stride +
+                           static_cast<long long>(m.g) * C::kRowBytes;
+    const int c = lane % C::kChunks;
+#pragma unroll
+    for (int k = 0; k < (kBlockSize * C::kChunks) / 32; ++k) {
+      const int t = lane / C::kChunks + k * (32 / C::kChunks);
+      const long long off = base + t * row_stride + c * 16;
+      const uint32_t so = swz<C::kRowBytes>(t, c);
+      const int vb = t < valid_rows ? kbytes : 0;
+      cp_async16(st + so, kc + off, vb);
+      cp_async16(st + C::kTileBytes + so, vc + off, vb);
+    }
+    cp_async_commit();
+    ++issued;
+    ++iss_i;
+    return true;
+  };
+  auto wait_for = [&](int idx) {  // block `idx` of the stream has landed
+    const int newer = min(issued - idx - 1, NS - 1);  // groups allowed to stay in flight
+    switch (newer) {
+      case 7: cp_async_wait<7>(); break;
+      case 6: cp_async_wait<6>(); break;
+      case 5: cp_async_wait<5>(); break;
+      case 4: cp_async_wait<4>(); break;
+      case 3: cp_async_wait<3>(); break;
+      case 2: cp_async_wait<2>(); break;
+      case 1: cp_async_wait<1>(); break;
+      default: cp_async_wait<0>(); break;
+    }
+    __syncwarp();
+  };
+
+  if (!sched) {
+    for (int i = 0; i < NS - 1; ++i)
+      if (!issue_one(1)) break;
+  }
+
+  // ---- scheduler warp: join the warps' states of a finished unit, write the
+  // output or the split's partial, and merge the splits if it is the last.
+  auto finish_unit = [&](const UnitTail& u, int buf) {
+    const float* cb = comb + buf * NW * R * D;
+    const float* cm = comb_ml + buf * NW * R * 2;
+    const long long part_base = (static_cast<long long>(u.item) * Hkv + u.g) * R;
+    for (int idx = lane; idx < R * D / 4; idx += 32) {
+      const int row = (idx * 4) / D, d = idx * 4 - row * D;
+      const int jj = row / G, hh = row - jj * G;
+      if (jj >= u.npos) continue;
+      float M = -CUDART_INF_F;
+#pragma unroll
+      for (int w = 0; w < NW; ++w) M = fmaxf(M, cm[(w * R + row) * 2]);
+      float4 num = make_float4(0.f, 0.f, 0.f, 0.f);
+      float den = 0.f;
+      if (M != -CUDART_INF_F) {
+#pragma unroll
+        for (int w = 0; w < NW; ++w) {
+          const float f = exp2f(cm[(w * R + row) * 2] - M);
+          const float4 c4 = *reinterpret_cast<const float4*>(cb + (w * R + row) * D + d);
+          num.x = fmaf(c4.x, f, num.x); num.y = fmaf(c4.y, f, num.y);
+          num.z = fmaf(c4.z, f, num.z); num.w = fmaf(c4.w, f, num.w);
+          den = fmaf(cm[(w * R + row) * 2 + 1], f, den);
+        }
+      }
+      if (u.nsplit == 1) {
+        const long long tok = u.a + u.j0 + jj;
+        const float inv = 1.f / den;
+        *reinterpret_cast<uint2*>(out + (tok * Hq + u.g * G + hh) * D + d) =
+            make_uint2(pack_bf16(num.x * inv, num.y * inv), pack_bf16(num.z * inv, num.w * inv));
+      } else {
+        *reinterpret_cast<float4*>(p.part_acc + (part_base + row) * D + d) = num;
+        if (d == 0) *reinterpret_cast<float2*>(p.part_ml + (part_base + row) * 2) = make_float2(M, den);
+      }
+    }
+    if (u.nsplit > 1) {
+      __threadfence();
+      __syncwarp();
+      int last = 0;
+      if (lane == 0) last = atomicAdd(p.merge_cnt + u.tile * Hkv + u.g, 1) == u.nsplit - 1;
+      last = __shfl_sync(0xffffffffu, last, 0);
+      if (last) {
+        __threadfence();
+        for (int idx = lane; idx < R * D / 4; idx += 32) {
+          const int row = (idx * 4) / D, d = idx * 4 - row * D;
+          const int jj = row / G, hh = row - jj * G;
+          if (jj >= u.npos) continue;
+          float M = -CUDART_INF_F, den = 0.f;
+          float4 num = make_float4(0.f, 0.f, 0.f, 0.f);
+          for (int sp = 0; sp < u.nsplit; ++sp) {
+            const long long pb = (static_cast<long long>(u.first + sp) * Hkv + u.g) * R + row;
+            const float2 ml = __ldcg(reinterpret_cast<const float2*>(p.part_ml + pb * 2));
+            if (ml.x == -CUDART_INF_F) continue;
+            const float4 a4 = __ldcg(reinterpret_cast<const float4*>(p.part_acc + pb * D + d));
+            if (ml.x > M) {  // online rescale to the new maximum
+              const float sc = exp2f(M - ml.x);
+              num.x *= sc; num.y *= sc; num.z *= sc; num.w *= sc; den *= sc;
+              M = ml.x;
+            }
+            const float f = exp2f(ml.x - M);
+            num.x = fmaf(a4.x, f, num.x); num.y = fmaf(a4.y, f, num.y);
+            num.z = fmaf(a4.z, f, num.z); num.w = fmaf(a4.w, f, num.w);
+            den = fmaf(ml.y, f, den);
+          }
+          const long long tok = u.a + u.j0 + jj;
+          const float inv = 1.f / den;
+          *reinterpret_cast<uint2*>(out + (tok * Hq + u.g * G + hh) * D + d) =
+              make_uint2(pack_bf16(num.x * inv, num.y * inv), pack_bf16(num.z * inv, num.w * inv));
+        }
+      }
+    }
+  };
+
+  UnitTail tail;
+  tail.valid = 0;
+  int k = 0;
+  for (;; ++k) {
+    const UnitMeta& cur = meta[k % 3];
+    if (!cur.valid) break;
+    if (sched) {
+      // finish unit k-1 while the compute warps stream unit k
+      if (tail.valid) finish_unit(tail, (k - 1) & 1);
+      tail.valid = 1; tail.item = cur.item; tail.g = cur.g; tail.a = cur.a; tail.j0 = cur.j0;
+      tail.npos = cur.npos; tail.tile = cur.tile; tail.nsplit = cur.nsplit; tail.first = cur.first;
+      fetch_unit(meta[(k + 2) % 3]);
+      __syncwarp();
+      stage_q(meta[(k + 1) % 3], (k + 1) & 1);
+    } else {
+      // Every block of units < k has been issued and computed; move the issue
+      // pointer off unit k-1, whose metadata slot the scheduler warp is now
+      // overwriting with unit k+2.
+      if (iss_unit < k) {
+        iss_unit = k;
+        iss_i = 0;
+      }
+      // q fragments (A operand, rows x D) for this unit
+      uint32_t qa[C::kKSteps][4];
+      {
+        const uint32_t qb = q_u32 + (k & 1) * 16 * C::kRowBytes;
+        const int mi = lane >> 3, rr = (lane & 7) + ((mi & 1) << 3);
+#pragma unroll
+        for (int kk = 0; kk < C::kKSteps; ++kk)
+          ldsm_x4(qb + swz<C::kRowBytes>(rr, 2 * kk + (mi >> 1)), qa[kk][0], qa[kk][1],
+                  qa[kk][2], qa[kk][3]);
+      }
+      float o[C::kNTiles][4];
+#pragma unroll
+      for (int j = 0; j < C::kNTiles; ++j) o[j][0] = o[j][1] = o[j][2] = o[j][3] = 0.f;
+      float mA = -CUDART_INF_F, mB = -CUDART_INF_F, lA = 0.f, lB = 0.f;
+      const int rowA = lane >> 2, rowB = rowA + 8;
+      const int nb = share(cur);
+      for (int i = 0; i < nb; ++i) {
+        issue_one(k + 1);
+        wait_for(computed);
+        const uint32_t st = ring_u32 + (computed % NS) * C::kStageBytes;
+        const int tok0 = (cur.b0 + warp + i * NW) * kBlockSize;
+        // S = Q K^T for the block's 16 tokens: two n-tiles of 8 tokens
+        float s[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+        {
+          const int mi = lane >> 3;
+          const int t = ((mi >> 1) << 3) + (lane & 7);
+#pragma unroll
+          for (int kk = 0; kk < C::kKSteps; ++kk) {
+            uint32_t b0, b1, b2, b3;
+            ldsm_x4(st + swz<C::kRowBytes>(t, 2 * kk + (mi & 1)), b0, b1, b2, b3);
+            mma_bf16(s[0], qa[kk], b0, b1);
+            mma_bf16(s[1], qa[kk], b2, b3);
+          }
+        }
+        // mask and online softmax (base 2); lane holds rows rowA (c0,c1) and rowB (c2,c3)
+        float pA[4], pB[4];
+        bool rescale;
+        {
+          float mx = -CUDART_INF_F;
+#pragma unroll
+          for (int j = 0; j < 2; ++j)
+#pragma unroll
+            for (int e = 0; e < 2; ++e) {
+              const int tok = tok0 + j * 8 + ((lane & 3) << 1) + e;
+              const int jj = rowA / G;
+              const bool ok = rowA < R && jj < cur.npos && tok < cur.kv_hi && tok <= cur.pos0 + jj;
+              s[j][e] = ok ? s[j][e] * p.scale_log2 : -CUDART_INF_F;
+              mx = fmaxf(mx, s[j][e]);
+            }
+          mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
+          mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
+          const float mn = fmaxf(mA, mx);
+          float corr = 1.f;
+          if (mn != -CUDART_INF_F) {
+            corr = exp2f(mA - mn);
+#pragma unroll
+            for (int j = 0; j < 2; ++j)
+#pragma unroll
+              for (int e = 0; e < 2; ++e) pA[j * 2 + e] = exp2f(s[j][e] - mn);
+          } else {
+#pragma unroll
+            for (int e = 0; e < 4; ++e) pA[e] = 0.f;
+          }
+          lA = lA * corr + (pA[0] + pA[1]) + (pA[2] + pA[3]);
+          mA = mn;
+          float corrB = 1.f;
+          if constexpr (R > 8) {
+            float mxb = -CUDART_INF_F;
+#pragma unroll
+            for (int j = 0; j < 2; ++j)
+#pragma unroll
+              for (int e = 0; e < 2; ++e) {
+                const int tok = tok0 + j * 8 + ((lane & 3) << 1) + e;
+                const int jj = rowB / G;
+                const bool ok = rowB < R && jj < cur.npos && tok < cur.kv_hi && tok <= cur.pos0 + jj;
+                s[j][2 + e] = ok ? s[j][2 + e] * p.scale_log2 : -CUDART_INF_F;
+                mxb = fmaxf(mxb, s[j][2 + e]);
+              }
+            mxb = fmaxf(mxb, __shfl_xor_sync(0xffffffffu, mxb, 1));
+            mxb = fmaxf(mxb, __shfl_xor_sync(0xffffffffu, mxb, 2));
+            const float mnb = fmaxf(mB, mxb);
+            if (mnb != -CUDART_INF_F) {
+              corrB = exp2f(mB - mnb);
+#pragma unroll
+              for (int j = 0; j < 2; ++j)
+#pragma unroll
+                for (int e = 0; e < 2; ++e) pB[j * 2 + e] = exp2f(s[j][2 + e] - mnb);
+            } else {
+#pragma unroll
+              for (int e = 0; e < 4; ++e) pB[e] = 0.f;
+            }
+            lB = lB * corrB + (pB[0] + pB[1]) + (pB[2] + pB[3]);
+            mB = mnb;
+          } else {
+#pragma unroll
+            for (int e = 0; e < 4; ++e) pB[e] = 0.f;
+          }
+          rescale = __any_sync(0xffffffffu, corr != 1.f || corrB != 1.f);
+          if (rescale) {
+#pragma unroll
+            for (int j = 0; j < C::kNTiles; ++j) {
+              o[j][0] *= corr; o[j][1] *= corr;
+              o[j][2] *= corrB; o[j][3] *= corrB;
+            }
+          }
+        }
+        // O += P V: P as the A operand (rows x 16 tokens), V via transposed ldmatrix
+        uint32_t pa[4];
+        pa[0] = pack_bf16(pA[0], pA[1]);
+        pa[1] = pack_bf16(pB[0], pB[1]);
+        pa[2] = pack_bf16(pA[2], pA[3]);
+        pa[3] = pack_bf16(pB[2], pB[3]);
+        {
+          const int mi = lane >> 3;
+          const int t = ((mi & 1) << 3) + (lane & 7);
+          const uint32_t vt = st + C::kTileBytes;
+#pragma unroll
+          for (int nt = 0; nt < C::kNTiles; nt += 2) {
+            uint32_t b0, b1, b2, b3;
+            ldsm_x4_t(vt + swz<C::kRowBytes>(t, nt + (mi >> 1)), b0, b1, b2, b3);
+            mma_bf16(o[nt], pa, b0, b1);
+            mma_bf16(o[nt + 1], pa, b2, b3);
+          }
+        }
+        __syncwarp();
+        ++computed;
+      }
+      // the warp's state for this unit -> shared memory (real rows only)
+      float* cb = comb + (k & 1) * NW * R * D;
+      float* cm = comb_ml + (k & 1) * NW * R * 2;
+      lA += __shfl_xor_sync(0xffffffffu, lA, 1);
+      lA += __shfl_xor_sync(0xffffffffu, lA, 2);
+      lB += __shfl_xor_sync(0xffffffffu, lB, 1);
+      lB += __shfl_xor_sync(0xffffffffu, lB, 2);
+      if (rowA < R) {
+#pragma unroll
+        for (int j = 0; j < C::kNTiles; ++j)
+          *reinterpret_cast<float2*>(cb + (warp * R + rowA) * D + j * 8 + ((lane & 3) << 1)) =
+              make_float2(o[j][0], o[j][1]);
+        if ((lane & 3) == 0) {
+          cm[(warp * R + rowA) * 2] = mA;
+          cm[(warp * R + rowA) * 2 + 1] = lA;
+        }
+      }
+      if constexpr (R > 8) {
+        if (rowB < R) {
+#pragma unroll
+          for (int j = 0; j < C::kNTiles; ++j)
+            *reinterpret_cast<float2*>(cb + (warp * R + rowB) * D + j * 8 + ((lane & 3) << 1)) =
+                make_float2(o[j][2], o[j][3]);
+          if ((lane & 3) == 0) {
+            cm[(warp * R + rowB) * 2] = mB;
+            cm[(warp * R + rowB) * 2 + 1] = lB;
+          }
+        }
+      }
+    }
+    __syncthreads();
+  }
+  if (sched && tail.valid) finish_unit(tail, (k - 1) & 1);
+  cp_async_wait<0>();
+}
+
+template <int D, int G, int P, int NW, int NS>
+cudaError_t launch_mma(const AttnParams& p, int num_sms, cudaStream_t stream) {
+  using C = MmaCfg<D, G, P, NW, NS>;
+  static int ctas_per_sm[64] = {0};
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+  if (ctas_per_sm[dev] == 0) {
+    e = cudaFuncSetAttribute(attn_mma_kernel<D, G, P, NW, NS>,
+                             cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
+    if (e != cudaSuccess) return e;
+    int n = 0;
+    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, attn_mma_kernel<D, G, P, NW, NS>,
+                                                      C::kThreads, C::kSmemBytes);
+    if (e != cudaSuccess) return e;
+    ctas_per_sm[dev] = n > 0 ? n : 1;
+  }
+  attn_mma_kernel<D, G, P, NW, NS>
+      <<<num_sms * ctas_per_sm[dev], C::kThreads, C::kSmemBytes, stream>>>(p);
+  return cudaGetLastError();
+}
+
+}  // namespace pa

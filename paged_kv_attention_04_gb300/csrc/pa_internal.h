@@ -9,7 +9,9 @@
 namespace pa {
 
 constexpr int kBlockSize = 16;        // tokens per KV block
-constexpr int kSmallRows = 16;        // query rows (positions x grouped heads) per CUDA-core tile
+constexpr int kSmallRows = 16;        // query rows (positions x grouped heads) per few-token tile
+constexpr int kMaxSplits = 64;        // KV splits per tile are kept at or below this ...
+constexpr int kMaxUnitBlocks = 256;   // ... unless a split would exceed this many blocks
 
 // Work-list classes written by the plan kernel.
 enum ReqClass : int { kClassNone = 0, kClassDecode = 1, kClassSmall = 2, kClassPrefill = 3 };
@@ -42,7 +44,7 @@ struct PlanParams {
   const int32_t* seq_lens;
   const int32_t* qsl;
   int num_seqs, num_tokens, max_query_len, max_seq_len, max_blocks_per_seq;
-  int bps;              // KV blocks per split
+  int bps;              // KV blocks per split (minimum; long requests use larger splits)
   int small_positions;  // query positions per small-q tile
   int prefill_min_qlen; // requests with q_len >= this go to the tensor-core kernel
   int prefill_rows;     // query rows (positions x group) per prefill tile
@@ -66,12 +68,11 @@ struct AttnParams {
   void* out;
   int max_blocks_per_seq;
   int num_q_heads, num_kv_heads, num_blocks, num_tokens;
-  int bps;
   float scale_log2;      // softmax scale * log2(e)
   const int* n_items;    // device count of work items (x num_kv_heads units)
   int* next;             // device work counter (zeroed by the plan kernel)
-  const int4* items;     // {r, m, s, tile}
-  const int2* tiles;     // {first item, number of splits}
+  const int4* items;     // {r, m, first KV block, tile}
+  const int4* tiles;     // {first item, number of splits, KV blocks per split, 0}
   int* merge_cnt;        // [tiles][num_kv_heads]
   float* part_acc;       // [items][num_kv_heads][rows][D]
   float* part_ml;        // [items][num_kv_heads][rows][2]

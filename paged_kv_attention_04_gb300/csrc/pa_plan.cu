@@ -52,6 +52,12 @@ __device__ int block_exclusive_scan(int v, int* warp_sums, int& total) {
 
 __device__ __forceinline__ int ceil_div(int a, int b) { return (a + b - 1) / b; }
 
+// KV blocks per split for a request with nb KV blocks: at least bps, large
+// enough that a tile has at most kMaxSplits splits, at most kMaxUnitBlocks.
+__device__ __forceinline__ int request_bps(int nb, int bps) {
+  return min(max(bps, ceil_div(nb, kMaxSplits)), kMaxUnitBlocks);
+}
+
 // Number of KV splits of a tile whose last query row sits at position pos_last.
 __device__ __forceinline__ int splits_for(int pos_last, int bps) {
   return ceil_div(ceil_div(pos_last + 1, kBlockSize), bps);
@@ -83,9 +89,9 @@ __global__ void __launch_bounds__(kPlanThreads, 1) plan_kernel(PlanParams p) {
   int* pfx_st = reinterpret_cast<int*>(ws + p.lay.pfx_s_tiles);
   int* pfx_pt = reinterpret_cast<int*>(ws + p.lay.pfx_p_tiles);
   int4* items_d = reinterpret_cast<int4*>(ws + p.lay.items_d);
-  int2* tiles_d = reinterpret_cast<int2*>(ws + p.lay.tiles_d);
+  int4* tiles_d = reinterpret_cast<int4*>(ws + p.lay.tiles_d);
   int4* items_s = reinterpret_cast<int4*>(ws + p.lay.items_s);
-  int2* tiles_s = reinterpret_cast<int2*>(ws + p.lay.tiles_s);
+  int4* tiles_s = reinterpret_cast<int4*>(ws + p.lay.tiles_s);
   int* cnt_d = reinterpret_cast<int*>(ws + p.lay.cnt_d);
   int* cnt_s = reinterpret_cast<int*>(ws + p.lay.cnt_s);
 
@@ -115,16 +121,17 @@ __global__ void __launch_bounds__(kPlanThreads, 1) plan_kernel(PlanParams p) {
       } else if (L == 1) {
         c = kClassDecode;
         nd_tiles = 1;
-        nd_items = splits_for(S - 1, p.bps);
+        nd_items = splits_for(S - 1, request_bps(ceil_div(S, kBlockSize), p.bps));
       } else if (L >= p.prefill_min_qlen) {
         c = kClassPrefill;
         np_tiles = ceil_div(L * p.group, p.prefill_rows);
       } else {
         c = kClassSmall;
         ns_tiles = ceil_div(L, p.small_positions);
+        const int rb = request_bps(ceil_div(S, kBlockSize), p.bps);
         for (int m = 0; m < ns_tiles; ++m) {
           const int last = min(L, (m + 1) * p.small_positions) - 1;
-          ns_items += splits_for(S - L + last, p.bps);
+          ns_items += splits_for(S - L + last, rb);
         }
       }
       cls[r] = c;
@@ -171,8 +178,9 @@ __global__ void __launch_bounds__(kPlanThreads, 1) plan_kernel(PlanParams p) {
     const int r = find_owner(pfx_di, B, i);
     const int s = i - pfx_di[r];
     const int tile = pfx_dt[r];
-    items_d[i] = make_int4(r, 0, s, tile);
-    if (s == 0) tiles_d[tile] = make_int2(i, pfx_di[r + 1] - pfx_di[r]);
+    const int rb = request_bps(ceil_div(__ldg(p.seq_lens + r), kBlockSize), p.bps);
+    items_d[i] = make_int4(r, 0, s * rb, tile);
+    if (s == 0) tiles_d[tile] = make_int4(i, pfx_di[r + 1] - pfx_di[r], rb, 0);
   }
   // Small-q tiles: each thread expands one tile into its splits.
   for (int tile = threadIdx.x; tile < n_st; tile += kPlanThreads) {
@@ -180,12 +188,13 @@ __global__ void __launch_bounds__(kPlanThreads, 1) plan_kernel(PlanParams p) {
     const int m = tile - pfx_st[r];
     const int S = __ldg(p.seq_lens + r);
     const int L = __ldg(p.qsl + r + 1) - __ldg(p.qsl + r);
+    const int rb = request_bps(ceil_div(S, kBlockSize), p.bps);
     int first = pfx_si[r];
     for (int mm = 0; mm < m; ++mm)
-      first += splits_for(S - L + min(L, (mm + 1) * p.small_positions) - 1, p.bps);
-    const int ns = splits_for(S - L + min(L, (m + 1) * p.small_positions) - 1, p.bps);
-    for (int s = 0; s < ns; ++s) items_s[first + s] = make_int4(r, m, s, tile);
-    tiles_s[tile] = make_int2(first, ns);
+      first += splits_for(S - L + min(L, (mm + 1) * p.small_positions) - 1, rb);
+    const int ns = splits_for(S - L + min(L, (m + 1) * p.small_positions) - 1, rb);
+    for (int s = 0; s < ns; ++s) items_s[first + s] = make_int4(r, m, s * rb, tile);
+    tiles_s[tile] = make_int4(first, ns, rb, 0);
   }
   for (int i = threadIdx.x; i < n_dt * p.num_kv_heads; i += kPlanThreads) cnt_d[i] = 0;
   for (int i = threadIdx.x; i < n_st * p.num_kv_heads; i += kPlanThreads) cnt_s[i] = 0;
