@@ -535,11 +535,12 @@ def run_ncu_case(spec_arg: str, iters: int = 3) -> None:
     build.build()
     name, _, n = spec_arg.partition(":")
     spec = W.CONFIGS[name]()
-    if n:
-        spec.seq_lens = spec.seq_lens[:int(n)]
-        spec.q_lens = spec.q_lens[:int(n)]
+    if n:  # N: the first N requests; -N: the last N
+        sl = slice(None, int(n)) if int(n) > 0 else slice(int(n), None)
+        spec.seq_lens = spec.seq_lens[sl]
+        spec.q_lens = spec.q_lens[sl]
         if spec.sharing is not None:
-            spec.sharing = spec.sharing[:int(n)]
+            spec.sharing = spec.sharing[sl]
     st = W.make_step(spec, device="cuda")
     lay = P.layout_of(st.k_cache, spec.num_q_heads)
     ws = P.alloc_workspace(lay, spec.num_seqs, spec.num_tokens, st.max_seq_len)
@@ -566,7 +567,8 @@ def main():
     ap.add_argument("--oracle-seconds", type=float, default=10.0)
     ap.add_argument("--oracle-stride", type=int, default=1)
     ap.add_argument("--ncu-case", default=None,
-                    help="run a small step for a profiler: NAME or NAME:N (first N requests)")
+                    help="run a small step for a profiler: NAME, NAME:N (first N requests) "
+                         "or NAME:-N (last N)")
     ap.add_argument("--oracle-budget", type=float, default=1.0, help=argparse.SUPPRESS)
     ap.add_argument("--oracle-worker", default=None, help=argparse.SUPPRESS)
     args = ap.parse_args()

@@ -65,6 +65,7 @@ typedef enum { PA_F32 = 0, PA_BF16 = 1 } pa_dtype;
 #define PA_DEV_QSL 4          /* query_start_loc not 0-based, decreasing, or not ending at num_tokens */
 #define PA_DEV_LENGTHS 8      /* q_len < 1, q_len > seq_len, or a host upper bound exceeded */
 #define PA_DEV_CAPACITY 16    /* the workspace was sized for a smaller step */
+#define PA_DEV_TIMEOUT 32     /* a tensor-core wait gave up; that kernel stopped early */
 
 /* Model-side shape of the KV cache. Supported: block_size 16; head_size 64
  * or 128; num_q_heads / num_kv_heads in {1, 2, 4, 8}; dtype f32 or bf16. */

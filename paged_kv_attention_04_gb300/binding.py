@@ -16,6 +16,7 @@ LIB_PATH = os.path.join(_PKG, "libpa.so")
 PA_OK, PA_ERR_INVALID, PA_ERR_UNSUPPORTED, PA_ERR_CUDA = 0, 1, 2, 3
 PA_F32, PA_BF16 = 0, 1
 PA_DEV_SLOT_RANGE, PA_DEV_BLOCK_RANGE, PA_DEV_QSL, PA_DEV_LENGTHS, PA_DEV_CAPACITY = 1, 2, 4, 8, 16
+PA_DEV_TIMEOUT = 32
 
 _DTYPES = {torch.float32: PA_F32, torch.bfloat16: PA_BF16}
 

@@ -94,7 +94,8 @@ Capacity capacity(const pa_layout* L, int B, int T, int max_seq_len) {
   c.decode_items = static_cast<long long>(B) * splits;
   c.small_tiles = (T > B ? cdiv(T - B, small_positions(L)) : 0) + multi;
   c.small_items = c.small_tiles * splits;
-  c.prefill_tiles = 0;
+  const long long group = L->num_q_heads / L->num_kv_heads;
+  c.prefill_tiles = L->dtype == PA_BF16 ? cdiv(static_cast<long long>(T) * group, kPrefillRows) + multi : 0;
   return c;
 }
 
@@ -255,8 +256,9 @@ int pa_forward(const void* q, const void* k_cache, const void* v_cache,
   pp.max_blocks_per_seq = max_blocks_per_seq;
   pp.bps = blocks_per_split(layout);
   pp.small_positions = small_positions(layout);
-  pp.prefill_min_qlen = 0x7fffffff;
-  pp.prefill_rows = 128;
+  const bool tc_prefill = layout->dtype == PA_BF16;
+  pp.prefill_min_qlen = tc_prefill ? kPrefillMinQlen : 0x7fffffff;
+  pp.prefill_rows = kPrefillRows;
   pp.group = group;
   pp.num_kv_heads = layout->num_kv_heads;
   pp.cap = cap;
@@ -306,6 +308,17 @@ int pa_forward(const void* q, const void* k_cache, const void* v_cache,
     e = launch_attn_cuda_core(ap, layout->dtype, layout->head_size, group, small_positions(layout),
                               num_sms, st);
     if (e != cudaSuccess) return fail_cuda(e, "small-q attention launch");
+  }
+  if (tc_prefill && max_query_len >= kPrefillMinQlen) {
+    ap.n_items = hdr + kHdrPrefillTiles;
+    ap.next = hdr + kHdrPrefillNext;
+    ap.items = reinterpret_cast<const int4*>(ws + lay.tiles_p);
+    ap.tiles = nullptr;
+    ap.merge_cnt = nullptr;
+    ap.part_acc = nullptr;
+    ap.part_ml = nullptr;
+    e = launch_prefill_tc(ap, layout->head_size, group, num_sms, st);
+    if (e != cudaSuccess) return fail_cuda(e, "prefill attention launch");
   }
   return PA_OK;
 }

@@ -12,6 +12,8 @@ constexpr int kBlockSize = 16;        // tokens per KV block
 constexpr int kSmallRows = 16;        // query rows (positions x grouped heads) per few-token tile
 constexpr int kMaxSplits = 64;        // KV splits per tile are kept at or below this ...
 constexpr int kMaxUnitBlocks = 256;   // ... unless a split would exceed this many blocks
+constexpr int kPrefillRows = 128;     // query rows per tensor-core prefill tile
+constexpr int kPrefillMinQlen = 16;   // bf16 chunks at least this long use the tensor-core kernel
 
 // Work-list classes written by the plan kernel.
 enum ReqClass : int { kClassNone = 0, kClassDecode = 1, kClassSmall = 2, kClassPrefill = 3 };
@@ -92,6 +94,9 @@ cudaError_t launch_cache_write(const void* k, const void* v, const int64_t* slot
 cudaError_t launch_plan(const PlanParams& p, cudaStream_t stream);
 // CUDA-core split-KV attention.  positions: 1 (decode list) or the small-q
 // tile height.  Returns cudaErrorInvalidValue for an unbuilt combination.
+// Tensor-core (tcgen05) chunked-prefill attention over the prefill list.
+cudaError_t launch_prefill_tc(const AttnParams& p, int head_size, int group, int num_sms,
+                              cudaStream_t stream);
 cudaError_t launch_attn_cuda_core(const AttnParams& p, pa_dtype dtype, int head_size, int group,
                                   int positions, int num_sms, cudaStream_t stream);
 

@@ -124,7 +124,7 @@ __global__ void __launch_bounds__(kPlanThreads, 1) plan_kernel(PlanParams p) {
         nd_items = splits_for(S - 1, request_bps(ceil_div(S, kBlockSize), p.bps));
       } else if (L >= p.prefill_min_qlen) {
         c = kClassPrefill;
-        np_tiles = ceil_div(L * p.group, p.prefill_rows);
+        np_tiles = ceil_div(L, p.prefill_rows / p.group);
       } else {
         c = kClassSmall;
         ns_tiles = ceil_div(L, p.small_positions);
@@ -195,6 +195,12 @@ __global__ void __launch_bounds__(kPlanThreads, 1) plan_kernel(PlanParams p) {
     const int ns = splits_for(S - L + min(L, (m + 1) * p.small_positions) - 1, rb);
     for (int s = 0; s < ns; ++s) items_s[first + s] = make_int4(r, m, s * rb, tile);
     tiles_s[tile] = make_int4(first, ns, rb, 0);
+  }
+  // Prefill tiles: 128 query rows (positions x grouped heads) each.
+  int4* tiles_p = reinterpret_cast<int4*>(ws + p.lay.tiles_p);
+  for (int tile = threadIdx.x; tile < n_pt; tile += kPlanThreads) {
+    const int r = find_owner(pfx_pt, B, tile);
+    tiles_p[tile] = make_int4(r, tile - pfx_pt[r], 0, 0);
   }
   for (int i = threadIdx.x; i < n_dt * p.num_kv_heads; i += kPlanThreads) cnt_d[i] = 0;
   for (int i = threadIdx.x; i < n_st * p.num_kv_heads; i += kPlanThreads) cnt_s[i] = 0;
