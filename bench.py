@@ -299,13 +299,22 @@ def dist_setup():
 
 
 def dist_max(x: float, world: int) -> float:
+    """Maximum of x over all ranks (x itself on one rank).  Uses the process
+    group's backend: CUDA tensors under nccl, CPU tensors under gloo."""
     if world == 1:
         return x
     import torch
     import torch.distributed as dist
-    t = torch.tensor([x], dtype=torch.float64, device="cuda")
+    dev = "cuda" if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([x], dtype=torch.float64, device=dev)
     dist.all_reduce(t, op=dist.ReduceOp.MAX)
     return float(t.item())
+
+
+def replica_value(bytes_per_rank: float, ms_max: float, world: int) -> float:
+    """Whole-job GB/s for `world` replicas that each moved bytes_per_rank, timed
+    by the slowest rank."""
+    return world * bytes_per_rank / (ms_max * 1e-3) / 1e9
 
 
 def barrier(world: int):
@@ -436,10 +445,10 @@ def run_gpu_arm(args):
     ms_max = dist_max(ms, world)
     dec_max = dist_max(dec_ms, world)
     w = runner.work
-    value = world * w["step_bytes"] / (ms_max * 1e-3) / 1e9
+    value = replica_value(w["step_bytes"], ms_max, world)
     e2e_ms, h2d, d2h = runner.time_e2e(max(3, args.steps // 4), max(3, args.warmup), world)
     e2e_ms = dist_max(e2e_ms, world)
-    e2e_value = world * w["step_bytes"] / (e2e_ms * 1e-3) / 1e9
+    e2e_value = replica_value(w["step_bytes"], e2e_ms, world)
     peak, peak_src = measured_peaks()
     achieved = w["decode_bytes"] / (dec_max * 1e-3) / 1e9
     traffic = recorded_traffic(HEADLINE)
