@@ -358,33 +358,83 @@ class StepRunner:
                      st.max_query_len, st.max_seq_len, st.scale, self.out, self.ws, self.layout,
                      self.status)
 
-    def time_device(self, steps: int, warmup: int, world: int, clocks: ClockSampler | None = None):
-        """Inputs resident in HBM; returns (ms per step, decode-kernel ms per launch,
-        forward ms per call)."""
+    def flush_l2(self):
+        """Write 256 MiB (twice the L2) so the next step starts with a cold L2."""
+        if not hasattr(self, "_flush"):
+            self._flush = self.torch.empty(256 << 20, dtype=self.torch.uint8, device="cuda")
+        self._flush.zero_()
+
+    def time_device(self, steps: int, warmup: int, world: int, clocks: ClockSampler | None = None,
+                    flush: bool = False):
+        """Inputs resident in HBM; returns (ms per step, decode-kernel ms per launch).
+        With flush, L2 is flushed before every step, outside the timed events."""
         torch, P = self.torch, self.P
         for _ in range(warmup):
             self.step()
         torch.cuda.synchronize()
         evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
                for _ in range(steps)]
+        steps_ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+                    for _ in range(steps if flush else 1)]
         barrier(world)
         torch.cuda.synchronize()
         if clocks:
             clocks.mark("timed_start")
-        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        e0.record()
+        if not flush:
+            steps_ev[0][0].record()
         for i in range(steps):
+            if flush:
+                self.flush_l2()
+                steps_ev[i][0].record()
             P.pa_set_profile_events(evs[i][0], evs[i][1])
             self.step()
-        e1.record()
+            if flush:
+                steps_ev[i][1].record()
+        if not flush:
+            steps_ev[0][1].record()
         torch.cuda.synchronize()
         if clocks:
             clocks.mark("timed_end")
         barrier(world)
         P.pa_set_profile_events(None, None)
-        total_ms = e0.elapsed_time(e1)
+        total_ms = sum(a.elapsed_time(b) for a, b in steps_ev)
         dec_ms = statistics.mean(a.elapsed_time(b) for a, b in evs)
         return total_ms / steps, dec_ms
+
+    def time_graph(self, steps: int, warmup: int, world: int, flush: bool = False) -> float:
+        """The same step captured once in a CUDA graph and replayed; ms per step
+        (with flush, L2 is flushed before every replay, outside the timed events)."""
+        torch = self.torch
+        self.step()  # per-device set-up happens on an eager call, before capture
+        torch.cuda.synchronize()
+        s = torch.cuda.Stream()
+        s.wait_stream(torch.cuda.current_stream())
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.stream(s):
+            with torch.cuda.graph(g):
+                self.step()
+        torch.cuda.current_stream().wait_stream(s)
+        for _ in range(warmup):
+            g.replay()
+        torch.cuda.synchronize()
+        barrier(world)
+        evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+               for _ in range(steps if flush else 1)]
+        if not flush:
+            evs[0][0].record()
+        for i in range(steps):
+            if flush:
+                self.flush_l2()
+                evs[i][0].record()
+            g.replay()
+            if flush:
+                evs[i][1].record()
+        if not flush:
+            evs[0][1].record()
+        torch.cuda.synchronize()
+        barrier(world)
+        del g
+        return sum(a.elapsed_time(b) for a, b in evs) / steps
 
     def time_e2e(self, steps: int, warmup: int, world: int):
         """Same step with this step's inputs copied from pinned host memory
@@ -446,6 +496,7 @@ def run_gpu_arm(args):
     dec_max = dist_max(dec_ms, world)
     w = runner.work
     value = replica_value(w["step_bytes"], ms_max, world)
+    graph_ms = dist_max(runner.time_graph(args.steps, args.warmup, world), world)
     e2e_ms, h2d, d2h = runner.time_e2e(max(3, args.steps // 4), max(3, args.warmup), world)
     e2e_ms = dist_max(e2e_ms, world)
     e2e_value = replica_value(w["step_bytes"], e2e_ms, world)
@@ -471,9 +522,28 @@ def run_gpu_arm(args):
         "chunk_and_write_ms": rest_ms,
         "chunk_tflops_upper": mw["chunk_flops"] / (rest_ms * 1e-3) / 1e12,
     }
+    mixed_info["graph_ms_per_step"] = dist_max(mixed.time_graph(max(3, args.steps // 2),
+                                                                 args.warmup, world), world)
     if int(mixed.status.item()) != 0:
         raise RuntimeError(f"mixed-step device status {int(mixed.status.item())}")
     del mixed
+    torch.cuda.empty_cache()
+
+    # a small decode step (79 MB of KV) where launch overhead is visible
+    small = StepRunner("tinyllama_decode", seed_offset=rank * 1000 if world > 1 else 0)
+    sms, sdec = small.time_device(args.steps, args.warmup, world, flush=True)
+    sms, sdec = dist_max(sms, world), dist_max(sdec, world)
+    sgraph = dist_max(small.time_graph(args.steps, args.warmup, world, flush=True), world)
+    sw = small.work
+    small_info = {
+        "workload": "TinyLlama-1.1B single-layer decode: batch 64, 32 q / 4 kv heads, D=64, bf16, "
+                    "context U[128,2048]",
+        "ms_per_step": sms, "graph_ms_per_step": sgraph, "decode_kernel_ms": sdec,
+        "decode_gbs": sw["decode_bytes"] / (sdec * 1e-3) / 1e9,
+        "graph_step_gbs": world * sw["step_bytes"] / (sgraph * 1e-3) / 1e9,
+        "l2": "flushed (256 MiB write) before every step, outside the timed events",
+    }
+    del small
     torch.cuda.empty_cache()
 
     line = {
@@ -490,9 +560,11 @@ def run_gpu_arm(args):
                      "algorithmic_bytes_per_launch": w["decode_bytes"], "kernel_ms": dec_max},
         "e2e": {"value": e2e_value, "unit": "GB/s", "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms},
+        "graph_ms_per_step": graph_ms,
         "gpu_launches": launches,
         "clocks": clock_info,
         "mixed": mixed_info,
+        "tinyllama_decode": small_info,
     }
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         o = time_oracle(HEADLINE, min_seconds=args.oracle_seconds, stride=args.oracle_stride)

@@ -23,31 +23,48 @@ namespace {
 
 constexpr int kPlanThreads = 1024;
 
-// Exclusive scan of one int per thread across the CTA; returns the CTA total.
-__device__ int block_exclusive_scan(int v, int* warp_sums, int& total) {
+constexpr int kLists = 5;  // decode items, decode tiles, small items, small tiles, prefill tiles
+
+// Exclusive scan of kLists ints per thread across the CTA, all lists at once;
+// `total` receives each list's CTA total.
+__device__ void block_exclusive_scan(int (&v)[kLists], int (*warp_sums)[kLists],
+                                     int (&total)[kLists]) {
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  int x = v;
+  int x[kLists];
+#pragma unroll
+  for (int k = 0; k < kLists; ++k) x[k] = v[k];
 #pragma unroll
   for (int o = 1; o < 32; o <<= 1) {
-    const int y = __shfl_up_sync(0xffffffffu, x, o);
-    if (lane >= o) x += y;
+#pragma unroll
+    for (int k = 0; k < kLists; ++k) {
+      const int y = __shfl_up_sync(0xffffffffu, x[k], o);
+      if (lane >= o) x[k] += y;
+    }
   }
-  if (lane == 31) warp_sums[warp] = x;
+  if (lane == 31) {
+#pragma unroll
+    for (int k = 0; k < kLists; ++k) warp_sums[warp][k] = x[k];
+  }
   __syncthreads();
   if (warp == 0) {
-    int w = (lane < (kPlanThreads / 32)) ? warp_sums[lane] : 0;
 #pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-      const int y = __shfl_up_sync(0xffffffffu, w, o);
-      if (lane >= o) w += y;
+    for (int k = 0; k < kLists; ++k) {
+      int w = (lane < (kPlanThreads / 32)) ? warp_sums[lane][k] : 0;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int y = __shfl_up_sync(0xffffffffu, w, o);
+        if (lane >= o) w += y;
+      }
+      warp_sums[lane][k] = w;  // inclusive
     }
-    warp_sums[lane] = w;  // inclusive
   }
   __syncthreads();
-  const int before = (warp > 0 ? warp_sums[warp - 1] : 0) + x - v;
-  total = warp_sums[kPlanThreads / 32 - 1];
+#pragma unroll
+  for (int k = 0; k < kLists; ++k) {
+    v[k] = (warp > 0 ? warp_sums[warp - 1][k] : 0) + x[k] - v[k];
+    total[k] = warp_sums[kPlanThreads / 32 - 1][k];
+  }
   __syncthreads();
-  return before;
 }
 
 __device__ __forceinline__ int ceil_div(int a, int b) { return (a + b - 1) / b; }
@@ -76,8 +93,8 @@ __device__ int find_owner(const int* pfx, int n, int i) {
 }  // namespace
 
 __global__ void __launch_bounds__(kPlanThreads, 1) plan_kernel(PlanParams p) {
-  __shared__ int warp_sums[32];
-  __shared__ int carry[5];
+  __shared__ int warp_sums[32][kLists];
+  __shared__ int carry[kLists];
   __shared__ int err;
   const int B = p.num_seqs;
   char* ws = p.ws;
@@ -104,9 +121,11 @@ __global__ void __launch_bounds__(kPlanThreads, 1) plan_kernel(PlanParams p) {
   __syncthreads();
 
   // Pass 1: classify and count, with a running exclusive scan per list.
+  int carry_r[kLists] = {0, 0, 0, 0, 0};
   for (int base = 0; base < B; base += kPlanThreads) {
     const int r = base + threadIdx.x;
-    int c = kClassNone, nd_items = 0, nd_tiles = 0, ns_items = 0, ns_tiles = 0, np_tiles = 0;
+    int c = kClassNone;
+    int cnt[kLists] = {0, 0, 0, 0, 0};
     if (r < B) {
       const int S = __ldg(p.seq_lens + r);
       const int a = __ldg(p.qsl + r), b = __ldg(p.qsl + r + 1);
@@ -120,40 +139,37 @@ __global__ void __launch_bounds__(kPlanThreads, 1) plan_kernel(PlanParams p) {
         atomicOr(&err, e);
       } else if (L == 1) {
         c = kClassDecode;
-        nd_tiles = 1;
-        nd_items = splits_for(S - 1, request_bps(ceil_div(S, kBlockSize), p.bps));
+        cnt[1] = 1;
+        cnt[0] = splits_for(S - 1, request_bps(ceil_div(S, kBlockSize), p.bps));
       } else if (L >= p.prefill_min_qlen) {
         c = kClassPrefill;
-        np_tiles = ceil_div(L, p.prefill_rows / p.group);
+        cnt[4] = ceil_div(L, p.prefill_rows / p.group);
       } else {
         c = kClassSmall;
-        ns_tiles = ceil_div(L, p.small_positions);
+        cnt[3] = ceil_div(L, p.small_positions);
         const int rb = request_bps(ceil_div(S, kBlockSize), p.bps);
-        for (int m = 0; m < ns_tiles; ++m) {
+        for (int m = 0; m < cnt[3]; ++m) {
           const int last = min(L, (m + 1) * p.small_positions) - 1;
-          ns_items += splits_for(S - L + last, rb);
+          cnt[2] += splits_for(S - L + last, rb);
         }
       }
       cls[r] = c;
     }
-    int tot;
-    const int o_di = block_exclusive_scan(nd_items, warp_sums, tot);
-    const int c_di = carry[0]; __syncthreads(); if (threadIdx.x == 0) carry[0] += tot;
-    const int o_dt = block_exclusive_scan(nd_tiles, warp_sums, tot);
-    const int c_dt = carry[1]; __syncthreads(); if (threadIdx.x == 0) carry[1] += tot;
-    const int o_si = block_exclusive_scan(ns_items, warp_sums, tot);
-    const int c_si = carry[2]; __syncthreads(); if (threadIdx.x == 0) carry[2] += tot;
-    const int o_st = block_exclusive_scan(ns_tiles, warp_sums, tot);
-    const int c_st = carry[3]; __syncthreads(); if (threadIdx.x == 0) carry[3] += tot;
-    const int o_pt = block_exclusive_scan(np_tiles, warp_sums, tot);
-    const int c_pt = carry[4]; __syncthreads(); if (threadIdx.x == 0) carry[4] += tot;
+    int tot[kLists];
+    block_exclusive_scan(cnt, warp_sums, tot);
     if (r < B) {
-      pfx_di[r] = c_di + o_di; pfx_dt[r] = c_dt + o_dt;
-      pfx_si[r] = c_si + o_si; pfx_st[r] = c_st + o_st;
-      pfx_pt[r] = c_pt + o_pt;
+      pfx_di[r] = carry_r[0] + cnt[0]; pfx_dt[r] = carry_r[1] + cnt[1];
+      pfx_si[r] = carry_r[2] + cnt[2]; pfx_st[r] = carry_r[3] + cnt[3];
+      pfx_pt[r] = carry_r[4] + cnt[4];
     }
-    __syncthreads();
+#pragma unroll
+    for (int k = 0; k < kLists; ++k) carry_r[k] += tot[k];
   }
+  if (threadIdx.x == 0) {
+#pragma unroll
+    for (int k = 0; k < kLists; ++k) carry[k] = carry_r[k];
+  }
+  __syncthreads();
   if (threadIdx.x == 0) {
     pfx_di[B] = carry[0]; pfx_dt[B] = carry[1]; pfx_si[B] = carry[2];
     pfx_st[B] = carry[3]; pfx_pt[B] = carry[4];
