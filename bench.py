@@ -81,11 +81,13 @@ def step_work(spec, meta) -> dict:
     n_chk_tok = int(sum(L for L in spec.q_lens if L > 1))
     uniq = lambda lst: int(len(np.unique(np.concatenate(lst)))) if lst else 0  # noqa: E731
     meta_bytes = 4 * (2 * spec.num_seqs + 1)
-    decode_bytes = (uniq(dec_slots) * row * 2 + 2 * n_dec * Hq * D * e + 4 * table_dec + meta_bytes)
+    kv_bytes = uniq(dec_slots) * row * 2
+    decode_bytes = (kv_bytes + 2 * n_dec * Hq * D * e + 4 * table_dec + meta_bytes)
     chunk_bytes = (uniq(chk_slots) * row * 2 + 2 * n_chk_tok * Hq * D * e + 4 * table_chk)
     T = spec.num_tokens
     write_bytes = 2 * 2 * T * row + 8 * T
-    return dict(decode_bytes=decode_bytes, chunk_bytes=chunk_bytes, write_bytes=write_bytes,
+    return dict(decode_bytes=decode_bytes, kv_bytes=kv_bytes, chunk_bytes=chunk_bytes,
+                write_bytes=write_bytes,
                 step_bytes=decode_bytes + chunk_bytes + write_bytes,
                 chunk_flops=4.0 * D * Hq * pairs, tokens=T)
 
@@ -326,7 +328,7 @@ def barrier(world: int):
 class StepRunner:
     """Device-resident step of one workload through the C ABI."""
 
-    def __init__(self, name: str, seed_offset: int = 0):
+    def __init__(self, name: str, seed_offset: int = 0, fp8_scales: tuple | None = None):
         import torch
 
         import paged_kv_attention_04_gb300 as P
@@ -340,7 +342,14 @@ class StepRunner:
         self.meta = W.make_meta(spec)
         self.st = W.make_step(spec, device="cuda")
         st = self.st
-        self.layout = P.layout_of(st.k_cache, spec.num_q_heads)
+        if fp8_scales:
+            # 8-bit cache: the bf16 history pool as E4M3 codes of x / scale
+            ks, vs = fp8_scales
+            st.k_cache = (st.k_cache.float() / ks).clamp(-448, 448).to(torch.float8_e4m3fn).view(torch.uint8)
+            st.v_cache = (st.v_cache.float() / vs).clamp(-448, 448).to(torch.float8_e4m3fn).view(torch.uint8)
+            self.layout = P.layout_of(st.k_cache, spec.num_q_heads, k_scale=ks, v_scale=vs)
+        else:
+            self.layout = P.layout_of(st.k_cache, spec.num_q_heads)
         self.ws = P.alloc_workspace(self.layout, spec.num_seqs, spec.num_tokens, st.max_seq_len)
         self.out = torch.empty_like(st.q)
         self.status = torch.zeros(1, dtype=torch.int32, device="cuda")
@@ -529,6 +538,23 @@ def run_gpu_arm(args):
     del mixed
     torch.cuda.empty_cache()
 
+    # the headline shape over an 8-bit (E4M3) KV cache: half the KV bytes per token
+    f8 = StepRunner(HEADLINE, seed_offset=rank * 1000 if world > 1 else 0, fp8_scales=(0.01, 0.01))
+    fms, fdec = f8.time_device(args.steps, args.warmup, world)
+    fms, fdec = dist_max(fms, world), dist_max(fdec, world)
+    fkv = f8.work["decode_bytes"] - f8.work["kv_bytes"] // 2  # KV counted at 1 byte/element
+    fp8_info = {
+        "workload": WORKLOAD_TEXT[HEADLINE] + ", KV cache FP8 E4M3 (per-tensor scales)",
+        "ms_per_step": fms, "decode_kernel_ms": fdec,
+        "decode_gbs": fkv / (fdec * 1e-3) / 1e9,
+        "decode_frac_of_peak": fkv / (fdec * 1e-3) / 1e9 / measured_peaks()[0],
+        "tokens_per_s": world * f8.spec.num_tokens / (fms * 1e-3),
+    }
+    if int(f8.status.item()) != 0:
+        raise RuntimeError(f"fp8 step device status {int(f8.status.item())}")
+    del f8
+    torch.cuda.empty_cache()
+
     # a small decode step (79 MB of KV) where launch overhead is visible
     small = StepRunner("tinyllama_decode", seed_offset=rank * 1000 if world > 1 else 0)
     sms, sdec = small.time_device(args.steps, args.warmup, world, flush=True)
@@ -565,6 +591,7 @@ def run_gpu_arm(args):
         "clocks": clock_info,
         "mixed": mixed_info,
         "tinyllama_decode": small_info,
+        "fp8_kv": fp8_info,
     }
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         o = time_oracle(HEADLINE, min_seconds=args.oracle_seconds, stride=args.oracle_stride)

@@ -32,7 +32,7 @@
  *   - Shapes:  q, out        [num_tokens][num_q_heads][head_size]
  *              k, v          [num_tokens][num_kv_heads][head_size]
  *              k_cache, v_cache [num_blocks][block_size][num_kv_heads][head_size]
- *     Element type is layout->dtype for all of them.
+ *     Element type is layout->dtype, except the caches: layout->cache_dtype.
  *   - Return value: PA_OK, or an error code with a message for
  *     pa_last_error().  Argument errors are found on the host before anything
  *     is launched.  Values that live in device memory (slots, block ids,
@@ -57,7 +57,7 @@ typedef enum {
   PA_ERR_CUDA = 3          /* a CUDA runtime call or launch failed */
 } pa_status;
 
-typedef enum { PA_F32 = 0, PA_BF16 = 1 } pa_dtype;
+typedef enum { PA_F32 = 0, PA_BF16 = 1, PA_FP8_E4M3 = 2 } pa_dtype;
 
 /* Bits the kernels OR into the optional device status word. */
 #define PA_DEV_SLOT_RANGE 1   /* slot >= num_blocks*block_size: that token's write skipped */
@@ -68,7 +68,16 @@ typedef enum { PA_F32 = 0, PA_BF16 = 1 } pa_dtype;
 #define PA_DEV_TIMEOUT 32     /* a tensor-core wait gave up; that kernel stopped early */
 
 /* Model-side shape of the KV cache. Supported: block_size 16; head_size 64
- * or 128; num_q_heads / num_kv_heads in {1, 2, 4, 8}; dtype f32 or bf16. */
+ * or 128; num_q_heads / num_kv_heads in {1, 2, 4, 8}.
+ *   dtype        element type of q, out and the new k, v: PA_F32 or PA_BF16.
+ *   cache_dtype  element type of k_cache / v_cache: equal to dtype, or
+ *                PA_FP8_E4M3 with dtype PA_BF16 (8-bit KV; "Serving models at
+ *                scale with vLLM", section Your model is too big: KV data can
+ *                be kept at 8-bit precision).  An FP8 element holds
+ *                code = E4M3(x / scale) (float32 division, round to nearest
+ *                even, saturating at +-448) and stands for code * scale.
+ *   k_scale, v_scale  the per-tensor scales of an FP8 cache (finite, > 0);
+ *                ignored otherwise. */
 typedef struct {
   int num_q_heads;
   int num_kv_heads;
@@ -76,12 +85,16 @@ typedef struct {
   int block_size;
   int num_blocks;
   pa_dtype dtype;
+  pa_dtype cache_dtype;
+  float k_scale;
+  float v_scale;
 } pa_layout;
 
 /*
  * reshape_and_cache: for every t < num_tokens with s = slot_mapping[t] >= 0,
  * copy k[t] and v[t] (num_kv_heads x head_size elements each, bits unchanged)
  * to k_cache[s / block_size][s % block_size] and the same row of v_cache.
+ * With an FP8 cache the rows are quantised on the way (see pa_layout).
  * Tokens with s < 0 are skipped.  Slots must be distinct (two tokens writing
  * one slot race).  s >= num_blocks*block_size sets PA_DEV_SLOT_RANGE.
  *

@@ -14,7 +14,7 @@ _PKG = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_PKG, "libpa.so")
 
 PA_OK, PA_ERR_INVALID, PA_ERR_UNSUPPORTED, PA_ERR_CUDA = 0, 1, 2, 3
-PA_F32, PA_BF16 = 0, 1
+PA_F32, PA_BF16, PA_FP8_E4M3 = 0, 1, 2
 PA_DEV_SLOT_RANGE, PA_DEV_BLOCK_RANGE, PA_DEV_QSL, PA_DEV_LENGTHS, PA_DEV_CAPACITY = 1, 2, 4, 8, 16
 PA_DEV_TIMEOUT = 32
 
@@ -24,7 +24,9 @@ _DTYPES = {torch.float32: PA_F32, torch.bfloat16: PA_BF16}
 class pa_layout(ctypes.Structure):
     _fields_ = [("num_q_heads", ctypes.c_int), ("num_kv_heads", ctypes.c_int),
                 ("head_size", ctypes.c_int), ("block_size", ctypes.c_int),
-                ("num_blocks", ctypes.c_int), ("dtype", ctypes.c_int)]
+                ("num_blocks", ctypes.c_int), ("dtype", ctypes.c_int),
+                ("cache_dtype", ctypes.c_int), ("k_scale", ctypes.c_float),
+                ("v_scale", ctypes.c_float)]
 
 
 class PaError(RuntimeError):
@@ -88,14 +90,29 @@ def _stream(stream) -> int | None:
 
 
 def make_layout(num_q_heads: int, num_kv_heads: int, head_size: int, num_blocks: int,
-                dtype, block_size: int = 16) -> pa_layout:
+                dtype, block_size: int = 16, cache_dtype=None, k_scale: float = 1.0,
+                v_scale: float = 1.0) -> pa_layout:
+    """Layout of a step; cache_dtype defaults to dtype (PA_FP8_E4M3 for an 8-bit cache)."""
     code = _DTYPES[dtype] if isinstance(dtype, torch.dtype) else int(dtype)
-    return pa_layout(num_q_heads, num_kv_heads, head_size, block_size, num_blocks, code)
+    if cache_dtype is None:
+        ccode = code
+    elif isinstance(cache_dtype, torch.dtype):
+        ccode = PA_FP8_E4M3 if cache_dtype == torch.uint8 else _DTYPES[cache_dtype]
+    else:
+        ccode = int(cache_dtype)
+    return pa_layout(num_q_heads, num_kv_heads, head_size, block_size, num_blocks, code, ccode,
+                     float(k_scale), float(v_scale))
 
 
-def layout_of(k_cache: torch.Tensor, num_q_heads: int) -> pa_layout:
-    """Layout of a cache tensor [num_blocks][block_size][num_kv_heads][head_size]."""
+def layout_of(k_cache: torch.Tensor, num_q_heads: int, dtype=None, k_scale: float = 1.0,
+              v_scale: float = 1.0) -> pa_layout:
+    """Layout of a cache tensor [num_blocks][block_size][num_kv_heads][head_size].  A
+    uint8 cache holds FP8 (E4M3) codes; then `dtype` (of q/out, default bf16) and the
+    scales apply."""
     nb, bs, hkv, d = k_cache.shape
+    if k_cache.dtype == torch.uint8:
+        return make_layout(num_q_heads, hkv, d, nb, dtype or torch.bfloat16, bs, PA_FP8_E4M3,
+                           k_scale, v_scale)
     return make_layout(num_q_heads, hkv, d, nb, k_cache.dtype, bs)
 
 

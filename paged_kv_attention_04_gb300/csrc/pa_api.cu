@@ -41,7 +41,9 @@ int fail_cuda(cudaError_t e, const char* what) {
   return fail(PA_ERR_CUDA, "%s: %s", what, cudaGetErrorString(e));
 }
 
-int elem_bytes(pa_dtype t) { return t == PA_BF16 ? 2 : 4; }
+int elem_bytes(pa_dtype t) { return t == PA_FP8_E4M3 ? 1 : (t == PA_BF16 ? 2 : 4); }
+
+bool fp8_cache(const pa_layout* L) { return L->cache_dtype == PA_FP8_E4M3; }
 
 bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
 
@@ -51,6 +53,16 @@ int check_layout(const pa_layout* L) {
   if (!L) return fail(PA_ERR_INVALID, "layout is NULL");
   if (L->dtype != PA_F32 && L->dtype != PA_BF16)
     return fail(PA_ERR_INVALID, "dtype %d is not PA_F32 or PA_BF16", static_cast<int>(L->dtype));
+  if (L->cache_dtype != L->dtype) {
+    if (L->cache_dtype != PA_FP8_E4M3)
+      return fail(PA_ERR_INVALID, "cache_dtype %d must equal dtype or be PA_FP8_E4M3",
+                  static_cast<int>(L->cache_dtype));
+    if (L->dtype != PA_BF16)
+      return fail(PA_ERR_UNSUPPORTED, "an FP8 cache is built for bf16 q/k/v only");
+    if (!(std::isfinite(L->k_scale) && L->k_scale > 0.f && std::isfinite(L->v_scale) &&
+          L->v_scale > 0.f))
+      return fail(PA_ERR_INVALID, "FP8 cache scales must be finite and positive");
+  }
   if (L->num_q_heads <= 0 || L->num_kv_heads <= 0 || L->head_size <= 0 || L->num_blocks <= 0)
     return fail(PA_ERR_INVALID, "heads, head_size and num_blocks must be positive");
   if (L->num_q_heads % L->num_kv_heads)
@@ -74,7 +86,7 @@ int check_layout(const pa_layout* L) {
 
 // Smallest KV split, in blocks: about PA_SPLIT_KV_BYTES of K+V per work unit.
 int blocks_per_split(const pa_layout* L) {
-  const int block_kv_bytes = 2 * kBlockSize * L->head_size * elem_bytes(L->dtype);
+  const int block_kv_bytes = 2 * kBlockSize * L->head_size * elem_bytes(L->cache_dtype);
   int b = PA_SPLIT_KV_BYTES / block_kv_bytes;
   if (b > kMaxUnitBlocks) b = kMaxUnitBlocks;
   return b < 1 ? 1 : b;
@@ -95,7 +107,8 @@ Capacity capacity(const pa_layout* L, int B, int T, int max_seq_len) {
   c.small_tiles = (T > B ? cdiv(T - B, small_positions(L)) : 0) + multi;
   c.small_items = c.small_tiles * splits;
   const long long group = L->num_q_heads / L->num_kv_heads;
-  c.prefill_tiles = L->dtype == PA_BF16 ? cdiv(static_cast<long long>(T) * group, kPrefillRows) + multi : 0;
+  c.prefill_tiles = (L->dtype == PA_BF16 && !fp8_cache(L))
+                        ? cdiv(static_cast<long long>(T) * group, kPrefillRows) + multi : 0;
   return c;
 }
 
@@ -183,8 +196,15 @@ int pa_cache_write(const void* k, const void* v, const int64_t* slot_mapping, in
   if (status && !aligned(status, 4)) return fail(PA_ERR_INVALID, "status must be 4-byte aligned");
   const int row_bytes = layout->num_kv_heads * layout->head_size * elem_bytes(layout->dtype);
   const long long num_slots = static_cast<long long>(layout->num_blocks) * kBlockSize;
-  cudaError_t e = launch_cache_write(k, v, slot_mapping, num_tokens, k_cache, v_cache, row_bytes,
-                                     num_slots, status, static_cast<cudaStream_t>(stream));
+  if (fp8_cache(layout) && !aligned(k_cache, 8)) return fail(PA_ERR_INVALID, "cache alignment");
+  cudaError_t e = fp8_cache(layout)
+                      ? launch_cache_write_fp8(k, v, slot_mapping, num_tokens, k_cache, v_cache,
+                                               row_bytes, num_slots, layout->k_scale,
+                                               layout->v_scale, status,
+                                               static_cast<cudaStream_t>(stream))
+                      : launch_cache_write(k, v, slot_mapping, num_tokens, k_cache, v_cache,
+                                           row_bytes, num_slots, status,
+                                           static_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return fail_cuda(e, "cache write launch");
   return PA_OK;
 }
@@ -256,7 +276,7 @@ int pa_forward(const void* q, const void* k_cache, const void* v_cache,
   pp.max_blocks_per_seq = max_blocks_per_seq;
   pp.bps = blocks_per_split(layout);
   pp.small_positions = small_positions(layout);
-  const bool tc_prefill = layout->dtype == PA_BF16;
+  const bool tc_prefill = layout->dtype == PA_BF16 && !fp8_cache(layout);
   pp.prefill_min_qlen = tc_prefill ? kPrefillMinQlen : 0x7fffffff;
   pp.prefill_rows = kPrefillRows;
   pp.group = group;
@@ -281,7 +301,8 @@ int pa_forward(const void* q, const void* k_cache, const void* v_cache,
   ap.num_kv_heads = layout->num_kv_heads;
   ap.num_blocks = layout->num_blocks;
   ap.num_tokens = num_tokens;
-  ap.scale_log2 = scale * 1.4426950408889634f;
+  ap.scale_log2 = scale * 1.4426950408889634f * (fp8_cache(layout) ? layout->k_scale : 1.f);
+  ap.out_scale = fp8_cache(layout) ? layout->v_scale : 1.f;
   ap.status = status;
 
   // decode rows (q_len == 1)
@@ -293,7 +314,9 @@ int pa_forward(const void* q, const void* k_cache, const void* v_cache,
   ap.part_acc = reinterpret_cast<float*>(ws + lay.part_acc_d);
   ap.part_ml = reinterpret_cast<float*>(ws + lay.part_ml_d);
   if (g_prof_start) cudaEventRecord(g_prof_start, st);
-  e = launch_attn_cuda_core(ap, layout->dtype, layout->head_size, group, 1, num_sms, st);
+  e = fp8_cache(layout)
+          ? launch_attn_fp8(ap, layout->head_size, group, 1, num_sms, st)
+          : launch_attn_cuda_core(ap, layout->dtype, layout->head_size, group, 1, num_sms, st);
   if (e != cudaSuccess) return fail_cuda(e, "decode attention launch");
   if (g_prof_stop) cudaEventRecord(g_prof_stop, st);
 
@@ -305,8 +328,10 @@ int pa_forward(const void* q, const void* k_cache, const void* v_cache,
     ap.merge_cnt = reinterpret_cast<int*>(ws + lay.cnt_s);
     ap.part_acc = reinterpret_cast<float*>(ws + lay.part_acc_s);
     ap.part_ml = reinterpret_cast<float*>(ws + lay.part_ml_s);
-    e = launch_attn_cuda_core(ap, layout->dtype, layout->head_size, group, small_positions(layout),
-                              num_sms, st);
+    e = fp8_cache(layout)
+            ? launch_attn_fp8(ap, layout->head_size, group, small_positions(layout), num_sms, st)
+            : launch_attn_cuda_core(ap, layout->dtype, layout->head_size, group,
+                                    small_positions(layout), num_sms, st);
     if (e != cudaSuccess) return fail_cuda(e, "small-q attention launch");
   }
   if (tc_prefill && max_query_len >= kPrefillMinQlen) {

@@ -70,25 +70,52 @@ __device__ __forceinline__ void mma_bf16(float* d, const uint32_t* a, uint32_t b
       : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
       : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
 }
+// Same with f16 inputs (used when the cache holds FP8 codes widened to f16).
+__device__ __forceinline__ void mma_f16(float* d, const uint32_t* a, uint32_t b0, uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
+      "{%8,%9}, {%0,%1,%2,%3};\n"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
 // Two floats -> packed bf16 pair (lo in the low half), round to nearest even.
 __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
   uint32_t r;
   asm("cvt.rn.bf16x2.f32 %0, %1, %2;\n" : "=r"(r) : "f"(hi), "f"(lo));
   return r;
 }
+__device__ __forceinline__ uint32_t pack_f16(float lo, float hi) {
+  uint32_t r;
+  asm("cvt.rn.f16x2.f32 %0, %1, %2;\n" : "=r"(r) : "f"(hi), "f"(lo));
+  return r;
+}
+// Two E4M3 codes (low byte first) -> two f16 values, exactly.
+__device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint32_t codes16) {
+  uint32_t r;
+  const uint16_t c = static_cast<uint16_t>(codes16);
+  asm("cvt.rn.f16x2.e4m3x2 %0, %1;\n" : "=r"(r) : "h"(c));
+  return r;
+}
 
-template <int D, int G, int P, int NW, int NS>
+template <int D, int G, int P, int NW, int NS, bool F8>
 struct MmaCfg {
   static constexpr int kR = P * G;                 // real query rows (<= 16)
-  static constexpr int kRowBytes = D * 2;
-  static constexpr int kChunks = kRowBytes / 16;   // 16-byte chunks per row
+  static constexpr int kRowBytes = D * 2;          // a 16-bit tile row (bf16, or f16 from FP8)
+  static constexpr int kChunks = kRowBytes / 16;   // 16-byte chunks per tile row
   static constexpr int kTileBytes = kBlockSize * kRowBytes;
-  static constexpr int kStageBytes = 2 * kTileBytes;  // K then V
+  static constexpr int kCacheRowBytes = F8 ? D : D * 2;       // one cached row (token, head)
+  static constexpr int kCacheChunks = kCacheRowBytes / 16;
+  static constexpr int kRawTileBytes = F8 ? kBlockSize * D : 0;  // FP8 codes as copied
+  // A ring stage holds one block's K and V as copied: 16-bit tiles, or raw FP8
+  // codes (then each warp also owns one f16 tile pair the codes are widened into).
+  static constexpr int kStageBytes = F8 ? 2 * kRawTileBytes : 2 * kTileBytes;
+  static constexpr int kWidenBytes = F8 ? 2 * kTileBytes : 0;
+  static constexpr int kWarpRingBytes = NS * kStageBytes + kWidenBytes;
   static constexpr int kKSteps = D / 16;
   static constexpr int kNTiles = D / 8;
   static constexpr int kThreads = (NW + 1) * 32;
   static constexpr int kRingOff = 0;
-  static constexpr int kRingBytes = NW * NS * kStageBytes;
+  static constexpr int kRingBytes = NW * kWarpRingBytes;
   static constexpr int kQOff = kRingOff + kRingBytes;
   static constexpr int kQBytes = 2 * 16 * kRowBytes;
   static constexpr int kCombOff = kQOff + kQBytes;
@@ -103,7 +130,7 @@ struct MmaCfg {
   static_assert(kR <= 16, "at most 16 query rows per tile");
   static_assert(NS >= 2 && NS <= 8, "2 to 8 pipeline stages");
   static_assert(kChunks % 8 == 0, "rows must be a multiple of 128 bytes");
-  static_assert((kBlockSize * kChunks) % 32 == 0, "tile chunks must split over a warp");
+  static_assert((kBlockSize * kCacheChunks) % 32 == 0, "tile chunks must split over a warp");
 };
 
 // Swizzled byte offset of 16-byte chunk c of row t in a tile.
@@ -112,11 +139,11 @@ __device__ __forceinline__ uint32_t swz(int t, int c) {
   return static_cast<uint32_t>(t * RowBytes + ((c ^ (t & 7)) << 4));
 }
 
-template <int D, int G, int P, int NW, int NS>
-__global__ void __launch_bounds__(MmaCfg<D, G, P, NW, NS>::kThreads,
-                                  MmaCfg<D, G, P, NW, NS>::kMinCtas)
+template <int D, int G, int P, int NW, int NS, bool F8>
+__global__ void __launch_bounds__(MmaCfg<D, G, P, NW, NS, F8>::kThreads,
+                                  MmaCfg<D, G, P, NW, NS, F8>::kMinCtas)
     attn_mma_kernel(const AttnParams p) {
-  using C = MmaCfg<D, G, P, NW, NS>;
+  using C = MmaCfg<D, G, P, NW, NS, F8>;
   constexpr int R = C::kR;
   extern __shared__ __align__(128) unsigned char smem[];
 
@@ -128,7 +155,7 @@ __global__ void __launch_bounds__(MmaCfg<D, G, P, NW, NS>::kThreads,
   UnitMeta* meta = reinterpret_cast<UnitMeta*>(smem + C::kMetaOff);
   float* comb = reinterpret_cast<float*>(smem + C::kCombOff);
   float* comb_ml = reinterpret_cast<float*>(smem + C::kMlOff);
-  const uint32_t ring_u32 = smem_u32(smem + C::kRingOff) + warp * NS * C::kStageBytes;
+  const uint32_t ring_u32 = smem_u32(smem + C::kRingOff) + warp * C::kWarpRingBytes;
   const uint32_t q_u32 = smem_u32(smem + C::kQOff);
   const unsigned char* kc = static_cast<const unsigned char*>(p.k_cache);
   const unsigned char* vc = static_cast<const unsigned char*>(p.v_cache);
@@ -177,6 +204,10 @@ __global__ void __launch_bounds__(MmaCfg<D, G, P, NW, NS>::kThreads,
         if (jj < m.npos) {
           const long long tok = m.a + m.j0 + jj;
           v = __ldg(reinterpret_cast<const uint4*>(q + (tok * Hq + m.g * G + hh) * D) + c);
+          if constexpr (F8) {  // the MMAs run in f16 against widened FP8 codes
+            v = make_uint4(pack_f16(bf16_lo(v.x), bf16_hi(v.x)), pack_f16(bf16_lo(v.y), bf16_hi(v.y)),
+                           pack_f16(bf16_lo(v.z), bf16_hi(v.z)), pack_f16(bf16_lo(v.w), bf16_hi(v.w)));
+          }
         }
       }
       *reinterpret_cast<uint4*>(smem + C::kQOff + buf * 16 * C::kRowBytes +
@@ -223,18 +254,24 @@ __global__ void __launch_bounds__(MmaCfg<D, G, P, NW, NS>::kThreads,
     }
     const int valid_rows = min(kBlockSize, m.kv_hi - b * kBlockSize);
     const uint32_t st = ring_u32 + (issued % NS) * C::kStageBytes;
-    const long long row_stride = static_cast<long long>(Hkv) * C::kRowBytes;
+    const long long row_stride = static_cast<long long>(Hkv) * C::kCacheRowBytes;
     const long long base = static_cast<long long>(phys) * kBlockSize * row_stride +
-                           static_cast<long long>(m.g) * C::kRowBytes;
-    const int c = lane % C::kChunks;
+                           static_cast<long long>(m.g) * C::kCacheRowBytes;
+    const int c = lane % C::kCacheChunks;
 #pragma unroll
-    for (int k = 0; k < (kBlockSize * C::kChunks) / 32; ++k) {
-      const int t = lane / C::kChunks + k * (32 / C::kChunks);
+    for (int k = 0; k < (kBlockSize * C::kCacheChunks) / 32; ++k) {
+      const int t = lane / C::kCacheChunks + k * (32 / C::kCacheChunks);
       const long long off = base + t * row_stride + c * 16;
-      const uint32_t so = swz<C::kRowBytes>(t, c);
       const int vb = t < valid_rows ? kbytes : 0;
-      cp_async16(st + so, kc + off, vb);
-      cp_async16(st + C::kTileBytes + so, vc + off, vb);
+      if constexpr (F8) {  // raw codes, unswizzled; widened after they land
+        const uint32_t so = t * C::kCacheRowBytes + c * 16;
+        cp_async16(st + so, kc + off, vb);
+        cp_async16(st + C::kRawTileBytes + so, vc + off, vb);
+      } else {
+        const uint32_t so = swz<C::kRowBytes>(t, c);
+        cp_async16(st + so, kc + off, vb);
+        cp_async16(st + C::kTileBytes + so, vc + off, vb);
+      }
     }
     cp_async_commit();
     ++issued;
@@ -288,7 +325,7 @@ __global__ void __launch_bounds__(MmaCfg<D, G, P, NW, NS>::kThreads,
       }
       if (u.nsplit == 1) {
         const long long tok = u.a + u.j0 + jj;
-        const float inv = 1.f / den;
+        const float inv = p.out_scale / den;
         *reinterpret_cast<uint2*>(out + (tok * Hq + u.g * G + hh) * D + d) =
             make_uint2(pack_bf16(num.x * inv, num.y * inv), pack_bf16(num.z * inv, num.w * inv));
       } else {
@@ -326,7 +363,7 @@ __global__ void __launch_bounds__(MmaCfg<D, G, P, NW, NS>::kThreads,
             den = fmaf(ml.y, f, den);
           }
           const long long tok = u.a + u.j0 + jj;
-          const float inv = 1.f / den;
+          const float inv = p.out_scale / den;
           *reinterpret_cast<uint2*>(out + (tok * Hq + u.g * G + hh) * D + d) =
               make_uint2(pack_bf16(num.x * inv, num.y * inv), pack_bf16(num.z * inv, num.w * inv));
         }
@@ -375,7 +412,31 @@ __global__ void __launch_bounds__(MmaCfg<D, G, P, NW, NS>::kThreads,
       for (int i = 0; i < nb; ++i) {
         issue_one(k + 1);
         wait_for(computed);
-        const uint32_t st = ring_u32 + (computed % NS) * C::kStageBytes;
+        uint32_t st = ring_u32 + (computed % NS) * C::kStageBytes;
+        if constexpr (F8) {
+          // widen the block's FP8 codes to f16 (exact) into the warp's swizzled tile pair
+          const unsigned char* raw_st =
+              smem + C::kRingOff + warp * C::kWarpRingBytes + (computed % NS) * C::kStageBytes;
+          unsigned char* wide = smem + C::kRingOff + warp * C::kWarpRingBytes + NS * C::kStageBytes;
+#pragma unroll
+          for (int k = 0; k < (2 * kBlockSize * C::kCacheChunks) / 32; ++k) {
+            const int idx = lane + 32 * k;                 // over K then V raw chunks
+            const int kv = idx / (kBlockSize * C::kCacheChunks);
+            const int rem = idx - kv * (kBlockSize * C::kCacheChunks);
+            const int t = rem / C::kCacheChunks, rc = rem - t * C::kCacheChunks;
+            const uint4 raw = *reinterpret_cast<const uint4*>(
+                raw_st + kv * C::kRawTileBytes + t * C::kCacheRowBytes + rc * 16);
+            const uint4 lo = make_uint4(e4m3x2_to_f16x2(raw.x), e4m3x2_to_f16x2(raw.x >> 16),
+                                        e4m3x2_to_f16x2(raw.y), e4m3x2_to_f16x2(raw.y >> 16));
+            const uint4 hi = make_uint4(e4m3x2_to_f16x2(raw.z), e4m3x2_to_f16x2(raw.z >> 16),
+                                        e4m3x2_to_f16x2(raw.w), e4m3x2_to_f16x2(raw.w >> 16));
+            unsigned char* tile = wide + kv * C::kTileBytes;
+            *reinterpret_cast<uint4*>(tile + swz<C::kRowBytes>(t, 2 * rc)) = lo;
+            *reinterpret_cast<uint4*>(tile + swz<C::kRowBytes>(t, 2 * rc + 1)) = hi;
+          }
+          __syncwarp();
+          st = ring_u32 + NS * C::kStageBytes;  // the MMAs read the widened pair
+        }
         const int tok0 = (cur.b0 + warp + i * NW) * kBlockSize;
         // S = Q K^T for the block's 16 tokens: two n-tiles of 8 tokens
         float s[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
@@ -386,8 +447,13 @@ __global__ void __launch_bounds__(MmaCfg<D, G, P, NW, NS>::kThreads,
           for (int kk = 0; kk < C::kKSteps; ++kk) {
             uint32_t b0, b1, b2, b3;
             ldsm_x4(st + swz<C::kRowBytes>(t, 2 * kk + (mi & 1)), b0, b1, b2, b3);
-            mma_bf16(s[0], qa[kk], b0, b1);
-            mma_bf16(s[1], qa[kk], b2, b3);
+            if constexpr (F8) {
+              mma_f16(s[0], qa[kk], b0, b1);
+              mma_f16(s[1], qa[kk], b2, b3);
+            } else {
+              mma_bf16(s[0], qa[kk], b0, b1);
+              mma_bf16(s[1], qa[kk], b2, b3);
+            }
           }
         }
         // mask and online softmax (base 2); lane holds rows rowA (c0,c1) and rowB (c2,c3)
@@ -464,10 +530,17 @@ __global__ void __launch_bounds__(MmaCfg<D, G, P, NW, NS>::kThreads,
         }
         // O += P V: P as the A operand (rows x 16 tokens), V via transposed ldmatrix
         uint32_t pa[4];
-        pa[0] = pack_bf16(pA[0], pA[1]);
-        pa[1] = pack_bf16(pB[0], pB[1]);
-        pa[2] = pack_bf16(pA[2], pA[3]);
-        pa[3] = pack_bf16(pB[2], pB[3]);
+        if constexpr (F8) {
+          pa[0] = pack_f16(pA[0], pA[1]);
+          pa[1] = pack_f16(pB[0], pB[1]);
+          pa[2] = pack_f16(pA[2], pA[3]);
+          pa[3] = pack_f16(pB[2], pB[3]);
+        } else {
+          pa[0] = pack_bf16(pA[0], pA[1]);
+          pa[1] = pack_bf16(pB[0], pB[1]);
+          pa[2] = pack_bf16(pA[2], pA[3]);
+          pa[3] = pack_bf16(pB[2], pB[3]);
+        }
         {
           const int mi = lane >> 3;
           const int t = ((mi & 1) << 3) + (lane & 7);
@@ -476,8 +549,13 @@ __global__ void __launch_bounds__(MmaCfg<D, G, P, NW, NS>::kThreads,
           for (int nt = 0; nt < C::kNTiles; nt += 2) {
             uint32_t b0, b1, b2, b3;
             ldsm_x4_t(vt + swz<C::kRowBytes>(t, nt + (mi >> 1)), b0, b1, b2, b3);
-            mma_bf16(o[nt], pa, b0, b1);
-            mma_bf16(o[nt + 1], pa, b2, b3);
+            if constexpr (F8) {
+              mma_f16(o[nt], pa, b0, b1);
+              mma_f16(o[nt + 1], pa, b2, b3);
+            } else {
+              mma_bf16(o[nt], pa, b0, b1);
+              mma_bf16(o[nt + 1], pa, b2, b3);
+            }
           }
         }
         __syncwarp();
@@ -519,25 +597,25 @@ __global__ void __launch_bounds__(MmaCfg<D, G, P, NW, NS>::kThreads,
   cp_async_wait<0>();
 }
 
-template <int D, int G, int P, int NW, int NS>
+template <int D, int G, int P, int NW, int NS, bool F8 = false>
 cudaError_t launch_mma(const AttnParams& p, int num_sms, cudaStream_t stream) {
-  using C = MmaCfg<D, G, P, NW, NS>;
+  using C = MmaCfg<D, G, P, NW, NS, F8>;
   static int ctas_per_sm[64] = {0};
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
   if (ctas_per_sm[dev] == 0) {
-    e = cudaFuncSetAttribute(attn_mma_kernel<D, G, P, NW, NS>,
+    e = cudaFuncSetAttribute(attn_mma_kernel<D, G, P, NW, NS, F8>,
                              cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
     if (e != cudaSuccess) return e;
     int n = 0;
-    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, attn_mma_kernel<D, G, P, NW, NS>,
+    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, attn_mma_kernel<D, G, P, NW, NS, F8>,
                                                       C::kThreads, C::kSmemBytes);
     if (e != cudaSuccess) return e;
     ctas_per_sm[dev] = n > 0 ? n : 1;
   }
-  attn_mma_kernel<D, G, P, NW, NS>
+  attn_mma_kernel<D, G, P, NW, NS, F8>
       <<<num_sms * ctas_per_sm[dev], C::kThreads, C::kSmemBytes, stream>>>(p);
   return cudaGetLastError();
 }

@@ -70,7 +70,8 @@ struct AttnParams {
   void* out;
   int max_blocks_per_seq;
   int num_q_heads, num_kv_heads, num_blocks, num_tokens;
-  float scale_log2;      // softmax scale * log2(e)
+  float scale_log2;      // softmax scale * log2(e) (times k_scale for an FP8 cache)
+  float out_scale;       // applied to the normalised output (v_scale for an FP8 cache)
   const int* n_items;    // device count of work items (x num_kv_heads units)
   int* next;             // device work counter (zeroed by the plan kernel)
   const int4* items;     // {r, m, first KV block, tile}
@@ -91,6 +92,11 @@ WsLayout ws_layout(const Capacity& cap, int num_seqs, int num_kv_heads, int head
 cudaError_t launch_cache_write(const void* k, const void* v, const int64_t* slot_mapping,
                                int num_tokens, void* k_cache, void* v_cache, int row_bytes,
                                long long num_slots, int32_t* status, cudaStream_t stream);
+// Quantising slot write into an FP8 (E4M3) cache; row_bytes is the bf16 input row.
+cudaError_t launch_cache_write_fp8(const void* k, const void* v, const int64_t* slot_mapping,
+                                   int num_tokens, void* k_cache, void* v_cache, int row_bytes,
+                                   long long num_slots, float k_scale, float v_scale,
+                                   int32_t* status, cudaStream_t stream);
 cudaError_t launch_plan(const PlanParams& p, cudaStream_t stream);
 // CUDA-core split-KV attention.  positions: 1 (decode list) or the small-q
 // tile height.  Returns cudaErrorInvalidValue for an unbuilt combination.
@@ -99,5 +105,8 @@ cudaError_t launch_prefill_tc(const AttnParams& p, int head_size, int group, int
                               cudaStream_t stream);
 cudaError_t launch_attn_cuda_core(const AttnParams& p, pa_dtype dtype, int head_size, int group,
                                   int positions, int num_sms, cudaStream_t stream);
+// bf16 q/out over an FP8 (E4M3) cache (tensor-core decode and few-token tiles).
+cudaError_t launch_attn_fp8(const AttnParams& p, int head_size, int group, int positions,
+                            int num_sms, cudaStream_t stream);
 
 }  // namespace pa
