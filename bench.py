@@ -632,9 +632,10 @@ def run_reference_arm(args):
     print(json.dumps(line))
 
 
-def run_ncu_case(spec_arg: str, iters: int = 3) -> None:
+def run_ncu_case(spec_arg: str, iters: int = 3, fp8: bool = False) -> None:
     """A small step for profilers: `NAME` or `NAME:N` (the first N requests of
-    workload NAME); runs pa_cache_write + pa_forward `iters` times."""
+    workload NAME); runs pa_cache_write + pa_forward `iters` times (over an FP8
+    cache with scales 0.01 when fp8)."""
     import torch
 
     import paged_kv_attention_04_gb300 as P
@@ -650,7 +651,12 @@ def run_ncu_case(spec_arg: str, iters: int = 3) -> None:
         if spec.sharing is not None:
             spec.sharing = spec.sharing[sl]
     st = W.make_step(spec, device="cuda")
-    lay = P.layout_of(st.k_cache, spec.num_q_heads)
+    if fp8:
+        st.k_cache = (st.k_cache.float() / 0.01).clamp(-448, 448).to(torch.float8_e4m3fn).view(torch.uint8)
+        st.v_cache = (st.v_cache.float() / 0.01).clamp(-448, 448).to(torch.float8_e4m3fn).view(torch.uint8)
+        lay = P.layout_of(st.k_cache, spec.num_q_heads, k_scale=0.01, v_scale=0.01)
+    else:
+        lay = P.layout_of(st.k_cache, spec.num_q_heads)
     ws = P.alloc_workspace(lay, spec.num_seqs, spec.num_tokens, st.max_seq_len)
     out = torch.empty_like(st.q)
     status = torch.zeros(1, dtype=torch.int32, device="cuda")
@@ -677,11 +683,12 @@ def main():
     ap.add_argument("--ncu-case", default=None,
                     help="run a small step for a profiler: NAME, NAME:N (first N requests) "
                          "or NAME:-N (last N)")
+    ap.add_argument("--fp8-kv", action="store_true", help="with --ncu-case: an FP8 (E4M3) cache")
     ap.add_argument("--oracle-budget", type=float, default=1.0, help=argparse.SUPPRESS)
     ap.add_argument("--oracle-worker", default=None, help=argparse.SUPPRESS)
     args = ap.parse_args()
     if args.ncu_case:
-        run_ncu_case(args.ncu_case)
+        run_ncu_case(args.ncu_case, fp8=args.fp8_kv)
         return
     if args.oracle_worker:
         oracle_worker(args.oracle_worker, args.oracle_seconds, args.oracle_stride, args.steps,

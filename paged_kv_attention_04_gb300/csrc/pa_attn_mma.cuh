@@ -106,11 +106,11 @@ struct MmaCfg {
   static constexpr int kCacheRowBytes = F8 ? D : D * 2;       // one cached row (token, head)
   static constexpr int kCacheChunks = kCacheRowBytes / 16;
   static constexpr int kRawTileBytes = F8 ? kBlockSize * D : 0;  // FP8 codes as copied
-  // A ring stage holds one block's K and V as copied: 16-bit tiles, or raw FP8
-  // codes (then each warp also owns one f16 tile pair the codes are widened into).
+  // A ring stage holds one block's K and V as copied: swizzled 16-bit tiles, or
+  // raw FP8 codes (16-byte chunks XOR-swizzled by row) read straight into MMA
+  // fragments.
   static constexpr int kStageBytes = F8 ? 2 * kRawTileBytes : 2 * kTileBytes;
-  static constexpr int kWidenBytes = F8 ? 2 * kTileBytes : 0;
-  static constexpr int kWarpRingBytes = NS * kStageBytes + kWidenBytes;
+  static constexpr int kWarpRingBytes = NS * kStageBytes;
   static constexpr int kKSteps = D / 16;
   static constexpr int kNTiles = D / 8;
   static constexpr int kThreads = (NW + 1) * 32;
@@ -203,10 +203,21 @@ __global__ void __launch_bounds__(MmaCfg<D, G, P, NW, NS, F8>::kThreads,
         const int jj = row / G, hh = row - jj * G;
         if (jj < m.npos) {
           const long long tok = m.a + m.j0 + jj;
-          v = __ldg(reinterpret_cast<const uint4*>(q + (tok * Hq + m.g * G + hh) * D) + c);
-          if constexpr (F8) {  // the MMAs run in f16 against widened FP8 codes
-            v = make_uint4(pack_f16(bf16_lo(v.x), bf16_hi(v.x)), pack_f16(bf16_lo(v.y), bf16_hi(v.y)),
-                           pack_f16(bf16_lo(v.z), bf16_hi(v.z)), pack_f16(bf16_lo(v.w), bf16_hi(v.w)));
+          if constexpr (F8) {
+            // f16, head dimension permuted to match the FP8 K fragments: logical
+            // chunk c (k-step c/2, half c%2) holds bf16 pairs at words
+            // (D/8)*t + 2*(c/2) + c%2 for t = 0..3 of the row (see qk_f8 below)
+            const uint32_t* qw = reinterpret_cast<const uint32_t*>(q + (tok * Hq + m.g * G + hh) * D);
+            const int wb = 2 * (c >> 1) + (c & 1);
+            uint32_t w[4];
+#pragma unroll
+            for (int t = 0; t < 4; ++t) {
+              const uint32_t x = __ldg(qw + (D / 8) * t + wb);
+              w[t] = pack_f16(bf16_lo(x), bf16_hi(x));
+            }
+            v = make_uint4(w[0], w[1], w[2], w[3]);
+          } else {
+            v = __ldg(reinterpret_cast<const uint4*>(q + (tok * Hq + m.g * G + hh) * D) + c);
           }
         }
       }
@@ -263,8 +274,8 @@ __global__ void __launch_bounds__(MmaCfg<D, G, P, NW, NS, F8>::kThreads,
       const int t = lane / C::kCacheChunks + k * (32 / C::kCacheChunks);
       const long long off = base + t * row_stride + c * 16;
       const int vb = t < valid_rows ? kbytes : 0;
-      if constexpr (F8) {  // raw codes, unswizzled; widened after they land
-        const uint32_t so = t * C::kCacheRowBytes + c * 16;
+      if constexpr (F8) {  // raw codes, 16-byte chunks XOR-swizzled by row
+        const uint32_t so = t * C::kCacheRowBytes + ((c ^ (t & (C::kCacheChunks - 1))) << 4);
         cp_async16(st + so, kc + off, vb);
         cp_async16(st + C::kRawTileBytes + so, vc + off, vb);
       } else {
@@ -412,48 +423,46 @@ __global__ void __launch_bounds__(MmaCfg<D, G, P, NW, NS, F8>::kThreads,
       for (int i = 0; i < nb; ++i) {
         issue_one(k + 1);
         wait_for(computed);
-        uint32_t st = ring_u32 + (computed % NS) * C::kStageBytes;
-        if constexpr (F8) {
-          // widen the block's FP8 codes to f16 (exact) into the warp's swizzled tile pair
-          const unsigned char* raw_st =
-              smem + C::kRingOff + warp * C::kWarpRingBytes + (computed % NS) * C::kStageBytes;
-          unsigned char* wide = smem + C::kRingOff + warp * C::kWarpRingBytes + NS * C::kStageBytes;
-#pragma unroll
-          for (int k = 0; k < (2 * kBlockSize * C::kCacheChunks) / 32; ++k) {
-            const int idx = lane + 32 * k;                 // over K then V raw chunks
-            const int kv = idx / (kBlockSize * C::kCacheChunks);
-            const int rem = idx - kv * (kBlockSize * C::kCacheChunks);
-            const int t = rem / C::kCacheChunks, rc = rem - t * C::kCacheChunks;
-            const uint4 raw = *reinterpret_cast<const uint4*>(
-                raw_st + kv * C::kRawTileBytes + t * C::kCacheRowBytes + rc * 16);
-            const uint4 lo = make_uint4(e4m3x2_to_f16x2(raw.x), e4m3x2_to_f16x2(raw.x >> 16),
-                                        e4m3x2_to_f16x2(raw.y), e4m3x2_to_f16x2(raw.y >> 16));
-            const uint4 hi = make_uint4(e4m3x2_to_f16x2(raw.z), e4m3x2_to_f16x2(raw.z >> 16),
-                                        e4m3x2_to_f16x2(raw.w), e4m3x2_to_f16x2(raw.w >> 16));
-            unsigned char* tile = wide + kv * C::kTileBytes;
-            *reinterpret_cast<uint4*>(tile + swz<C::kRowBytes>(t, 2 * rc)) = lo;
-            *reinterpret_cast<uint4*>(tile + swz<C::kRowBytes>(t, 2 * rc + 1)) = hi;
-          }
-          __syncwarp();
-          st = ring_u32 + NS * C::kStageBytes;  // the MMAs read the widened pair
-        }
+        const uint32_t st = ring_u32 + (computed % NS) * C::kStageBytes;
+
         const int tok0 = (cur.b0 + warp + i * NW) * kBlockSize;
         // S = Q K^T for the block's 16 tokens: two n-tiles of 8 tokens
         float s[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
-        {
+        if constexpr (F8) {
+          // K codes straight into B fragments.  With the head dimension permuted
+          // as pi(kk, k) = (D/4)*((k%8)/2) + 4*kk + (k%2) + 2*(k/8) on Q and K alike,
+          // lane (gid, tig) needs, for every k-step kk, the 4 codes at dims
+          // (D/4)*tig + 4*kk .. +3 of tokens gid and gid + 8: one contiguous run of
+          // D/4 bytes per token.
+          const int gid = lane >> 2, tig = lane & 3;
+          uint32_t kw[2][D / 16];
+#pragma unroll
+          for (int h = 0; h < 2; ++h) {
+            const int t = gid + 8 * h;
+#pragma unroll
+            for (int j = 0; j < D / 64; ++j) {
+              const int c = (D / 64) * tig + j;
+              uint4 v;
+              asm volatile("ld.shared.v4.b32 {%0,%1,%2,%3}, [%4];\n"
+                           : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+                           : "r"(st + t * C::kCacheRowBytes + ((c ^ (t & (C::kCacheChunks - 1))) << 4)));
+              kw[h][4 * j] = v.x; kw[h][4 * j + 1] = v.y; kw[h][4 * j + 2] = v.z; kw[h][4 * j + 3] = v.w;
+            }
+          }
+#pragma unroll
+          for (int kk = 0; kk < C::kKSteps; ++kk) {
+            mma_f16(s[0], qa[kk], e4m3x2_to_f16x2(kw[0][kk]), e4m3x2_to_f16x2(kw[0][kk] >> 16));
+            mma_f16(s[1], qa[kk], e4m3x2_to_f16x2(kw[1][kk]), e4m3x2_to_f16x2(kw[1][kk] >> 16));
+          }
+        } else {
           const int mi = lane >> 3;
           const int t = ((mi >> 1) << 3) + (lane & 7);
 #pragma unroll
           for (int kk = 0; kk < C::kKSteps; ++kk) {
             uint32_t b0, b1, b2, b3;
             ldsm_x4(st + swz<C::kRowBytes>(t, 2 * kk + (mi & 1)), b0, b1, b2, b3);
-            if constexpr (F8) {
-              mma_f16(s[0], qa[kk], b0, b1);
-              mma_f16(s[1], qa[kk], b2, b3);
-            } else {
-              mma_bf16(s[0], qa[kk], b0, b1);
-              mma_bf16(s[1], qa[kk], b2, b3);
-            }
+            mma_bf16(s[0], qa[kk], b0, b1);
+            mma_bf16(s[1], qa[kk], b2, b3);
           }
         }
         // mask and online softmax (base 2); lane holds rows rowA (c0,c1) and rowB (c2,c3)
@@ -541,7 +550,44 @@ __global__ void __launch_bounds__(MmaCfg<D, G, P, NW, NS, F8>::kThreads,
           pa[2] = pack_bf16(pA[2], pA[3]);
           pa[3] = pack_bf16(pB[2], pB[3]);
         }
-        {
+        if constexpr (F8) {
+          // V codes straight into B fragments.  Output column n of n-tile nt is
+          // head dim sigma(nt, n) = (D/8)*n + nt, so lane (gid, tig) needs dims
+          // (D/8)*gid .. +D/8-1 of tokens 2tig, 2tig+1, 2tig+8, 2tig+9; byte pairs
+          // from two tokens are interleaved and widened in one conversion.
+          const int gid = lane >> 2, tig = lane & 3;
+          const uint32_t vt = st + C::kRawTileBytes;
+          uint32_t vw[4][D / 32];
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            const int t = 2 * tig + (i & 1) + 8 * (i >> 1);
+            if constexpr (D == 128) {
+              uint4 v;
+              asm volatile("ld.shared.v4.b32 {%0,%1,%2,%3}, [%4];\n"
+                           : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+                           : "r"(vt + t * C::kCacheRowBytes + ((gid ^ (t & 7)) << 4)));
+              vw[i][0] = v.x; vw[i][1] = v.y; vw[i][2] = v.z; vw[i][3] = v.w;
+            } else {
+              uint2 v;
+              asm volatile("ld.shared.v2.b32 {%0,%1}, [%2];\n"
+                           : "=r"(v.x), "=r"(v.y)
+                           : "r"(vt + t * C::kCacheRowBytes + (((gid >> 1) ^ (t & 3)) << 4) +
+                                 ((gid & 1) << 3)));
+              vw[i][0] = v.x; vw[i][1] = v.y;
+            }
+          }
+#pragma unroll
+          for (int w = 0; w < D / 32; ++w) {
+            const uint32_t lo0 = __byte_perm(vw[0][w], vw[1][w], 0x5140);
+            const uint32_t hi0 = __byte_perm(vw[0][w], vw[1][w], 0x7362);
+            const uint32_t lo1 = __byte_perm(vw[2][w], vw[3][w], 0x5140);
+            const uint32_t hi1 = __byte_perm(vw[2][w], vw[3][w], 0x7362);
+            mma_f16(o[4 * w + 0], pa, e4m3x2_to_f16x2(lo0), e4m3x2_to_f16x2(lo1));
+            mma_f16(o[4 * w + 1], pa, e4m3x2_to_f16x2(lo0 >> 16), e4m3x2_to_f16x2(lo1 >> 16));
+            mma_f16(o[4 * w + 2], pa, e4m3x2_to_f16x2(hi0), e4m3x2_to_f16x2(hi1));
+            mma_f16(o[4 * w + 3], pa, e4m3x2_to_f16x2(hi0 >> 16), e4m3x2_to_f16x2(hi1 >> 16));
+          }
+        } else {
           const int mi = lane >> 3;
           const int t = ((mi & 1) << 3) + (lane & 7);
           const uint32_t vt = st + C::kTileBytes;
@@ -549,13 +595,8 @@ __global__ void __launch_bounds__(MmaCfg<D, G, P, NW, NS, F8>::kThreads,
           for (int nt = 0; nt < C::kNTiles; nt += 2) {
             uint32_t b0, b1, b2, b3;
             ldsm_x4_t(vt + swz<C::kRowBytes>(t, nt + (mi >> 1)), b0, b1, b2, b3);
-            if constexpr (F8) {
-              mma_f16(o[nt], pa, b0, b1);
-              mma_f16(o[nt + 1], pa, b2, b3);
-            } else {
-              mma_bf16(o[nt], pa, b0, b1);
-              mma_bf16(o[nt + 1], pa, b2, b3);
-            }
+            mma_bf16(o[nt], pa, b0, b1);
+            mma_bf16(o[nt + 1], pa, b2, b3);
           }
         }
         __syncwarp();
@@ -568,11 +609,19 @@ __global__ void __launch_bounds__(MmaCfg<D, G, P, NW, NS, F8>::kThreads,
       lA += __shfl_xor_sync(0xffffffffu, lA, 2);
       lB += __shfl_xor_sync(0xffffffffu, lB, 1);
       lB += __shfl_xor_sync(0xffffffffu, lB, 2);
+      // column n of n-tile j is head dim j*8 + n, or (D/8)*n + j on the FP8 path
+      auto dim_of = [&](int j, int n) { return F8 ? (D / 8) * n + j : j * 8 + n; };
       if (rowA < R) {
 #pragma unroll
-        for (int j = 0; j < C::kNTiles; ++j)
-          *reinterpret_cast<float2*>(cb + (warp * R + rowA) * D + j * 8 + ((lane & 3) << 1)) =
-              make_float2(o[j][0], o[j][1]);
+        for (int j = 0; j < C::kNTiles; ++j) {
+          if constexpr (F8) {
+            cb[(warp * R + rowA) * D + dim_of(j, (lane & 3) << 1)] = o[j][0];
+            cb[(warp * R + rowA) * D + dim_of(j, ((lane & 3) << 1) + 1)] = o[j][1];
+          } else {
+            *reinterpret_cast<float2*>(cb + (warp * R + rowA) * D + j * 8 + ((lane & 3) << 1)) =
+                make_float2(o[j][0], o[j][1]);
+          }
+        }
         if ((lane & 3) == 0) {
           cm[(warp * R + rowA) * 2] = mA;
           cm[(warp * R + rowA) * 2 + 1] = lA;
@@ -581,9 +630,15 @@ __global__ void __launch_bounds__(MmaCfg<D, G, P, NW, NS, F8>::kThreads,
       if constexpr (R > 8) {
         if (rowB < R) {
 #pragma unroll
-          for (int j = 0; j < C::kNTiles; ++j)
-            *reinterpret_cast<float2*>(cb + (warp * R + rowB) * D + j * 8 + ((lane & 3) << 1)) =
-                make_float2(o[j][2], o[j][3]);
+          for (int j = 0; j < C::kNTiles; ++j) {
+            if constexpr (F8) {
+              cb[(warp * R + rowB) * D + dim_of(j, (lane & 3) << 1)] = o[j][2];
+              cb[(warp * R + rowB) * D + dim_of(j, ((lane & 3) << 1) + 1)] = o[j][3];
+            } else {
+              *reinterpret_cast<float2*>(cb + (warp * R + rowB) * D + j * 8 + ((lane & 3) << 1)) =
+                  make_float2(o[j][2], o[j][3]);
+            }
+          }
           if ((lane & 3) == 0) {
             cm[(warp * R + rowB) * 2] = mB;
             cm[(warp * R + rowB) * 2 + 1] = lB;
