@@ -144,6 +144,15 @@ size_t pa_forward_workspace_size(const pa_layout* layout, int num_seqs, int num_
  *                    initialisation and are overwritten
  *   out              device, [num_tokens][num_q_heads][head_size]
  * Rows of skipped requests are left unwritten.
+ *
+ * Streams: everything is ordered on `stream`.  When the step can hold bf16
+ * chunks of at least 16 tokens (max_query_len >= 16), their tensor-core
+ * kernel runs on a library side stream forked from `stream` after the
+ * planning kernel and joined back before the call returns, so it overlaps
+ * the decode kernel.  The side stream and its two events are created once
+ * per host thread and device, on the first such call (they hold no device
+ * memory); make that first call before capturing `stream` into a CUDA graph.
+ * A captured step records the fork and join as parallel graph branches.
  */
 int pa_forward(const void* q, const void* k_cache, const void* v_cache,
                const int32_t* block_tables, int max_blocks_per_seq,
@@ -175,7 +184,9 @@ int pa_set_profile_events(void* start, void* stop);
  * inside the library: every GPU that loads the library holds it until the
  * process exits.  A step whose pa_forward_workspace_size exceeds that is
  * rejected with PA_ERR_INVALID before anything is launched.  The call makes
- * no cudaMalloc/cudaFree or other allocation.
+ * no cudaMalloc/cudaFree or other device-memory allocation (a step with
+ * prefill chunks may, on its first call, create pa_forward's side stream and
+ * events, which hold no device memory).
  *
  * The first call on each device looks up the array's device address
  * (cudaGetSymbolAddress, with that device current); make that first call

@@ -114,6 +114,31 @@ Capacity capacity(const pa_layout* L, int B, int T, int max_seq_len) {
 
 size_t align256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
 
+// Per host thread and device: a side stream and two events used to run the
+// tensor-core prefill kernel beside the decode kernel (fork after the plan,
+// join before returning).  Created on the first call that needs them.
+struct SideStream {
+  cudaStream_t stream = nullptr;
+  cudaEvent_t fork = nullptr, join = nullptr;
+};
+thread_local SideStream g_side[64];
+
+int side_stream_of_current_device(SideStream** out) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return fail_cuda(e, "cudaGetDevice");
+  if (dev < 0 || dev >= 64) return fail(PA_ERR_CUDA, "device ordinal %d", dev);
+  SideStream& s = g_side[dev];
+  if (!s.stream) {
+    e = cudaStreamCreateWithFlags(&s.stream, cudaStreamNonBlocking);
+    if (e == cudaSuccess) e = cudaEventCreateWithFlags(&s.fork, cudaEventDisableTiming);
+    if (e == cudaSuccess) e = cudaEventCreateWithFlags(&s.join, cudaEventDisableTiming);
+    if (e != cudaSuccess) return fail_cuda(e, "side stream set-up");
+  }
+  *out = &s;
+  return PA_OK;
+}
+
 int num_sms_of_current_device(int* out) {
   static int cache[64] = {0};
   int dev = 0;
@@ -155,6 +180,8 @@ WsLayout ws_layout(const Capacity& cap, int B, int Hkv, int D, int group) {
   w.items_s = take(sizeof(int4) * cap.small_items);
   w.tiles_s = take(sizeof(int4) * cap.small_tiles);
   w.tiles_p = take(sizeof(int4) * cap.prefill_tiles);
+  w.recs_d = take(sizeof(UnitRec) * cap.decode_items);
+  w.recs_s = take(sizeof(UnitRec) * cap.small_items);
   w.cnt_d = take(sizeof(int) * cap.decode_tiles * Hkv);
   w.cnt_s = take(sizeof(int) * cap.small_tiles * Hkv);
   w.part_acc_d = take(sizeof(float) * cap.decode_items * Hkv * rows_d * D);
@@ -288,6 +315,15 @@ int pa_forward(const void* q, const void* k_cache, const void* v_cache,
   cudaError_t e = launch_plan(pp, st);
   if (e != cudaSuccess) return fail_cuda(e, "plan launch");
 
+  // Chunked prefill (tensor cores) runs on a side stream, launched before the
+  // decode kernel so that decode CTAs fill the SMs the prefill CTAs leave:
+  // the HBM-bound and the tensor-bound work overlap.
+  const bool run_prefill = tc_prefill && max_query_len >= kPrefillMinQlen;
+  SideStream* side = nullptr;
+  if (run_prefill) {
+    if (int rc = side_stream_of_current_device(&side)) return rc;
+  }
+
   AttnParams ap{};
   ap.q = q;
   ap.k_cache = k_cache;
@@ -305,10 +341,30 @@ int pa_forward(const void* q, const void* k_cache, const void* v_cache,
   ap.out_scale = fp8_cache(layout) ? layout->v_scale : 1.f;
   ap.status = status;
 
+  if (run_prefill) {
+    AttnParams pf = ap;
+    pf.n_items = hdr + kHdrPrefillTiles;
+    pf.next = hdr + kHdrPrefillNext;
+    pf.items = reinterpret_cast<const int4*>(ws + lay.tiles_p);
+    pf.recs = nullptr;
+    pf.tiles = nullptr;
+    pf.merge_cnt = nullptr;
+    pf.part_acc = nullptr;
+    pf.part_ml = nullptr;
+    e = cudaEventRecord(side->fork, st);
+    if (e == cudaSuccess) e = cudaStreamWaitEvent(side->stream, side->fork, 0);
+    if (e != cudaSuccess) return fail_cuda(e, "side stream fork");
+    e = launch_prefill_tc(pf, layout->head_size, group, num_sms, side->stream);
+    if (e != cudaSuccess) return fail_cuda(e, "prefill attention launch");
+    e = cudaEventRecord(side->join, side->stream);
+    if (e != cudaSuccess) return fail_cuda(e, "side stream join");
+  }
+
   // decode rows (q_len == 1)
   ap.n_items = hdr + kHdrDecodeItems;
   ap.next = hdr + kHdrDecodeNext;
   ap.items = reinterpret_cast<const int4*>(ws + lay.items_d);
+  ap.recs = reinterpret_cast<const UnitRec*>(ws + lay.recs_d);
   ap.tiles = reinterpret_cast<const int4*>(ws + lay.tiles_d);
   ap.merge_cnt = reinterpret_cast<int*>(ws + lay.cnt_d);
   ap.part_acc = reinterpret_cast<float*>(ws + lay.part_acc_d);
@@ -324,6 +380,7 @@ int pa_forward(const void* q, const void* k_cache, const void* v_cache,
     ap.n_items = hdr + kHdrSmallItems;
     ap.next = hdr + kHdrSmallNext;
     ap.items = reinterpret_cast<const int4*>(ws + lay.items_s);
+    ap.recs = reinterpret_cast<const UnitRec*>(ws + lay.recs_s);
     ap.tiles = reinterpret_cast<const int4*>(ws + lay.tiles_s);
     ap.merge_cnt = reinterpret_cast<int*>(ws + lay.cnt_s);
     ap.part_acc = reinterpret_cast<float*>(ws + lay.part_acc_s);
@@ -334,16 +391,9 @@ int pa_forward(const void* q, const void* k_cache, const void* v_cache,
                                     small_positions(layout), num_sms, st);
     if (e != cudaSuccess) return fail_cuda(e, "small-q attention launch");
   }
-  if (tc_prefill && max_query_len >= kPrefillMinQlen) {
-    ap.n_items = hdr + kHdrPrefillTiles;
-    ap.next = hdr + kHdrPrefillNext;
-    ap.items = reinterpret_cast<const int4*>(ws + lay.tiles_p);
-    ap.tiles = nullptr;
-    ap.merge_cnt = nullptr;
-    ap.part_acc = nullptr;
-    ap.part_ml = nullptr;
-    e = launch_prefill_tc(ap, layout->head_size, group, num_sms, st);
-    if (e != cudaSuccess) return fail_cuda(e, "prefill attention launch");
+  if (run_prefill) {
+    e = cudaStreamWaitEvent(st, side->join, 0);
+    if (e != cudaSuccess) return fail_cuda(e, "side stream join wait");
   }
   return PA_OK;
 }

@@ -36,6 +36,13 @@
 #include "pa_device.cuh"
 #include "pa_internal.h"
 
+#ifndef PA_CLAIM_AHEAD
+#define PA_CLAIM_AHEAD 0  // 1: the scheduler warp claims a unit one fetch early
+#endif
+#ifndef PA_QK_SPLIT_ACC
+#define PA_QK_SPLIT_ACC 0  // 1: two accumulator sets per score tile (shorter MMA chains)
+#endif
+
 namespace pa {
 
 struct UnitMeta {
@@ -164,39 +171,36 @@ __global__ void __launch_bounds__(MmaCfg<D, G, P, NW, NS, F8>::kThreads,
   const int n_units = __ldg(p.n_items) * Hkv;
 
   // ---- scheduler-warp helpers -------------------------------------------
-  auto fetch_unit = [&](UnitMeta& m) {  // whole scheduler warp
-    int u = 0;
-    if (lane == 0) u = atomicAdd(p.next, 1);
-    u = __shfl_sync(0xffffffffu, u, 0);
+  // Decode unit u (claimed earlier) into m: one precomputed record plus the
+  // unit's block-table slice.
+  auto fetch_unit = [&](UnitMeta& m, int u) {  // whole scheduler warp
     if (u >= n_units) {
       if (lane == 0) m.valid = 0;
       return;
     }
     const int item = u / Hkv;
-    const int g = u - item * Hkv;
-    const int4 it = __ldg(p.items + item);
-    const int4 ti = __ldg(p.tiles + it.w);
-    const int S = __ldg(p.seq_lens + it.x);
-    const int a = __ldg(p.qsl + it.x);
-    const int L = __ldg(p.qsl + it.x + 1) - a;
-    const int j0 = it.y * P;
-    const int npos = min(P, L - j0);
-    const int pos0 = S - L + j0;
-    const int kv_end = pos0 + npos;
-    const int nblk = (kv_end + kBlockSize - 1) / kBlockSize;
-    const int b0 = it.z;
-    const int b1 = min(b0 + ti.z, nblk);
-    const int32_t* row = p.block_tables + static_cast<long long>(it.x) * p.max_blocks_per_seq;
-    for (int i = lane; i < b1 - b0; i += 32) m.bt[i] = __ldg(row + b0 + i);
+    const UnitRec* rec = p.recs + item;
+    const int4 ra = __ldg(&rec->a), rb = __ldg(&rec->b), rc = __ldg(&rec->c);
+    const int32_t* row = p.block_tables + static_cast<long long>(ra.x) * p.max_blocks_per_seq;
+    for (int i = lane; i < ra.w - ra.z; i += 32) m.bt[i] = __ldg(row + ra.z + i);
     if (lane == 0) {
-      m.valid = 1; m.item = item; m.g = g; m.r = it.x; m.a = a; m.j0 = j0; m.npos = npos;
-      m.pos0 = pos0; m.kv_hi = min(b1 * kBlockSize, kv_end); m.b0 = b0; m.b1 = b1;
-      m.tile = it.w; m.nsplit = ti.y; m.first = ti.x;
+      m.valid = 1; m.item = item; m.g = u - item * Hkv; m.r = ra.x; m.a = rb.w; m.j0 = ra.y;
+      m.npos = rc.x; m.pos0 = rc.y; m.kv_hi = rc.z; m.b0 = ra.z; m.b1 = ra.w;
+      m.tile = rb.x; m.first = rb.y; m.nsplit = rb.z;
     }
   };
-  auto stage_q = [&](const UnitMeta& m, int buf) {  // whole scheduler warp
-    // rows: (position jj, grouped head hh) = (row / G, row % G); rows >= R are zero
-    for (int idx = lane; idx < 16 * C::kChunks; idx += 32) {
+  auto claim = [&]() -> int {
+    int u = 0;
+    if (lane == 0) u = atomicAdd(p.next, 1);
+    return __shfl_sync(0xffffffffu, u, 0);
+  };
+  // q rows of unit m (row = position row/G, head row%G), loaded into registers
+  // first and stored later, so the loads overlap other scheduler work.
+  constexpr int kQPerLane = (R * C::kChunks + 31) / 32;
+  auto load_q = [&](const UnitMeta& m, uint4 (&qv)[kQPerLane]) {
+#pragma unroll
+    for (int i = 0; i < kQPerLane; ++i) {
+      const int idx = lane + 32 * i;
       const int row = idx / C::kChunks, c = idx - row * C::kChunks;
       uint4 v = make_uint4(0, 0, 0, 0);
       if (m.valid && row < R) {
@@ -206,32 +210,61 @@ __global__ void __launch_bounds__(MmaCfg<D, G, P, NW, NS, F8>::kThreads,
           if constexpr (F8) {
             // f16, head dimension permuted to match the FP8 K fragments: logical
             // chunk c (k-step c/2, half c%2) holds bf16 pairs at words
-            // (D/8)*t + 2*(c/2) + c%2 for t = 0..3 of the row (see qk_f8 below)
+            // (D/8)*t + 2*(c/2) + c%2 for t = 0..3 of the row (see the K loads)
             const uint32_t* qw = reinterpret_cast<const uint32_t*>(q + (tok * Hq + m.g * G + hh) * D);
             const int wb = 2 * (c >> 1) + (c & 1);
-            uint32_t w[4];
-#pragma unroll
-            for (int t = 0; t < 4; ++t) {
-              const uint32_t x = __ldg(qw + (D / 8) * t + wb);
-              w[t] = pack_f16(bf16_lo(x), bf16_hi(x));
-            }
-            v = make_uint4(w[0], w[1], w[2], w[3]);
+            v = make_uint4(__ldg(qw + wb), __ldg(qw + (D / 8) + wb), __ldg(qw + 2 * (D / 8) + wb),
+                           __ldg(qw + 3 * (D / 8) + wb));
           } else {
             v = __ldg(reinterpret_cast<const uint4*>(q + (tok * Hq + m.g * G + hh) * D) + c);
           }
         }
       }
-      *reinterpret_cast<uint4*>(smem + C::kQOff + buf * 16 * C::kRowBytes +
-                                swz<C::kRowBytes>(row, c)) = v;
+      qv[i] = v;
+    }
+  };
+  auto store_q = [&](const uint4 (&qv)[kQPerLane], int buf) {
+#pragma unroll
+    for (int i = 0; i < kQPerLane; ++i) {
+      const int idx = lane + 32 * i;
+      const int row = idx / C::kChunks, c = idx - row * C::kChunks;
+      if (row < R) {
+        uint4 v = qv[i];
+        if constexpr (F8)
+          v = make_uint4(pack_f16(bf16_lo(v.x), bf16_hi(v.x)), pack_f16(bf16_lo(v.y), bf16_hi(v.y)),
+                         pack_f16(bf16_lo(v.z), bf16_hi(v.z)), pack_f16(bf16_lo(v.w), bf16_hi(v.w)));
+        *reinterpret_cast<uint4*>(smem + C::kQOff + buf * 16 * C::kRowBytes +
+                                  swz<C::kRowBytes>(row, c)) = v;
+      }
     }
   };
 
+  // scheduler-warp state kept in shared memory so it holds no registers in
+  // the compute warps: the unit claimed for the next fetch, the unit to finish
+  __shared__ int s_next_u;
+  __shared__ UnitTail s_tail;
   if (sched) {
-    fetch_unit(meta[0]);
+    // rows >= R of both q buffers stay zero for the whole kernel
+    for (int idx = lane; idx < 2 * 16 * C::kChunks; idx += 32) {
+      const int buf = idx / (16 * C::kChunks), rem = idx - buf * 16 * C::kChunks;
+      const int row = rem / C::kChunks, c = rem - row * C::kChunks;
+      if (row >= R)
+        *reinterpret_cast<uint4*>(smem + C::kQOff + buf * 16 * C::kRowBytes +
+                                  swz<C::kRowBytes>(row, c)) = make_uint4(0, 0, 0, 0);
+    }
+    const int u0 = claim();
+    const int u1 = claim();
+    const int u2 = PA_CLAIM_AHEAD ? claim() : 0;
+    if (lane == 0) {
+      s_next_u = u2;
+      s_tail.valid = 0;
+    }
+    fetch_unit(meta[0], u0);
+    fetch_unit(meta[1], u1);
     __syncwarp();
-    fetch_unit(meta[1]);
-    __syncwarp();
-    stage_q(meta[0], 0);
+    uint4 qv[kQPerLane];
+    load_q(meta[0], qv);
+    store_q(qv, 0);
   }
   __syncthreads();
 
@@ -382,20 +415,28 @@ __global__ void __launch_bounds__(MmaCfg<D, G, P, NW, NS, F8>::kThreads,
     }
   };
 
-  UnitTail tail;
-  tail.valid = 0;
   int k = 0;
   for (;; ++k) {
     const UnitMeta& cur = meta[k % 3];
     if (!cur.valid) break;
     if (sched) {
-      // finish unit k-1 while the compute warps stream unit k
+      // while the compute warps stream unit k: load unit k+1's q, finish unit
+      // k-1, store the q rows, decode unit k+2 and claim the one after it
+      uint4 qv[kQPerLane];
+      load_q(meta[(k + 1) % 3], qv);
+      const UnitTail tail = s_tail;
       if (tail.valid) finish_unit(tail, (k - 1) & 1);
-      tail.valid = 1; tail.item = cur.item; tail.g = cur.g; tail.a = cur.a; tail.j0 = cur.j0;
-      tail.npos = cur.npos; tail.tile = cur.tile; tail.nsplit = cur.nsplit; tail.first = cur.first;
-      fetch_unit(meta[(k + 2) % 3]);
+      store_q(qv, (k + 1) & 1);
+      const int nu = claim();
+      fetch_unit(meta[(k + 2) % 3], PA_CLAIM_AHEAD ? s_next_u : nu);
       __syncwarp();
-      stage_q(meta[(k + 1) % 3], (k + 1) & 1);
+      if (lane == 0) {
+        s_next_u = nu;
+        s_tail.valid = 1; s_tail.item = cur.item; s_tail.g = cur.g; s_tail.a = cur.a;
+        s_tail.j0 = cur.j0; s_tail.npos = cur.npos; s_tail.tile = cur.tile;
+        s_tail.nsplit = cur.nsplit; s_tail.first = cur.first;
+      }
+      __syncwarp();
     } else {
       // Every block of units < k has been issued and computed; move the issue
       // pointer off unit k-1, whose metadata slot the scheduler warp is now
@@ -449,20 +490,36 @@ __global__ void __launch_bounds__(MmaCfg<D, G, P, NW, NS, F8>::kThreads,
               kw[h][4 * j] = v.x; kw[h][4 * j + 1] = v.y; kw[h][4 * j + 2] = v.z; kw[h][4 * j + 3] = v.w;
             }
           }
+          float s2[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
 #pragma unroll
           for (int kk = 0; kk < C::kKSteps; ++kk) {
-            mma_f16(s[0], qa[kk], e4m3x2_to_f16x2(kw[0][kk]), e4m3x2_to_f16x2(kw[0][kk] >> 16));
-            mma_f16(s[1], qa[kk], e4m3x2_to_f16x2(kw[1][kk]), e4m3x2_to_f16x2(kw[1][kk] >> 16));
+            float* d0 = (PA_QK_SPLIT_ACC && (kk & 1)) ? s2[0] : s[0];
+            float* d1 = (PA_QK_SPLIT_ACC && (kk & 1)) ? s2[1] : s[1];
+            mma_f16(d0, qa[kk], e4m3x2_to_f16x2(kw[0][kk]), e4m3x2_to_f16x2(kw[0][kk] >> 16));
+            mma_f16(d1, qa[kk], e4m3x2_to_f16x2(kw[1][kk]), e4m3x2_to_f16x2(kw[1][kk] >> 16));
+          }
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            s[0][e] += s2[0][e];
+            s[1][e] += s2[1][e];
           }
         } else {
           const int mi = lane >> 3;
           const int t = ((mi >> 1) << 3) + (lane & 7);
+          float s2[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
 #pragma unroll
           for (int kk = 0; kk < C::kKSteps; ++kk) {
             uint32_t b0, b1, b2, b3;
             ldsm_x4(st + swz<C::kRowBytes>(t, 2 * kk + (mi & 1)), b0, b1, b2, b3);
-            mma_bf16(s[0], qa[kk], b0, b1);
-            mma_bf16(s[1], qa[kk], b2, b3);
+            float* d0 = (PA_QK_SPLIT_ACC && (kk & 1)) ? s2[0] : s[0];
+            float* d1 = (PA_QK_SPLIT_ACC && (kk & 1)) ? s2[1] : s[1];
+            mma_bf16(d0, qa[kk], b0, b1);
+            mma_bf16(d1, qa[kk], b2, b3);
+          }
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            s[0][e] += s2[0][e];
+            s[1][e] += s2[1][e];
           }
         }
         // mask and online softmax (base 2); lane holds rows rowA (c0,c1) and rowB (c2,c3)
@@ -648,7 +705,10 @@ __global__ void __launch_bounds__(MmaCfg<D, G, P, NW, NS, F8>::kThreads,
     }
     __syncthreads();
   }
-  if (sched && tail.valid) finish_unit(tail, (k - 1) & 1);
+  if (sched) {
+    const UnitTail tail = s_tail;
+    if (tail.valid) finish_unit(tail, (k - 1) & 1);
+  }
   cp_async_wait<0>();
 }
 

@@ -37,6 +37,7 @@ struct Capacity {
 struct WsLayout {
   size_t hdr, req_class, pfx_d_items, pfx_d_tiles, pfx_s_items, pfx_s_tiles, pfx_p_tiles;
   size_t items_d, tiles_d, items_s, tiles_s, tiles_p;
+  size_t recs_d, recs_s;  // per item: 3 x int4 unit records (see UnitRec)
   size_t cnt_d, cnt_s;
   size_t part_acc_d, part_ml_d, part_acc_s, part_ml_s;
   size_t total;
@@ -58,6 +59,16 @@ struct PlanParams {
   int32_t* status;
 };
 
+// Everything a kernel needs to start on one item, precomputed by the plan
+// kernel so a work fetch is one load (plus the block-table slice):
+//   a = {r, j0 (first query position of the tile), b0, b1 (KV blocks [b0, b1))}
+//   b = {tile, first item of the tile, splits of the tile, qsl[r]}
+//   c = {valid positions in the tile, position of its first row, one past the
+//        last visible key of this split, 0}
+struct UnitRec {
+  int4 a, b, c;
+};
+
 // One unit of CUDA-core attention work: request r, query tile m, KV split s,
 // and the tile's global index (for the split merge).
 struct AttnParams {
@@ -75,6 +86,7 @@ struct AttnParams {
   const int* n_items;    // device count of work items (x num_kv_heads units)
   int* next;             // device work counter (zeroed by the plan kernel)
   const int4* items;     // {r, m, first KV block, tile}
+  const UnitRec* recs;   // per item, the same fully decoded
   const int4* tiles;     // {first item, number of splits, KV blocks per split, 0}
   int* merge_cnt;        // [tiles][num_kv_heads]
   float* part_acc;       // [items][num_kv_heads][rows][D]

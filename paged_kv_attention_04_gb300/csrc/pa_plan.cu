@@ -109,6 +109,8 @@ __global__ void __launch_bounds__(kPlanThreads, 1) plan_kernel(PlanParams p) {
   int4* tiles_d = reinterpret_cast<int4*>(ws + p.lay.tiles_d);
   int4* items_s = reinterpret_cast<int4*>(ws + p.lay.items_s);
   int4* tiles_s = reinterpret_cast<int4*>(ws + p.lay.tiles_s);
+  UnitRec* recs_d = reinterpret_cast<UnitRec*>(ws + p.lay.recs_d);
+  UnitRec* recs_s = reinterpret_cast<UnitRec*>(ws + p.lay.recs_s);
   int* cnt_d = reinterpret_cast<int*>(ws + p.lay.cnt_d);
   int* cnt_s = reinterpret_cast<int*>(ws + p.lay.cnt_s);
 
@@ -194,9 +196,16 @@ __global__ void __launch_bounds__(kPlanThreads, 1) plan_kernel(PlanParams p) {
     const int r = find_owner(pfx_di, B, i);
     const int s = i - pfx_di[r];
     const int tile = pfx_dt[r];
-    const int rb = request_bps(ceil_div(__ldg(p.seq_lens + r), kBlockSize), p.bps);
+    const int S = __ldg(p.seq_lens + r);
+    const int nb = ceil_div(S, kBlockSize);
+    const int rb = request_bps(nb, p.bps);
+    const int ns = pfx_di[r + 1] - pfx_di[r];
     items_d[i] = make_int4(r, 0, s * rb, tile);
-    if (s == 0) tiles_d[tile] = make_int4(i, pfx_di[r + 1] - pfx_di[r], rb, 0);
+    if (s == 0) tiles_d[tile] = make_int4(i, ns, rb, 0);
+    const int b0 = s * rb, b1 = min(b0 + rb, nb);
+    recs_d[i].a = make_int4(r, 0, b0, b1);
+    recs_d[i].b = make_int4(tile, i - s, ns, __ldg(p.qsl + r));
+    recs_d[i].c = make_int4(1, S - 1, min(b1 * kBlockSize, S), 0);
   }
   // Small-q tiles: each thread expands one tile into its splits.
   for (int tile = threadIdx.x; tile < n_st; tile += kPlanThreads) {
@@ -209,7 +218,19 @@ __global__ void __launch_bounds__(kPlanThreads, 1) plan_kernel(PlanParams p) {
     for (int mm = 0; mm < m; ++mm)
       first += splits_for(S - L + min(L, (mm + 1) * p.small_positions) - 1, rb);
     const int ns = splits_for(S - L + min(L, (m + 1) * p.small_positions) - 1, rb);
-    for (int s = 0; s < ns; ++s) items_s[first + s] = make_int4(r, m, s * rb, tile);
+    const int P = p.small_positions;
+    const int npos = min(P, L - m * P);
+    const int pos0 = S - L + m * P;
+    const int kv_end = pos0 + npos;
+    const int nblk = ceil_div(kv_end, kBlockSize);
+    const int a = __ldg(p.qsl + r);
+    for (int s = 0; s < ns; ++s) {
+      items_s[first + s] = make_int4(r, m, s * rb, tile);
+      const int b0 = s * rb, b1 = min(b0 + rb, nblk);
+      recs_s[first + s].a = make_int4(r, m * P, b0, b1);
+      recs_s[first + s].b = make_int4(tile, first, ns, a);
+      recs_s[first + s].c = make_int4(npos, pos0, min(b1 * kBlockSize, kv_end), 0);
+    }
     tiles_s[tile] = make_int4(first, ns, rb, 0);
   }
   // Prefill tiles: 128 query rows (positions x grouped heads) each.
