@@ -47,11 +47,12 @@ struct PfCfg {
   static constexpr int kQOff = 0;
   static constexpr int kKOff = kQOff + kTileBytes;        // 2 buffers
   static constexpr int kVOff = kKOff + 2 * kTileBytes;    // 2 buffers
-  static constexpr int kPOff = kVOff + 2 * kTileBytes;
-  static constexpr int kSmemBytes = kPOff + kPBytes + 1024;  // + alignment slack
-  static constexpr int kTmemCols = 256;                   // S (128) + O (D <= 128)
+  static constexpr int kPOff = kVOff + 2 * kTileBytes;    // 2 buffers
+  static constexpr int kSmemBytes = kPOff + 2 * kPBytes + 1024;  // + alignment slack
+  static constexpr int kTmemCols = 512;                   // S x 2 (256) + O (D <= 128)
   static constexpr int kChunks = D / 8;                   // 16-byte chunks per row
   static_assert(D == 64 || D == 128, "head size 64 or 128");
+  static_assert(kSmemBytes <= 227 * 1024, "shared memory per CTA exceeds 227 KB");
 };
 
 // Byte offset of 16-byte chunk c of row r in a 128-byte-swizzled tile whose
@@ -99,37 +100,67 @@ __global__ void __launch_bounds__(kPfThreads, 1) prefill_tc_kernel(const AttnPar
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = tmem_slot;
-  const uint32_t tmem_s = tmem;        // S: columns [0, 128)
-  const uint32_t tmem_o = tmem + 128;  // O: columns [128, 128 + D)
+  const uint32_t tmem_s = tmem;        // S: two buffers, columns [0, 128) and [128, 256)
+  const uint32_t tmem_o = tmem + 256;  // O: columns [256, 256 + D)
   const uint32_t lane_off = static_cast<uint32_t>(warp * 32) << 16;
   uint32_t ph_s = 0, ph_o = 0;
   bool aborted = false;
 
-  // Load a KV tile (tokens kt*128 ..) of unit `u` into buffer `buf`.
-  auto load_kv = [&](const UnitInfo& u, int kt, int buf) {
+  // Load the K or V half (or both) of KV tile kt (tokens kt*128 ..) of unit u
+  // into buffer buf.  Lanes take consecutive 16-byte chunks of a row (2 rows
+  // per warp instruction for D=128); with the loop unrolled, the KV block of
+  // every chunk a thread copies is known at compile time, so the tile's 8
+  // block-table entries are read once, independently, before any copy.
+  auto load_kv_part = [&](const UnitInfo& u, int kt, int buf, bool do_k, bool do_v) {
     const int32_t* bt_row = p.block_tables + static_cast<long long>(u.r) * p.max_blocks_per_seq;
     const long long row_stride = static_cast<long long>(Hkv) * D * 2;
     const uint32_t kdst = sbase + C::kKOff + buf * C::kTileBytes;
     const uint32_t vdst = sbase + C::kVOff + buf * C::kTileBytes;
-#pragma unroll 4
-    for (int idx = tid; idx < kTileN * C::kChunks; idx += kPfThreads) {
-      const int tt = idx / C::kChunks, c = idx - tt * C::kChunks;
-      const int tok = kt * kTileN + tt;
-      long long off = 0;
-      int bytes = 0;
-      if (tok < u.kv_end) {
-        int phys = __ldg(bt_row + tok / kBlockSize);
+    constexpr int kBlocks = kTileN / kBlockSize;
+    long long base[kBlocks];
+    int lim[kBlocks];  // tokens of block b (from its first) that exist; 0 for a bad id
+#pragma unroll
+    for (int b = 0; b < kBlocks; ++b) {
+      const int tok0 = kt * kTileN + b * kBlockSize;
+      base[b] = 0;
+      lim[b] = 0;
+      if (tok0 < u.kv_end) {
+        const int phys = __ldg(bt_row + tok0 / kBlockSize);
         if (phys < 0 || phys >= p.num_blocks) {
           flag_error(p.status, PA_DEV_BLOCK_RANGE);
         } else {
-          off = (static_cast<long long>(phys) * kBlockSize + tok % kBlockSize) * row_stride +
-                static_cast<long long>(u.g) * D * 2 + c * 16;
-          bytes = 16;
+          base[b] = static_cast<long long>(phys) * kBlockSize * row_stride +
+                    static_cast<long long>(u.g) * D * 2;
+          lim[b] = u.kv_end - tok0;
         }
       }
-      cp_async16(kdst + sw128(tt, c), kc + off, bytes);
-      cp_async16(vdst + sw128(tt, c), vc + off, bytes);
     }
+    constexpr int kRowsPerPass = kPfThreads / C::kChunks;
+    const int c = tid % C::kChunks;
+#pragma unroll
+    for (int k = 0; k < kTileN / kRowsPerPass; ++k) {
+      const int tt = tid / C::kChunks + k * kRowsPerPass;
+      const int b = (k * kRowsPerPass) / kBlockSize;  // compile-time (tt / 16)
+      const int r = tt - b * kBlockSize;
+      const int bytes = r < lim[b] ? 16 : 0;
+      const long long off = bytes ? base[b] + r * row_stride + c * 16 : 0;
+      if (do_k) cp_async16(kdst + sw128(tt, c), kc + off, bytes);
+      if (do_v) cp_async16(vdst + sw128(tt, c), vc + off, bytes);
+    }
+  };
+  auto load_kv = [&](const UnitInfo& u, int kt, int buf) { load_kv_part(u, kt, buf, true, true); };
+  auto load_kv_k = [&](const UnitInfo& u, int kt, int buf) { load_kv_part(u, kt, buf, true, false); };
+  auto load_kv_v = [&](const UnitInfo& u, int kt, int buf) { load_kv_part(u, kt, buf, false, true); };
+  // S(kt) = Q K(kt)^T into TMEM S buffer sb (one thread).
+  auto issue_s = [&](int kt, int sb) {
+    const uint32_t qa = sbase + C::kQOff, kb = sbase + C::kKOff + (kt & 1) * C::kTileBytes;
+#pragma unroll
+    for (int kk = 0; kk < D / 16; ++kk) {
+      const uint32_t koff = (kk >> 2) * (kTileM * 128) + (kk & 3) * 32;
+      tc_mma_f16(tmem_s + sb * kTileN, smem_desc_sw128(qa + koff, 16, 1024),
+                 smem_desc_sw128(kb + koff, 16, 1024), idesc_bf16(kTileM, kTileN, 0), kk > 0);
+    }
+    tc_commit(smem_u32(&mbar[0]));
   };
 
   for (;;) {
@@ -171,6 +202,8 @@ __global__ void __launch_bounds__(kPfThreads, 1) prefill_tc_kernel(const AttnPar
     }
     load_kv(u, 0, 0);
     cp_async_commit();
+    if (n_kv > 1) load_kv_k(u, 1, 1);  // K of tile 1; its V follows one tile later
+    cp_async_commit();
 
     // this thread's query row
     const int my_jj = tid / G;
@@ -178,47 +211,59 @@ __global__ void __launch_bounds__(kPfThreads, 1) prefill_tc_kernel(const AttnPar
     const int my_pos = u.pos0 + my_jj;
     float m_used = 0.f, l_sum = 0.f;
 
+    // S(0) = Q K(0)^T
+    cp_async_wait<1>();
+    fence_proxy_async_smem();
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    if (tid == 0) issue_s(0, 0);
+
+    // Per KV tile j: S(j+1) is issued before the softmax of tile j and PV(j)
+    // is left in flight, so the tensor cores work while the threads do the
+    // softmax.  Buffers: S in TMEM x2, K, V and P in shared memory x2.
     for (int kt = 0; kt < n_kv; ++kt) {
       const int buf = kt & 1;
-      if (kt + 1 < n_kv) load_kv(u, kt + 1, buf ^ 1);
-      cp_async_commit();
-      cp_async_wait<1>();
-      fence_proxy_async_smem();
-      tc_fence_before();
-      __syncthreads();
-      tc_fence_after();
-      if (tid == 0) {
-        const uint32_t qa = sbase + C::kQOff, kb = sbase + C::kKOff + buf * C::kTileBytes;
-#pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk) {
-          const uint32_t koff = (kk >> 2) * (kTileM * 128) + (kk & 3) * 32;
-          tc_mma_f16(tmem_s, smem_desc_sw128(qa + koff, 16, 1024),
-                     smem_desc_sw128(kb + koff, 16, 1024), idesc_bf16(kTileM, kTileN, 0), kk > 0);
-        }
-        tc_commit(smem_u32(&mbar[0]));
-      }
       const bool ok_s = mbar_wait(smem_u32(&mbar[0]), ph_s, kWaitLimit);
       ph_s ^= 1;
       if (__syncthreads_or(!ok_s)) { aborted = true; break; }
       tc_fence_after();
+      // PV(j-1) must be done before V(j+1) reuses its buffer (and before O is touched)
+      if (kt > 0) {
+        const bool ok_o = mbar_wait(smem_u32(&mbar[1]), ph_o, kWaitLimit);
+        ph_o ^= 1;
+        if (__syncthreads_or(!ok_o)) { aborted = true; break; }
+        tc_fence_after();
+      }
+      // K(j+1) and V(j) have landed: issue S(j+1), then load V(j+1) and K(j+2)
+      cp_async_wait<0>();
+      fence_proxy_async_smem();
+      tc_fence_before();
+      __syncthreads();
+      tc_fence_after();
+      if (tid == 0 && kt + 1 < n_kv) issue_s(kt + 1, buf ^ 1);
+      if (kt + 1 < n_kv) load_kv_v(u, kt + 1, buf ^ 1);
+      if (kt + 2 < n_kv) load_kv_k(u, kt + 2, buf);
+      cp_async_commit();
 
       // ---- softmax of this thread's row over the tile's 128 keys
+      const int tok0 = kt * kTileN;
       uint32_t sr[kTileN];
 #pragma unroll
       for (int c0 = 0; c0 < kTileN; c0 += 32) {
         uint32_t* dst = sr + c0;
-        PA_TMEM_LD32(tmem_s + lane_off + c0, dst);
+        PA_TMEM_LD32(tmem_s + buf * kTileN + lane_off + c0, dst);
       }
       tmem_wait_ld();
-      const int tok0 = kt * kTileN;
-      float mx = -CUDART_INF_F;
+      float mx4[4] = {-CUDART_INF_F, -CUDART_INF_F, -CUDART_INF_F, -CUDART_INF_F};
 #pragma unroll
       for (int t = 0; t < kTileN; ++t) {
         const bool vis = row_ok && tok0 + t <= my_pos;
         const float x = vis ? __uint_as_float(sr[t]) * p.scale_log2 : -CUDART_INF_F;
         sr[t] = __float_as_uint(x);
-        mx = fmaxf(mx, x);
+        mx4[t & 3] = fmaxf(mx4[t & 3], x);
       }
+      const float mx = fmaxf(fmaxf(mx4[0], mx4[1]), fmaxf(mx4[2], mx4[3]));
       float factor = 1.f;
       if (row_ok) {
         if (kt == 0) {
@@ -229,7 +274,8 @@ __global__ void __launch_bounds__(kPfThreads, 1) prefill_tc_kernel(const AttnPar
           m_used = mx;
         }
       }
-      // rescale O rows whose maximum moved (whole warp takes part in tcgen05.ld/st)
+      // rescale O rows whose maximum moved (whole warp takes part in tcgen05.ld/st);
+      // PV(j-1) is complete, so O is stable
       if (kt > 0 && __any_sync(0xffffffffu, factor != 1.f)) {
 #pragma unroll
         for (int c0 = 0; c0 < D; c0 += 32) {
@@ -242,9 +288,9 @@ __global__ void __launch_bounds__(kPfThreads, 1) prefill_tc_kernel(const AttnPar
         }
         tmem_wait_st();
       }
-      // P = exp2(x - m_used) as bf16, K-major rows of 128 keys
-      float psum = 0.f;
-      const uint32_t prow = sbase + C::kPOff;
+      // P = exp2(x - m_used) as bf16, K-major rows of 128 keys, into P buffer j%2
+      float ps4[4] = {0.f, 0.f, 0.f, 0.f};
+      const uint32_t prow = sbase + C::kPOff + buf * C::kPBytes;
 #pragma unroll
       for (int c = 0; c < kTileN / 8; ++c) {
         uint32_t w[4];
@@ -252,20 +298,21 @@ __global__ void __launch_bounds__(kPfThreads, 1) prefill_tc_kernel(const AttnPar
         for (int e = 0; e < 4; ++e) {
           const float p0 = exp2f(__uint_as_float(sr[c * 8 + 2 * e]) - m_used);
           const float p1 = exp2f(__uint_as_float(sr[c * 8 + 2 * e + 1]) - m_used);
-          psum += p0 + p1;
+          ps4[e] += p0 + p1;
           asm("cvt.rn.bf16x2.f32 %0, %1, %2;\n" : "=r"(w[e]) : "f"(p1), "f"(p0));
         }
         asm volatile("st.shared.v4.b32 [%0], {%1,%2,%3,%4};\n" ::"r"(prow + sw128(tid, c)),
                      "r"(w[0]), "r"(w[1]), "r"(w[2]), "r"(w[3])
                      : "memory");
       }
-      l_sum += psum;
+      l_sum += (ps4[0] + ps4[1]) + (ps4[2] + ps4[3]);
       fence_proxy_async_smem();
       tc_fence_before();
       __syncthreads();
       tc_fence_after();
       if (tid == 0) {
-        const uint32_t pa = sbase + C::kPOff, vb = sbase + C::kVOff + buf * C::kTileBytes;
+        const uint32_t pa = sbase + C::kPOff + buf * C::kPBytes;
+        const uint32_t vb = sbase + C::kVOff + buf * C::kTileBytes;
 #pragma unroll
         for (int kk = 0; kk < kTileN / 16; ++kk) {
           tc_mma_f16(tmem_o, smem_desc_sw128(pa + (kk >> 2) * (kTileM * 128) + (kk & 3) * 32, 16, 1024),
@@ -274,9 +321,11 @@ __global__ void __launch_bounds__(kPfThreads, 1) prefill_tc_kernel(const AttnPar
         }
         tc_commit(smem_u32(&mbar[1]));
       }
+    }
+    if (!aborted) {  // the last PV
       const bool ok_o = mbar_wait(smem_u32(&mbar[1]), ph_o, kWaitLimit);
       ph_o ^= 1;
-      if (__syncthreads_or(!ok_o)) { aborted = true; break; }
+      if (__syncthreads_or(!ok_o)) aborted = true;
       tc_fence_after();
     }
     if (aborted) break;
