@@ -173,3 +173,26 @@ def test_empty_step_is_a_noop():
     P.pa_cache_write(e, e, torch.empty(0, dtype=torch.int64, device="cuda"), kc, kc, lay)
     torch.cuda.synchronize()
     assert int(kc.abs().sum()) == 0
+
+
+PREFILL_SHAPES = [
+    # q_len around the tensor-core threshold (15 -> few-token tiles, 16/17 -> tcgen05)
+    ("bf16", 128, 4, [15, 16, 17], [15, 40, 17]),
+    # last 128-row tile holds one position (33 = 32 + 1 positions at G = 4)
+    ("bf16", 128, 4, [33, 1], [33, 90]),
+    # long prior context: ~40 KV tiles of 128 tokens behind a 300-token chunk
+    ("bf16", 128, 4, [300], [5000]),
+    # G = 8, D = 64: 16 positions per 128-row tile
+    ("bf16", 64, 8, [70, 1, 16], [1000, 50, 16]),
+    # G = 1: 128 positions per tile
+    ("bf16", 128, 1, [200], [260]),
+    # fp32 chunk (CUDA-core path) with splits
+    ("f32", 128, 2, [100, 1], [700, 300]),
+]
+
+
+@pytest.mark.parametrize("case", range(len(PREFILL_SHAPES)))
+def test_prefill_shapes(case):
+    dtype, D, G, q_lens, seq_lens = PREFILL_SHAPES[case]
+    spec = W.custom_spec(f"prefill-{case}", dtype, 2 * G, 2, D, q_lens, seq_lens, seed=200 + case)
+    _full_parity(W.make_step(spec))
