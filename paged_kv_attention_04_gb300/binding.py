@@ -81,6 +81,23 @@ def _ptr(t) -> int | None:
     return None if t is None else t.data_ptr()
 
 
+def _on_one_device(**tensors) -> None:
+    """Every tensor argument must be a contiguous CUDA tensor, all on one
+    device (a host pointer would reach the kernels unchecked)."""
+    dev = None
+    for name, t in tensors.items():
+        if t is None:
+            continue
+        if not t.is_cuda:
+            raise PaError(PA_ERR_INVALID, f"{name} is not a CUDA tensor")
+        if not t.is_contiguous():
+            raise PaError(PA_ERR_INVALID, f"{name} is not contiguous")
+        if dev is None:
+            dev = t.device
+        elif t.device != dev:
+            raise PaError(PA_ERR_INVALID, f"{name} is on {t.device}, expected {dev}")
+
+
 def _stream(stream) -> int | None:
     if stream is None:
         return torch.cuda.current_stream().cuda_stream
@@ -119,6 +136,8 @@ def layout_of(k_cache: torch.Tensor, num_q_heads: int, dtype=None, k_scale: floa
 def pa_cache_write(k, v, slot_mapping, k_cache, v_cache, layout: pa_layout,
                    status: torch.Tensor | None = None, stream=None) -> None:
     """Write k[t], v[t] into slot slot_mapping[t] of the caches (in place)."""
+    _on_one_device(k=k, v=v, slot_mapping=slot_mapping, k_cache=k_cache, v_cache=v_cache,
+                   status=status)
     _check(lib().pa_cache_write(_ptr(k), _ptr(v), _ptr(slot_mapping), int(k.shape[0]),
                                 _ptr(k_cache), _ptr(v_cache), ctypes.byref(layout),
                                 _ptr(status), _stream(stream)))
@@ -137,6 +156,9 @@ def pa_forward(q, k_cache, v_cache, block_tables, seq_lens, query_start_loc,
                max_query_len: int, max_seq_len: int, scale: float, out, workspace,
                layout: pa_layout, status: torch.Tensor | None = None, stream=None) -> None:
     """Attention for every row of the flattened step, written into `out`."""
+    _on_one_device(q=q, k_cache=k_cache, v_cache=v_cache, block_tables=block_tables,
+                   seq_lens=seq_lens, query_start_loc=query_start_loc, out=out,
+                   workspace=workspace, status=status)
     _check(lib().pa_forward(_ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(block_tables),
                             int(block_tables.shape[1]), _ptr(seq_lens), _ptr(query_start_loc),
                             int(seq_lens.shape[0]), int(q.shape[0]), int(max_query_len),
@@ -150,6 +172,8 @@ def pa_forward_noalloc(q, k_cache, v_cache, block_tables, seq_lens, query_start_
                        layout: pa_layout, status: torch.Tensor | None = None, stream=None) -> None:
     """pa_forward using the library's built-in device scratch instead of a
     caller workspace (for callers that cannot allocate device memory)."""
+    _on_one_device(q=q, k_cache=k_cache, v_cache=v_cache, block_tables=block_tables,
+                   seq_lens=seq_lens, query_start_loc=query_start_loc, out=out, status=status)
     _check(lib().pa_forward_noalloc(_ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(block_tables),
                                     int(block_tables.shape[1]), _ptr(seq_lens),
                                     _ptr(query_start_loc), int(seq_lens.shape[0]), int(q.shape[0]),

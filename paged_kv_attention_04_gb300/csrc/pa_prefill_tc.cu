@@ -1,29 +1,40 @@
-// Chunked-prefill attention on the 5th-generation tensor cores (tcgen05).
+// Chunked-prefill attention on the 5th-generation tensor cores (tcgen05),
+// warp-specialised.
 //
 // A chunk of L new tokens of a request with S KV tokens: row j sits at
 // position S - L + j and sees positions 0 .. S - L + j, its earlier chunks
 // read back from the paged cache ("Serving models at scale with vLLM",
 // section Chunked prefill; "Inside vLLM", section Chunked prefill).  With
-// query length > 1 the two products are dense, so they run on tcgen05:
+// query length > 1 the two products are dense, so they run on tcgen05.
 //
-//   * a work unit is (request, kv head g, 128-row query tile); the rows are
-//     128/G positions x the G q heads that share kv head g, so each K/V byte
-//     staged serves 128 query rows;
-//   * K and V tiles of 128 tokens (8 KV blocks, gathered through the block
-//     table) are double-buffered by cp.async into 128-byte-swizzled shared
-//     memory; Q, K and P are K-major operands, V an MN-major operand;
-//   * S = Q K^T and O += P V are issued by one thread as
-//     tcgen05.mma.kind::f16 (bf16 in, fp32 accumulate) into tensor memory;
-//     completion is signalled through mbarriers (bounded waits);
-//   * softmax: thread i owns query row i = TMEM lane i, reads its S row with
-//     tcgen05.ld, masks causally, and writes P (bf16) back to shared memory.
-//     The running maximum is only moved when a row's maximum grows by more
-//     than 2^8 (base-2 logits), so O in tensor memory is rescaled rarely;
-//     between moves p <= 2^8, well inside fp32 and bf16 range.
-// Keys past the last visible position are zero-filled in V so masked
-// probabilities never meet unwritten (NaN) cache slots.
+// Work unit: (request, kv head g, 128-row query tile); the rows are 128/G
+// positions x the G q heads that share kv head g, so every K/V byte staged
+// serves 128 query rows.  Units are fetched from a counter, longest first.
+// One CTA per SM, 11 warps with fixed roles:
+//   * warps 8 and 10 (loaders): warp 8 fetches units and copies the Q tile
+//     and the K tiles of 128 keys, warp 10 the V tiles, all by TMA into
+//     128-byte-swizzled shared memory; a K/V tile is gathered through the
+//     block table one 16-token block (one box) at a time, blocks past the
+//     unit's keys read out of bounds, which fills zeros.  Each unit starts at
+//     a different KV tile (rotated by its query tile), so the CTAs that share
+//     a kv head do not read the same lines at the same time;
+//   * warp 9 (MMA): one thread issues S = Q K^T and O += P V as
+//     tcgen05.mma.kind::f16 (bf16 in, fp32 accumulate in tensor memory);
+//   * warps 0-3 and 4-7: two softmax warpgroups.  Warpgroup w takes the KV
+//     tiles t = w, w + 2, ... of the unit, with its own K, V and P buffers and
+//     its own S and O in tensor memory, so one group's softmax runs while the
+//     tensor cores serve the other.  Thread i owns query row i = TMEM lane i;
+//     the running maximum moves only when a row's maximum grows by more than
+//     2^8 (base-2 logits), so O is rescaled rarely.  At the end of the unit
+//     the two partial states (m, l, O) are merged (log-sum-exp) and written.
+// Hand-offs are mbarriers; every wait is bounded and a timeout makes the whole
+// CTA stop (status PA_DEV_TIMEOUT), drain its copies and MMAs, and free TMEM.
+#include <cuda.h>
+#include <cudaTypedefs.h>
 #include <cuda_bf16.h>
 #include <math_constants.h>
+
+#include <mutex>
 
 #include "pa_device.cuh"
 #include "pa_internal.h"
@@ -33,26 +44,65 @@ namespace pa {
 
 namespace {
 
-constexpr int kTileM = 128;              // query rows per unit
-constexpr int kTileN = 128;              // KV tokens per tile
-constexpr int kPfThreads = 128;          // one thread per query row
+constexpr int kTileM = 128;  // query rows per unit
+constexpr int kTileN = 128;  // keys per KV tile
+constexpr int kKLoadWarp = 8;   // unit fetch, Q (TMA), K tiles
+constexpr int kMmaWarp = 9;
+constexpr int kVLoadWarp = 10;  // V tiles
+constexpr int kPfThreads = 352;
 constexpr uint32_t kWaitLimit = 1u << 24;
-constexpr float kRescaleThreshold = 8.f; // base-2 logit growth that forces a rescale
+constexpr float kRescaleThreshold = 8.f;  // base-2 logit growth that forces a rescale
 
 template <int D>
 struct PfCfg {
-  static constexpr int kRegions = D / 64;                 // 128-byte column groups
-  static constexpr int kTileBytes = kTileM * D * 2;       // Q, K or V tile
-  static constexpr int kPBytes = kTileM * kTileN * 2;     // P tile
+  static constexpr int kRegionBytes = kTileM * 128;     // 128 rows x 64 bf16
+  static constexpr int kTileBytes = kTileM * D * 2;     // Q, K or V tile
+  static constexpr int kPBytes = kTileM * kTileN * 2;   // P tile
   static constexpr int kQOff = 0;
-  static constexpr int kKOff = kQOff + kTileBytes;        // 2 buffers
-  static constexpr int kVOff = kKOff + 2 * kTileBytes;    // 2 buffers
-  static constexpr int kPOff = kVOff + 2 * kTileBytes;    // 2 buffers
+  static constexpr int kKOff = kQOff + kTileBytes;      // K0, K1
+  static constexpr int kVOff = kKOff + 2 * kTileBytes;  // V0, V1
+  static constexpr int kPOff = kVOff + 2 * kTileBytes;  // P0, P1
   static constexpr int kSmemBytes = kPOff + 2 * kPBytes + 1024;  // + alignment slack
-  static constexpr int kTmemCols = 512;                   // S x 2 (256) + O (D <= 128)
-  static constexpr int kChunks = D / 8;                   // 16-byte chunks per row
+  static constexpr int kTmemCols = 512;  // S0, S1 at 0 / 128; O0, O1 at 256 / 384
   static_assert(D == 64 || D == 128, "head size 64 or 128");
+  static_assert(kTileN == kTileM, "K and V tiles share the Q tile geometry");
   static_assert(kSmemBytes <= 227 * 1024, "shared memory per CTA exceeds 227 KB");
+};
+
+// mbarriers.  [2] = one per softmax warpgroup (or ring slot).
+enum Bar : int {
+  kUnitFull = 0,    // [2] unit info published (loader)
+  kUnitEmpty = 2,   // [2] unit info read (8 softmax warps, MMA warp, V loader)
+  kQFull = 4,       // Q tile landed (TMA)
+  kQEmpty = 5,      // every S of the unit done (MMA commit)
+  kKFull = 6,       // [2] K tile landed (TMA)
+  kSFull = 8,       // [2] S = Q K^T done (MMA commit); also frees the K buffer
+  kSEmpty = 10,     // [2] S read into registers (4 warps)
+  kVFull = 12,      // [2] V tile landed (TMA)
+  kPFull = 14,      // [2] P written (4 warps)
+  kPVDone = 16,     // [2] O += P V done (MMA commit); frees V and P, O stable
+  kMlFull = 18,     // row (m, l) of both groups published (8 warps)
+  kMlRead = 19,     // ... and read (8 warps)
+  kOFree = 20,      // O of both groups read by the epilogue (8 warps)
+  kDrain = 21,      // teardown after a timeout
+  kNumBars = 22
+};
+
+struct UnitInfo {
+  int r, g, a, j0, npos, pos0, kv_end, n_kv;  // r < 0: no more units
+  int rot;                                    // KV tile processed first
+};
+
+// KV tile processed s-th in unit u (tiles are visited in rotated order).
+__device__ __forceinline__ int tile_of(const UnitInfo& u, int s) {
+  const int t = s + u.rot;
+  return t >= u.n_kv ? t - u.n_kv : t;
+}
+
+struct PfMaps {
+  CUtensorMap q;  // q [T][Hq][D] as 3-D (D, Hq, T), box (64, G, 128/G)
+  CUtensorMap k;  // k_cache [NB][16][Hkv][D] as 4-D (D, Hkv, 16, NB), box (64, 1, 16, 1)
+  CUtensorMap v;
 };
 
 // Byte offset of 16-byte chunk c of row r in a 128-byte-swizzled tile whose
@@ -61,121 +111,134 @@ __device__ __forceinline__ uint32_t sw128(int r, int c) {
   return static_cast<uint32_t>((c >> 3) * (kTileM * 128) + r * 128 + (((c & 7) ^ (r & 7)) << 4));
 }
 
-struct UnitInfo {
-  int r, g, a, j0, npos, pos0, kv_end;
-};
+__device__ __forceinline__ float ex2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;\n" : "=f"(y) : "f"(x));
+  return y;
+}
+
+// Warp-uniform bounded wait for phase `parity` of `bar`; false after a
+// timeout (which it records) or once another role has given up.
+__device__ __forceinline__ bool wait_bar(uint32_t bar, uint32_t parity, volatile int* abort,
+                                         int32_t* status) {
+  for (uint32_t i = 0; i < kWaitLimit; ++i) {
+    const bool ok = mbar_try_wait(bar, parity);
+    if (__all_sync(0xffffffffu, ok)) return true;
+    if (__any_sync(0xffffffffu, *abort != 0)) return false;
+  }
+  if ((threadIdx.x & 31) == 0) {
+    *abort = 1;
+    flag_error(status, PA_DEV_TIMEOUT);
+  }
+  __syncwarp();
+  return false;
+}
+
+// Arrivals that complete a phase of each barrier.
+__device__ __forceinline__ uint32_t bar_count(int i) {
+  if (i == kUnitEmpty || i == kUnitEmpty + 1) return 10;  // 8 softmax warps, MMA, V loader
+  if (i == kSEmpty || i == kSEmpty + 1 || i == kPFull || i == kPFull + 1) return 4;
+  if (i == kMlFull || i == kMlRead || i == kOFree) return 8;
+  return 1;  // TMA (arrive + bytes) or tcgen05.commit
+}
+
+// Teardown wait (warp-uniform, bounded, ignores the abort flag).
+__device__ __forceinline__ void drain_wait(uint32_t bar, uint32_t parity) {
+  for (uint32_t i = 0; i < kWaitLimit; ++i)
+    if (__all_sync(0xffffffffu, mbar_try_wait(bar, parity))) return;
+}
+
+// One arrival per warp, after every lane's preceding work.
+__device__ __forceinline__ void warp_arrive(uint32_t bar) {
+  __syncwarp();
+  if ((threadIdx.x & 31) == 0) mbar_arrive(bar);
+}
+
+__device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
+  uint32_t w;
+  asm("cvt.rn.bf16x2.f32 %0, %1, %2;\n" : "=r"(w) : "f"(hi), "f"(lo));
+  return w;
+}
 
 }  // namespace
 
 template <int D, int G>
-__global__ void __launch_bounds__(kPfThreads, 1) prefill_tc_kernel(const AttnParams p) {
+__global__ void __launch_bounds__(kPfThreads, 1)
+    prefill_tc_kernel(const AttnParams p, const __grid_constant__ PfMaps maps) {
   using C = PfCfg<D>;
   constexpr int PM = kTileM / G;  // positions per unit
   extern __shared__ unsigned char smem_raw[];
-  __shared__ __align__(8) uint64_t mbar[3];  // S done, O done, drain
-  __shared__ uint32_t tmem_slot;
-  __shared__ int s_unit;
-  __shared__ UnitInfo s_info;
+  __shared__ __align__(8) uint64_t bars[kNumBars];
+  __shared__ UnitInfo s_units[2];
+  __shared__ uint32_t s_tmem;
+  __shared__ int s_abort;
 
   unsigned char* smem = reinterpret_cast<unsigned char*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
   const uint32_t sbase = smem_u32(smem);
   const int tid = threadIdx.x;
-  const int warp = tid >> 5;
-  const int Hkv = p.num_kv_heads, Hq = p.num_q_heads;
-  const unsigned char* kc = static_cast<const unsigned char*>(p.k_cache);
-  const unsigned char* vc = static_cast<const unsigned char*>(p.v_cache);
-  const __nv_bfloat16* q = static_cast<const __nv_bfloat16*>(p.q);
-  __nv_bfloat16* out = static_cast<__nv_bfloat16*>(p.out);
-  const int n_units = __ldg(p.n_items) * Hkv;
+  const int warp = tid >> 5, lane = tid & 31;
+  volatile int* abort = &s_abort;
+  auto bar = [&](int i) { return smem_u32(&bars[i]); };
 
   if (tid == 0) {
-    mbar_init(smem_u32(&mbar[0]), 1);
-    mbar_init(smem_u32(&mbar[1]), 1);
-    mbar_init(smem_u32(&mbar[2]), 1);
+    for (int i = 0; i < kNumBars; ++i) mbar_init(bar(i), bar_count(i));
+    s_abort = 0;
     mbar_fence_init();
   }
-  if (warp == 0) tmem_alloc(smem_u32(&tmem_slot), C::kTmemCols);
+  if (warp == 0) tmem_alloc(smem_u32(&s_tmem), C::kTmemCols);
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
-  const uint32_t tmem = tmem_slot;
-  const uint32_t tmem_s = tmem;        // S: two buffers, columns [0, 128) and [128, 256)
-  const uint32_t tmem_o = tmem + 256;  // O: columns [256, 256 + D)
-  const uint32_t lane_off = static_cast<uint32_t>(warp * 32) << 16;
-  uint32_t ph_s = 0, ph_o = 0;
-  bool aborted = false;
+  const uint32_t tmem = s_tmem;
 
-  // Load the K or V half (or both) of KV tile kt (tokens kt*128 ..) of unit u
-  // into buffer buf.  Lanes take consecutive 16-byte chunks of a row (2 rows
-  // per warp instruction for D=128); with the loop unrolled, the KV block of
-  // every chunk a thread copies is known at compile time, so the tile's 8
-  // block-table entries are read once, independently, before any copy.
-  auto load_kv_part = [&](const UnitInfo& u, int kt, int buf, bool do_k, bool do_v) {
-    const int32_t* bt_row = p.block_tables + static_cast<long long>(u.r) * p.max_blocks_per_seq;
-    const long long row_stride = static_cast<long long>(Hkv) * D * 2;
-    const uint32_t kdst = sbase + C::kKOff + buf * C::kTileBytes;
-    const uint32_t vdst = sbase + C::kVOff + buf * C::kTileBytes;
-    constexpr int kBlocks = kTileN / kBlockSize;
-    long long base[kBlocks];
-    int lim[kBlocks];  // tokens of block b (from its first) that exist; 0 for a bad id
-#pragma unroll
-    for (int b = 0; b < kBlocks; ++b) {
-      const int tok0 = kt * kTileN + b * kBlockSize;
-      base[b] = 0;
-      lim[b] = 0;
-      if (tok0 < u.kv_end) {
-        const int phys = __ldg(bt_row + tok0 / kBlockSize);
-        if (phys < 0 || phys >= p.num_blocks) {
-          flag_error(p.status, PA_DEV_BLOCK_RANGE);
-        } else {
-          base[b] = static_cast<long long>(phys) * kBlockSize * row_stride +
-                    static_cast<long long>(u.g) * D * 2;
-          lim[b] = u.kv_end - tok0;
-        }
-      }
+  // Physical block of KV block `lane` (< 8) of tile t, -1 past the unit's
+  // keys; checked where it is used, so the load's latency stays hidden.
+  auto tile_phys = [&](const UnitInfo& u, int t) {
+    const int lb = t * (kTileN / kBlockSize) + lane;
+    if (lane < kTileN / kBlockSize && lb * kBlockSize < u.kv_end)
+      return __ldg(p.block_tables + static_cast<long long>(u.r) * p.max_blocks_per_seq + lb);
+    return -1;
+  };
+  // TMA copy of KV tile t of unit u into the swizzled buffer at dst: lane
+  // b < 8 copies block b (one box per 64 columns); a block past the unit's
+  // keys or with a bad table entry is read at index num_blocks (zeros).
+  auto copy_kv_tile = [&](const UnitInfo& u, int t, int ph, const CUtensorMap* map, uint32_t dst,
+                          uint32_t full) {
+    if (lane < kTileN / kBlockSize && ph != -1 && (ph < 0 || ph >= p.num_blocks)) {
+      flag_error(p.status, PA_DEV_BLOCK_RANGE);
+      ph = -1;
     }
-    constexpr int kRowsPerPass = kPfThreads / C::kChunks;
-    const int c = tid % C::kChunks;
+    if (lane == 0) mbar_arrive_expect_tx(full, C::kTileBytes);
+    __syncwarp();
+    if (lane < kTileN / kBlockSize) {
+      const int coord = ph < 0 ? p.num_blocks : ph;
 #pragma unroll
-    for (int k = 0; k < kTileN / kRowsPerPass; ++k) {
-      const int tt = tid / C::kChunks + k * kRowsPerPass;
-      const int b = (k * kRowsPerPass) / kBlockSize;  // compile-time (tt / 16)
-      const int r = tt - b * kBlockSize;
-      const int bytes = r < lim[b] ? 16 : 0;
-      const long long off = bytes ? base[b] + r * row_stride + c * 16 : 0;
-      if (do_k) cp_async16(kdst + sw128(tt, c), kc + off, bytes);
-      if (do_v) cp_async16(vdst + sw128(tt, c), vc + off, bytes);
+      for (int h = 0; h < D / 64; ++h)
+        tma_load_4d(dst + h * C::kRegionBytes + lane * (kBlockSize * 128), map, h * 64, u.g, 0,
+                    coord, full);
     }
   };
-  auto load_kv = [&](const UnitInfo& u, int kt, int buf) { load_kv_part(u, kt, buf, true, true); };
-  auto load_kv_k = [&](const UnitInfo& u, int kt, int buf) { load_kv_part(u, kt, buf, true, false); };
-  auto load_kv_v = [&](const UnitInfo& u, int kt, int buf) { load_kv_part(u, kt, buf, false, true); };
-  // S(kt) = Q K(kt)^T into TMEM S buffer sb (one thread).
-  auto issue_s = [&](int kt, int sb) {
-    const uint32_t qa = sbase + C::kQOff, kb = sbase + C::kKOff + (kt & 1) * C::kTileBytes;
-#pragma unroll
-    for (int kk = 0; kk < D / 16; ++kk) {
-      const uint32_t koff = (kk >> 2) * (kTileM * 128) + (kk & 3) * 32;
-      tc_mma_f16(tmem_s + sb * kTileN, smem_desc_sw128(qa + koff, 16, 1024),
-                 smem_desc_sw128(kb + koff, 16, 1024), idesc_bf16(kTileM, kTileN, 0), kk > 0);
-    }
-    tc_commit(smem_u32(&mbar[0]));
-  };
 
-  for (;;) {
-    if (tid == 0) {
-      const int unit = atomicAdd(p.next, 1);
-      s_unit = unit;
+  if (warp == kKLoadWarp) {
+    // ------------------------------------------------------------ units, Q, K
+    const int Hkv = p.num_kv_heads;
+    const int n_units = __ldg(p.n_items) * Hkv;
+    uint32_t nk[2] = {0, 0}, nq = 0;
+    for (int uc = 0;; ++uc) {
+      int unit = 0;
+      if (lane == 0) unit = atomicAdd(p.next, 1);
+      unit = __shfl_sync(0xffffffffu, unit, 0);
+      UnitInfo u;
+      u.r = -1;
       if (unit < n_units) {
         // last tile first: within a chunk later query tiles see more keys, and
-        // later chunks of the step carry more prior context, so long units start first
+        // later chunks of the step carry more prior context
         const int tile = __ldg(p.n_items) - 1 - unit / Hkv;
         const int4 tr = __ldg(p.items + tile);
         const int S = __ldg(p.seq_lens + tr.x);
         const int a = __ldg(p.qsl + tr.x);
         const int L = __ldg(p.qsl + tr.x + 1) - a;
-        UnitInfo u;
         u.r = tr.x;
         u.g = unit % Hkv;
         u.a = a;
@@ -183,187 +246,352 @@ __global__ void __launch_bounds__(kPfThreads, 1) prefill_tc_kernel(const AttnPar
         u.npos = min(PM, L - u.j0);
         u.pos0 = S - L + u.j0;
         u.kv_end = u.pos0 + u.npos;
-        s_info = u;
+        u.n_kv = (u.kv_end + kTileN - 1) / kTileN;
+        u.rot = tr.y % u.n_kv;
       }
+      const int slot = uc & 1;
+      if (uc >= 2 && !wait_bar(bar(kUnitEmpty + slot), ((uc >> 1) - 1) & 1, abort, p.status)) break;
+      if (lane == 0) {
+        s_units[slot] = u;
+        mbar_arrive(bar(kUnitFull + slot));
+      }
+      if (u.r < 0) break;
+
+      int ph = tile_phys(u, tile_of(u, 0));
+      // Q tile: rows (position, head) of 128/G tokens x G heads, one box per 64 columns
+      if (uc > 0 && !wait_bar(bar(kQEmpty), (uc - 1) & 1, abort, p.status)) break;
+      if (lane == 0) {
+        mbar_arrive_expect_tx(bar(kQFull), C::kTileBytes);
+#pragma unroll
+        for (int h = 0; h < D / 64; ++h)
+          tma_load_3d(sbase + C::kQOff + h * C::kRegionBytes, &maps.q, h * 64, u.g * G,
+                      u.a + u.j0, bar(kQFull));
+      }
+      ++nq;
+      bool ok = true;
+      for (int sq = 0; sq < u.n_kv; ++sq) {
+        const int w = sq & 1;
+        // K buffer w is free once S of the group's previous tile is done
+        if (nk[w] > 0 && !wait_bar(bar(kSFull + w), (nk[w] - 1) & 1, abort, p.status)) {
+          ok = false;
+          break;
+        }
+        copy_kv_tile(u, tile_of(u, sq), ph, &maps.k, sbase + C::kKOff + w * C::kTileBytes,
+                     bar(kKFull + w));
+        ++nk[w];
+        if (sq + 1 < u.n_kv) ph = tile_phys(u, tile_of(u, sq + 1));
+      }
+      if (!ok) break;
     }
-    __syncthreads();
-    if (s_unit >= n_units || aborted) break;
-    const UnitInfo u = s_info;
-    const int n_kv = (u.kv_end + kTileN - 1) / kTileN;
-
-    // Q tile: row i = (position i / G, head i % G); rows past the chunk are zero
-    for (int idx = tid; idx < kTileM * C::kChunks; idx += kPfThreads) {
-      const int row = idx / C::kChunks, c = idx - row * C::kChunks;
-      const int jj = row / G, hh = row - jj * G;
-      const bool ok = jj < u.npos;
-      const long long tok = u.a + u.j0 + (ok ? jj : 0);
-      cp_async16(sbase + C::kQOff + sw128(row, c),
-                 q + (tok * Hq + u.g * G + hh) * D + c * 8, ok ? 16 : 0);
+    if (*abort) {  // let every copy issued land before the CTA ends
+      if (nq > 0) drain_wait(bar(kQFull), (nq - 1) & 1);
+      for (int w = 0; w < 2; ++w)
+        if (nk[w] > 0) drain_wait(bar(kKFull + w), (nk[w] - 1) & 1);
     }
-    load_kv(u, 0, 0);
-    cp_async_commit();
-    if (n_kv > 1) load_kv_k(u, 1, 1);  // K of tile 1; its V follows one tile later
-    cp_async_commit();
-
-    // this thread's query row
-    const int my_jj = tid / G;
-    const bool row_ok = my_jj < u.npos;
-    const int my_pos = u.pos0 + my_jj;
-    float m_used = 0.f, l_sum = 0.f;
-
-    // S(0) = Q K(0)^T
-    cp_async_wait<1>();
-    fence_proxy_async_smem();
-    tc_fence_before();
-    __syncthreads();
-    tc_fence_after();
-    if (tid == 0) issue_s(0, 0);
-
-    // Per KV tile j: S(j+1) is issued before the softmax of tile j and PV(j)
-    // is left in flight, so the tensor cores work while the threads do the
-    // softmax.  Buffers: S in TMEM x2, K, V and P in shared memory x2.
-    for (int kt = 0; kt < n_kv; ++kt) {
-      const int buf = kt & 1;
-      const bool ok_s = mbar_wait(smem_u32(&mbar[0]), ph_s, kWaitLimit);
-      ph_s ^= 1;
-      if (__syncthreads_or(!ok_s)) { aborted = true; break; }
+    __syncwarp();
+  } else if (warp == kVLoadWarp) {
+    // ------------------------------------------------------------ V
+    uint32_t nv[2] = {0, 0};
+    for (int uc = 0;; ++uc) {
+      const int slot = uc & 1;
+      if (!wait_bar(bar(kUnitFull + slot), (uc >> 1) & 1, abort, p.status)) break;
+      const UnitInfo u = s_units[slot];
+      warp_arrive(bar(kUnitEmpty + slot));
+      if (u.r < 0) break;
+      int ph = tile_phys(u, tile_of(u, 0));
+      bool ok = true;
+      for (int sq = 0; sq < u.n_kv; ++sq) {
+        const int w = sq & 1;
+        // V buffer w is free once PV of the group's previous tile is done
+        if (nv[w] > 0 && !wait_bar(bar(kPVDone + w), (nv[w] - 1) & 1, abort, p.status)) {
+          ok = false;
+          break;
+        }
+        copy_kv_tile(u, tile_of(u, sq), ph, &maps.v, sbase + C::kVOff + w * C::kTileBytes,
+                     bar(kVFull + w));
+        ++nv[w];
+        if (sq + 1 < u.n_kv) ph = tile_phys(u, tile_of(u, sq + 1));
+      }
+      if (!ok) break;
+    }
+    if (*abort) {
+      for (int w = 0; w < 2; ++w)
+        if (nv[w] > 0) drain_wait(bar(kVFull + w), (nv[w] - 1) & 1);
+    }
+    __syncwarp();
+  } else if (warp == kMmaWarp) {
+    // ------------------------------------------------------------ MMA issue
+    uint32_t ns[2] = {0, 0}, npv[2] = {0, 0};
+    bool ok = true;
+    for (int uc = 0; ok; ++uc) {
+      const int slot = uc & 1;
+      if (!wait_bar(bar(kUnitFull + slot), (uc >> 1) & 1, abort, p.status)) break;
+      const UnitInfo u = s_units[slot];
+      warp_arrive(bar(kUnitEmpty + slot));
+      if (u.r < 0) break;
+      if (!wait_bar(bar(kQFull), uc & 1, abort, p.status)) break;
       tc_fence_after();
-      // PV(j-1) must be done before V(j+1) reuses its buffer (and before O is touched)
-      if (kt > 0) {
-        const bool ok_o = mbar_wait(smem_u32(&mbar[1]), ph_o, kWaitLimit);
-        ph_o ^= 1;
-        if (__syncthreads_or(!ok_o)) { aborted = true; break; }
+
+      auto issue_s = [&](int t) {
+        const int w = t & 1;
+        const uint32_t n = ns[w];
+        if (!wait_bar(bar(kKFull + w), n & 1, abort, p.status)) return false;
+        if (n > 0 && !wait_bar(bar(kSEmpty + w), (n - 1) & 1, abort, p.status)) return false;
         tc_fence_after();
-      }
-      // K(j+1) and V(j) have landed: issue S(j+1), then load V(j+1) and K(j+2)
-      cp_async_wait<0>();
-      fence_proxy_async_smem();
-      tc_fence_before();
-      __syncthreads();
-      tc_fence_after();
-      if (tid == 0 && kt + 1 < n_kv) issue_s(kt + 1, buf ^ 1);
-      if (kt + 1 < n_kv) load_kv_v(u, kt + 1, buf ^ 1);
-      if (kt + 2 < n_kv) load_kv_k(u, kt + 2, buf);
-      cp_async_commit();
-
-      // ---- softmax of this thread's row over the tile's 128 keys
-      const int tok0 = kt * kTileN;
-      uint32_t sr[kTileN];
+        if (lane == 0) {
+          const uint32_t qa = sbase + C::kQOff, kb = sbase + C::kKOff + w * C::kTileBytes;
 #pragma unroll
-      for (int c0 = 0; c0 < kTileN; c0 += 32) {
-        uint32_t* dst = sr + c0;
-        PA_TMEM_LD32(tmem_s + buf * kTileN + lane_off + c0, dst);
-      }
-      tmem_wait_ld();
-      float mx4[4] = {-CUDART_INF_F, -CUDART_INF_F, -CUDART_INF_F, -CUDART_INF_F};
+          for (int kk = 0; kk < D / 16; ++kk) {
+            const uint32_t koff = (kk >> 2) * C::kRegionBytes + (kk & 3) * 32;
+            tc_mma_f16(tmem + w * kTileN, smem_desc_sw128(qa + koff, 16, 1024),
+                       smem_desc_sw128(kb + koff, 16, 1024), idesc_bf16(kTileM, kTileN, 0),
+                       kk > 0);
+          }
+          tc_commit(bar(kSFull + w));
+        }
+        __syncwarp();
+        ns[w] = n + 1;
+        return true;
+      };
+      auto issue_pv = [&](int t) {
+        const int w = t & 1;
+        const uint32_t n = npv[w];
+        if (!wait_bar(bar(kPFull + w), n & 1, abort, p.status)) return false;
+        if (!wait_bar(bar(kVFull + w), n & 1, abort, p.status)) return false;
+        // the previous unit's epilogue must have read O before it is overwritten
+        if (t == 0 && uc > 0 && !wait_bar(bar(kOFree), (uc - 1) & 1, abort, p.status)) return false;
+        tc_fence_after();
+        if (lane == 0) {
+          const uint32_t pa = sbase + C::kPOff + w * C::kPBytes;
+          const uint32_t vb = sbase + C::kVOff + w * C::kTileBytes;
 #pragma unroll
-      for (int t = 0; t < kTileN; ++t) {
-        const bool vis = row_ok && tok0 + t <= my_pos;
-        const float x = vis ? __uint_as_float(sr[t]) * p.scale_log2 : -CUDART_INF_F;
-        sr[t] = __float_as_uint(x);
-        mx4[t & 3] = fmaxf(mx4[t & 3], x);
-      }
-      const float mx = fmaxf(fmaxf(mx4[0], mx4[1]), fmaxf(mx4[2], mx4[3]));
-      float factor = 1.f;
-      if (row_ok) {
-        if (kt == 0) {
-          m_used = mx;  // position 0 is visible to every row, so mx is finite
-        } else if (mx > m_used + kRescaleThreshold) {
-          factor = exp2f(m_used - mx);
-          l_sum *= factor;
-          m_used = mx;
+          for (int kk = 0; kk < kTileN / 16; ++kk)
+            tc_mma_f16(tmem + 256 + w * 128,
+                       smem_desc_sw128(pa + (kk >> 2) * C::kRegionBytes + (kk & 3) * 32, 16, 1024),
+                       smem_desc_sw128(vb + kk * 2048, C::kRegionBytes, 1024),
+                       idesc_bf16(kTileM, D, 1), (t >= 2 || kk > 0) ? 1u : 0u);
+          tc_commit(bar(kPVDone + w));
+        }
+        __syncwarp();
+        npv[w] = n + 1;
+        return true;
+      };
+      auto release_q = [&]() {
+        if (lane == 0) tc_commit(bar(kQEmpty));
+        __syncwarp();
+      };
+      // PV(t) goes before S(t + 2): when a group's next S is done, so is its
+      // previous PV (a commit covers every earlier MMA), so its softmax never
+      // waits for P or O to be free; the other group keeps the tensor cores busy
+      ok = issue_s(0) && (u.n_kv < 2 || issue_s(1));
+      if (ok && u.n_kv <= 2) release_q();
+      for (int t = 0; ok && t < u.n_kv; ++t) {
+        ok = issue_pv(t);
+        if (ok && t + 2 < u.n_kv) {
+          ok = issue_s(t + 2);
+          if (ok && t + 2 == u.n_kv - 1) release_q();
         }
       }
-      // rescale O rows whose maximum moved (whole warp takes part in tcgen05.ld/st);
-      // PV(j-1) is complete, so O is stable
-      if (kt > 0 && __any_sync(0xffffffffu, factor != 1.f)) {
-#pragma unroll
-        for (int c0 = 0; c0 < D; c0 += 32) {
-          uint32_t o[32];
-          PA_TMEM_LD32(tmem_o + lane_off + c0, o);
+    }
+    if (*abort) {  // every MMA issued must finish before TMEM is released
+      if (lane == 0) tc_commit(bar(kDrain));
+      __syncwarp();
+      drain_wait(bar(kDrain), 0);
+    }
+    __syncwarp();
+  } else {
+    // ------------------------------------------------------------ softmax
+    const int w = warp >> 2;       // warpgroup
+    const int i = tid & 127;       // query row = TMEM lane
+    const uint32_t lane_off = static_cast<uint32_t>((warp & 3) * 32) << 16;
+    const uint32_t tmem_s = tmem + w * kTileN + lane_off;
+    const uint32_t tmem_o0 = tmem + 256 + lane_off, tmem_o1 = tmem + 384 + lane_off;
+    const float sl2 = p.scale_log2;
+    const int Hq = p.num_q_heads;
+    __nv_bfloat16* out = static_cast<__nv_bfloat16*>(p.out);
+    const uint32_t pbuf = sbase + C::kPOff + w * C::kPBytes;
+    uint32_t n = 0;  // this group's tiles so far (all units)
+    for (int uc = 0;; ++uc) {
+      const int slot = uc & 1;
+      if (!wait_bar(bar(kUnitFull + slot), (uc >> 1) & 1, abort, p.status)) break;
+      const UnitInfo u = s_units[slot];
+      warp_arrive(bar(kUnitEmpty + slot));
+      if (u.r < 0) break;
+      const int jj = i / G;
+      const bool row_ok = jj < u.npos;
+      const int my_pos = u.pos0 + jj;
+      float m_used = -CUDART_INF_F, l_sum = 0.f;
+      bool ok = true;
+      for (int t = w; t < u.n_kv; t += 2, ++n) {  // t: place in the unit's order
+        const int kt = tile_of(u, t);
+        const int tok0 = kt * kTileN;
+        if (!wait_bar(bar(kSFull + w), n & 1, abort, p.status)) { ok = false; break; }
+        // this group's previous PV is complete as well (S of this tile was
+        // issued after it), so P and O are free
+        if (n > 0 && !wait_bar(bar(kPVDone + w), (n - 1) & 1, abort, p.status)) { ok = false; break; }
+        tc_fence_after();
+
+        // causal edge (or a padding row): keys c > lim are masked
+        const bool masked = tok0 + kTileN - 1 > u.pos0 || !row_ok;
+        const int lim = row_ok ? my_pos - tok0 : -1;
+        const float mul = masked ? 1.f : sl2;  // turns what load_half leaves into base-2 logits
+        // 64 keys of the S row -> registers; returns their maximum base-2 logit
+        auto load_half = [&](int h, uint32_t* sr) {
+          PA_TMEM_LD32(tmem_s + h * 64, sr);
+          PA_TMEM_LD32(tmem_s + h * 64 + 32, (sr + 32));
           tmem_wait_ld();
+          float m4[4];
+          if (masked) {
 #pragma unroll
-          for (int j = 0; j < 32; ++j) o[j] = __float_as_uint(__uint_as_float(o[j]) * factor);
-          PA_TMEM_ST32(tmem_o + lane_off + c0, o);
+            for (int e = 0; e < 4; ++e) m4[e] = -CUDART_INF_F;
+#pragma unroll
+            for (int c = 0; c < 64; ++c) {
+              const float x = h * 64 + c <= lim ? __uint_as_float(sr[c]) * sl2 : -CUDART_INF_F;
+              sr[c] = __float_as_uint(x);
+              m4[c & 3] = fmaxf(m4[c & 3], x);
+            }
+            return fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3]));
+          }
+#pragma unroll
+          for (int e = 0; e < 4; ++e) m4[e] = __uint_as_float(sr[e]);
+          if (sl2 >= 0.f) {
+#pragma unroll
+            for (int c = 4; c < 64; ++c) m4[c & 3] = fmaxf(m4[c & 3], __uint_as_float(sr[c]));
+            return fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3])) * sl2;
+          }
+#pragma unroll
+          for (int c = 4; c < 64; ++c) m4[c & 3] = fminf(m4[c & 3], __uint_as_float(sr[c]));
+          return fminf(fminf(m4[0], m4[1]), fminf(m4[2], m4[3])) * sl2;
+        };
+        // P = exp2(logit - m) as bf16 for 64 keys, stored 8 keys (16 bytes) at a time
+        auto emit_half = [&](int h, const uint32_t* sr, float m_sub) {
+          float ps4[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+          for (int c = 0; c < 8; ++c) {
+            uint32_t pw[4];
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+              const float p0 = ex2(fmaf(__uint_as_float(sr[8 * c + 2 * e]), mul, -m_sub));
+              const float p1 = ex2(fmaf(__uint_as_float(sr[8 * c + 2 * e + 1]), mul, -m_sub));
+              ps4[e] += p0 + p1;
+              pw[e] = pack_bf16(p0, p1);
+            }
+            asm volatile("st.shared.v4.b32 [%0], {%1,%2,%3,%4};\n" ::"r"(pbuf + sw128(i, h * 8 + c)),
+                         "r"(pw[0]), "r"(pw[1]), "r"(pw[2]), "r"(pw[3])
+                         : "memory");
+          }
+          return (ps4[0] + ps4[1]) + (ps4[2] + ps4[3]);
+        };
+        float factor = 1.f;  // this tile's rescale of the row's earlier state
+        bool moved_late = false;
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+          uint32_t sr[64];
+          const float mx = load_half(h, sr);
+          if (mx > m_used + kRescaleThreshold) {
+            const float f = ex2(m_used - mx);  // 0 while the row had no visible key
+            l_sum *= f;
+            factor *= f;
+            moved_late = h == 1 && f > 0.f;  // half 0's P used the old maximum
+            m_used = mx;
+          }
+          l_sum += emit_half(h, sr, m_used == -CUDART_INF_F ? 0.f : m_used);
         }
-        tmem_wait_st();
-      }
-      // P = exp2(x - m_used) as bf16, K-major rows of 128 keys, into P buffer j%2
-      float ps4[4] = {0.f, 0.f, 0.f, 0.f};
-      const uint32_t prow = sbase + C::kPOff + buf * C::kPBytes;
-#pragma unroll
-      for (int c = 0; c < kTileN / 8; ++c) {
-        uint32_t w[4];
-#pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          const float p0 = exp2f(__uint_as_float(sr[c * 8 + 2 * e]) - m_used);
-          const float p1 = exp2f(__uint_as_float(sr[c * 8 + 2 * e + 1]) - m_used);
-          ps4[e] += p0 + p1;
-          asm("cvt.rn.bf16x2.f32 %0, %1, %2;\n" : "=r"(w[e]) : "f"(p1), "f"(p0));
+        if (__any_sync(0xffffffffu, moved_late)) {
+          // rare: redo half 0's P with the new maximum (its sum is already rescaled)
+          uint32_t sr[64];
+          load_half(0, sr);
+          emit_half(0, sr, m_used == -CUDART_INF_F ? 0.f : m_used);
         }
-        asm volatile("st.shared.v4.b32 [%0], {%1,%2,%3,%4};\n" ::"r"(prow + sw128(tid, c)),
-                     "r"(w[0]), "r"(w[1]), "r"(w[2]), "r"(w[3])
-                     : "memory");
+
+        // rescale O rows whose maximum moved (not on the group's first tile of
+        // the unit: its PV overwrites O)
+        if (t >= 2 && __any_sync(0xffffffffu, factor != 1.f)) {
+          const uint32_t tmem_o = w ? tmem_o1 : tmem_o0;
+#pragma unroll
+          for (int c0 = 0; c0 < D; c0 += 32) {
+            uint32_t o[32];
+            PA_TMEM_LD32(tmem_o + c0, o);
+            tmem_wait_ld();
+#pragma unroll
+            for (int j = 0; j < 32; ++j) o[j] = __float_as_uint(__uint_as_float(o[j]) * factor);
+            PA_TMEM_ST32(tmem_o + c0, o);
+          }
+          tmem_wait_st();
+        }
+        // last tile: V rows past the last key (unwritten slots of the final
+        // block) are zeroed, so p = 0 never meets a NaN there
+        if (kt == u.n_kv - 1 && (u.kv_end & (kBlockSize - 1))) {
+          if (!wait_bar(bar(kVFull + w), n & 1, abort, p.status)) { ok = false; break; }
+          const int r0 = u.kv_end - tok0;
+          const int r1 = ((u.kv_end + kBlockSize - 1) & ~(kBlockSize - 1)) - tok0;
+          const int per_row = (D / 64) * 8;
+          const uint32_t vb = sbase + C::kVOff + w * C::kTileBytes;
+          for (int idx = i; idx < (r1 - r0) * per_row; idx += 128) {
+            const int row = r0 + idx / per_row, c = idx % per_row;
+            asm volatile("st.shared.v4.b32 [%0], {%1,%1,%1,%1};\n" ::"r"(
+                             vb + (c >> 3) * C::kRegionBytes + row * 128 + (c & 7) * 16),
+                         "r"(0u)
+                         : "memory");
+          }
+        }
+        fence_proxy_async_smem();
+        tc_fence_before();
+        warp_arrive(bar(kSEmpty + w));
+        warp_arrive(bar(kPFull + w));
       }
-      l_sum += (ps4[0] + ps4[1]) + (ps4[2] + ps4[3]);
-      fence_proxy_async_smem();
+      if (!ok) break;
+
+      // ---- merge the two groups' (m, l, O) and write this group's half of the columns
+      const int n_mine = (u.n_kv + 1 - w) / 2;
+      if (n_mine > 0 && !wait_bar(bar(kPVDone + w), (n - 1) & 1, abort, p.status)) break;
+      tc_fence_after();
+      float* ml_mine = reinterpret_cast<float*>(smem + C::kPOff + w * C::kPBytes);
+      const float* ml_other = reinterpret_cast<const float*>(smem + C::kPOff + (w ^ 1) * C::kPBytes);
+      ml_mine[2 * i] = m_used;
+      ml_mine[2 * i + 1] = l_sum;
+      warp_arrive(bar(kMlFull));
+      if (!wait_bar(bar(kMlFull), uc & 1, abort, p.status)) break;
+      const float m_o = ml_other[2 * i], l_o = ml_other[2 * i + 1];
+      warp_arrive(bar(kMlRead));
+      const float m0 = w ? m_o : m_used, l0 = w ? l_o : l_sum;
+      const float m1 = w ? m_used : m_o, l1 = w ? l_sum : l_o;
+      const float m = fmaxf(m0, m1);
+      const float f0 = m0 == -CUDART_INF_F ? 0.f : ex2(m0 - m);
+      const float f1 = m1 == -CUDART_INF_F ? 0.f : ex2(m1 - m);
+      const float inv = p.out_scale / (l0 * f0 + l1 * f1);
+      const bool has1 = u.n_kv > 1;  // group 1 had a tile: O1 holds this unit's data
+      tc_fence_after();
+      const long long tok = u.a + u.j0 + jj;
+      __nv_bfloat16* orow = out + (tok * Hq + u.g * G + (i - jj * G)) * D;
+#pragma unroll
+      for (int c0 = w * (D / 2); c0 < (w + 1) * (D / 2); c0 += 32) {
+        uint32_t o0[32], o1[32];
+        PA_TMEM_LD32(tmem_o0 + c0, o0);
+        if (has1) PA_TMEM_LD32(tmem_o1 + c0, o1);
+        tmem_wait_ld();
+        if (row_ok) {
+          uint4* dst = reinterpret_cast<uint4*>(orow + c0);
+#pragma unroll
+          for (int j = 0; j < 4; ++j) {
+            float v[8];
+#pragma unroll
+            for (int e = 0; e < 8; ++e) {
+              const float a0 = __uint_as_float(o0[8 * j + e]) * f0;
+              v[e] = (has1 ? fmaf(__uint_as_float(o1[8 * j + e]), f1, a0) : a0) * inv;
+            }
+            dst[j] = make_uint4(pack_bf16(v[0], v[1]), pack_bf16(v[2], v[3]),
+                                pack_bf16(v[4], v[5]), pack_bf16(v[6], v[7]));
+          }
+        }
+      }
       tc_fence_before();
-      __syncthreads();
-      tc_fence_after();
-      if (tid == 0) {
-        const uint32_t pa = sbase + C::kPOff + buf * C::kPBytes;
-        const uint32_t vb = sbase + C::kVOff + buf * C::kTileBytes;
-#pragma unroll
-        for (int kk = 0; kk < kTileN / 16; ++kk) {
-          tc_mma_f16(tmem_o, smem_desc_sw128(pa + (kk >> 2) * (kTileM * 128) + (kk & 3) * 32, 16, 1024),
-                     smem_desc_sw128(vb + kk * 2048, kTileM * 128, 1024), idesc_bf16(kTileM, D, 1),
-                     (kt > 0 || kk > 0) ? 1u : 0u);
-        }
-        tc_commit(smem_u32(&mbar[1]));
-      }
+      warp_arrive(bar(kOFree));
+      // nobody writes P (where the (m, l) pairs sit) before both groups read them
+      if (!wait_bar(bar(kMlRead), uc & 1, abort, p.status)) break;
     }
-    if (!aborted) {  // the last PV
-      const bool ok_o = mbar_wait(smem_u32(&mbar[1]), ph_o, kWaitLimit);
-      ph_o ^= 1;
-      if (__syncthreads_or(!ok_o)) aborted = true;
-      tc_fence_after();
-    }
-    if (aborted) break;
-
-    // ---- O / l -> out
-#pragma unroll
-    for (int c0 = 0; c0 < D; c0 += 32) {
-      uint32_t o[32];
-      PA_TMEM_LD32(tmem_o + lane_off + c0, o);
-      tmem_wait_ld();
-      if (row_ok) {
-        const float inv = 1.f / l_sum;
-        const long long tok = u.a + u.j0 + my_jj;
-        uint4* dst = reinterpret_cast<uint4*>(out + (tok * Hq + u.g * G + (tid - my_jj * G)) * D + c0);
-#pragma unroll
-        for (int j = 0; j < 4; ++j) {
-          uint4 v;
-          asm("cvt.rn.bf16x2.f32 %0, %1, %2;\n" : "=r"(v.x) : "f"(__uint_as_float(o[8 * j + 1]) * inv), "f"(__uint_as_float(o[8 * j]) * inv));
-          asm("cvt.rn.bf16x2.f32 %0, %1, %2;\n" : "=r"(v.y) : "f"(__uint_as_float(o[8 * j + 3]) * inv), "f"(__uint_as_float(o[8 * j + 2]) * inv));
-          asm("cvt.rn.bf16x2.f32 %0, %1, %2;\n" : "=r"(v.z) : "f"(__uint_as_float(o[8 * j + 5]) * inv), "f"(__uint_as_float(o[8 * j + 4]) * inv));
-          asm("cvt.rn.bf16x2.f32 %0, %1, %2;\n" : "=r"(v.w) : "f"(__uint_as_float(o[8 * j + 7]) * inv), "f"(__uint_as_float(o[8 * j + 6]) * inv));
-          dst[j] = v;
-        }
-      }
-    }
-    tc_fence_before();
-    __syncthreads();
-    tc_fence_after();
   }
 
-  cp_async_wait<0>();
-  if (aborted) {
-    if (tid == 0) {
-      flag_error(p.status, PA_DEV_TIMEOUT);
-      tc_commit(smem_u32(&mbar[2]));  // completes once every MMA issued so far is done
-    }
-    mbar_wait(smem_u32(&mbar[2]), 0, kWaitLimit);
-  }
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
@@ -371,28 +599,70 @@ __global__ void __launch_bounds__(kPfThreads, 1) prefill_tc_kernel(const AttnPar
 }
 
 namespace {
+
+PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* f = nullptr;
+    cudaDriverEntryPointQueryResult q = cudaDriverEntryPointSymbolNotFound;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(f);
+  });
+  return fn;
+}
+
+// bf16 tensor map with 128-byte swizzle and zero fill out of bounds.
+bool encode_map(CUtensorMap* m, const void* base, int rank, const cuuint64_t* dims,
+                const cuuint64_t* strides_bytes, const cuuint32_t* box) {
+  const auto enc = tensor_map_encoder();
+  if (!enc) return false;
+  const cuuint32_t estride[4] = {1, 1, 1, 1};
+  return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, static_cast<cuuint32_t>(rank),
+             const_cast<void*>(base), dims, strides_bytes, box, estride,
+             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) ==
+         CUDA_SUCCESS;
+}
+
 template <int D, int G>
 cudaError_t launch_pf(const AttnParams& p, int num_sms, cudaStream_t stream) {
   using C = PfCfg<D>;
-  static int ctas_per_sm[64] = {0};
+  static bool configured[64] = {false};
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
-  if (ctas_per_sm[dev] == 0) {
+  if (!configured[dev]) {
     e = cudaFuncSetAttribute(prefill_tc_kernel<D, G>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              C::kSmemBytes);
     if (e != cudaSuccess) return e;
-    int n = 0;
-    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, prefill_tc_kernel<D, G>, kPfThreads,
-                                                      C::kSmemBytes);
-    if (e != cudaSuccess) return e;
-    // each CTA holds 256 TMEM columns; two CTAs fill an SM's 512
-    ctas_per_sm[dev] = n < 1 ? 1 : (n > 2 ? 2 : n);
+    configured[dev] = true;
   }
-  prefill_tc_kernel<D, G><<<num_sms * ctas_per_sm[dev], kPfThreads, C::kSmemBytes, stream>>>(p);
+  PfMaps maps;
+  const cuuint64_t e2 = 2;
+  {
+    const cuuint64_t dims[3] = {static_cast<cuuint64_t>(D), static_cast<cuuint64_t>(p.num_q_heads),
+                                static_cast<cuuint64_t>(p.num_tokens)};
+    const cuuint64_t strides[2] = {D * e2, static_cast<cuuint64_t>(p.num_q_heads) * D * e2};
+    const cuuint32_t box[3] = {64, static_cast<cuuint32_t>(G), static_cast<cuuint32_t>(kTileM / G)};
+    if (!encode_map(&maps.q, p.q, 3, dims, strides, box)) return cudaErrorInvalidValue;
+  }
+  {
+    const cuuint64_t hkv = static_cast<cuuint64_t>(p.num_kv_heads);
+    const cuuint64_t dims[4] = {static_cast<cuuint64_t>(D), hkv, static_cast<cuuint64_t>(kBlockSize),
+                                static_cast<cuuint64_t>(p.num_blocks)};
+    const cuuint64_t strides[3] = {D * e2, hkv * D * e2, kBlockSize * hkv * D * e2};
+    const cuuint32_t box[4] = {64, 1, static_cast<cuuint32_t>(kBlockSize), 1};
+    if (!encode_map(&maps.k, p.k_cache, 4, dims, strides, box)) return cudaErrorInvalidValue;
+    if (!encode_map(&maps.v, p.v_cache, 4, dims, strides, box)) return cudaErrorInvalidValue;
+  }
+  prefill_tc_kernel<D, G><<<num_sms, kPfThreads, C::kSmemBytes, stream>>>(p, maps);
   return cudaGetLastError();
 }
+
 }  // namespace
 
 cudaError_t launch_prefill_tc(const AttnParams& p, int head_size, int group, int num_sms,

@@ -125,3 +125,17 @@ def test_missing_library_fails_loudly(monkeypatch, tmp_path):
     monkeypatch.setattr(binding, "_lib", None)
     with pytest.raises(RuntimeError, match="missing"):
         binding.lib()
+
+
+def test_binding_rejects_host_tensors():
+    """A host tensor is refused before any call into the library."""
+    import torch
+    lay = P.make_layout(8, 2, 64, 4, torch.bfloat16)
+    kc = torch.zeros(4, 16, 2, 64, dtype=torch.bfloat16)
+    e = torch.zeros(1, 2, 64, dtype=torch.bfloat16)
+    with pytest.raises(P.PaError, match="not a CUDA tensor"):
+        P.pa_cache_write(e, e, torch.zeros(1, dtype=torch.int64), kc, kc, lay)
+    with pytest.raises(P.PaError, match="not a CUDA tensor"):
+        P.pa_forward(e, kc, kc, torch.zeros(1, 1, dtype=torch.int32),
+                     torch.ones(1, dtype=torch.int32), torch.tensor([0, 1], dtype=torch.int32),
+                     1, 1, 0.125, e, torch.zeros(16, dtype=torch.uint8), lay)
