@@ -35,6 +35,7 @@ METRIC = "decode paged-attn HBM GB/s & % of GB300 peak; mixed-step tokens/s per 
 HEADLINE = "llama3_8b_decode"
 MIXED = "mixed_step"
 FALLBACK_HBM_GBS = 6800.0
+FALLBACK_BF16_TFLOPS = 1900.0
 WORKLOAD_TEXT = {
     "llama3_8b_decode": "Llama-3-8B single-layer decode: batch 256, 32 q / 8 kv heads, head_size 128, "
                         "bf16, context lognormal(median 1024, sigma 0.8, cap 8192), block_size 16, "
@@ -99,6 +100,16 @@ def measured_peaks() -> tuple[float, str]:
             return float(json.load(f)["hbm_gbs"]), "measured"
     except Exception:
         return FALLBACK_HBM_GBS, "fallback"
+
+
+def measured_bf16_tflops() -> tuple[float, str]:
+    """Dense bf16 peak (burst) from MEASURED_PEAKS.json, else the fallback."""
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            return float(json.load(f)["bf16_tflops"]), "measured"
+    except Exception:
+        return FALLBACK_BF16_TFLOPS, "fallback"
 
 
 def kernel_source_hash() -> str:
@@ -328,7 +339,8 @@ def barrier(world: int):
 class StepRunner:
     """Device-resident step of one workload through the C ABI."""
 
-    def __init__(self, name: str, seed_offset: int = 0, fp8_scales: tuple | None = None):
+    def __init__(self, name: str, seed_offset: int = 0, fp8_scales: tuple | None = None,
+                 requests: slice | None = None):
         import torch
 
         import paged_kv_attention_04_gb300 as P
@@ -338,6 +350,11 @@ class StepRunner:
         spec = fn()
         if seed_offset:
             spec.seed += seed_offset
+        if requests is not None:  # a subset of the workload's requests
+            spec.seq_lens = spec.seq_lens[requests]
+            spec.q_lens = spec.q_lens[requests]
+            if spec.sharing is not None:
+                spec.sharing = spec.sharing[requests]
         self.spec = spec
         self.meta = W.make_meta(spec)
         self.st = W.make_step(spec, device="cuda")
@@ -538,6 +555,29 @@ def run_gpu_arm(args):
     del mixed
     torch.cuda.empty_cache()
 
+    # the mixed step's two prefill chunks alone: the tensor-core kernel's own rate
+    pf = StepRunner(MIXED, seed_offset=rank * 1000 if world > 1 else 0, requests=slice(-2, None))
+    pms, _ = pf.time_device(max(3, args.steps // 2), args.warmup, world, flush=True)
+    pms = dist_max(pms, world)
+    bf16_peak = measured_bf16_tflops()
+    pf_tflops = pf.work["chunk_flops"] / (pms * 1e-3) / 1e12
+    prefill_info = {
+        "workload": "the mixed step's two chunked prefills alone: 512 tokens at prior 0 and "
+                    "512 at prior 1536, Llama-3-8B heads, bf16",
+        "ms_per_step": pms,
+        "tflops": pf_tflops,
+        "frac_of_bf16_peak": pf_tflops / bf16_peak[0] if bf16_peak[0] else None,
+        "peak_tflops": bf16_peak[0], "peak_source": bf16_peak[1],
+        "flops": pf.work["chunk_flops"],
+        "timed": "pa_cache_write + pa_forward (plan, tensor-core prefill kernel); L2 flushed "
+                 "(256 MiB write) before every step, outside the timed events; flops = 4 x D x "
+                 "Hq x visible (query, key) pairs",
+    }
+    if int(pf.status.item()) != 0:
+        raise RuntimeError(f"prefill step device status {int(pf.status.item())}")
+    del pf
+    torch.cuda.empty_cache()
+
     # the headline shape over an 8-bit (E4M3) KV cache: half the KV bytes per token
     f8 = StepRunner(HEADLINE, seed_offset=rank * 1000 if world > 1 else 0, fp8_scales=(0.01, 0.01))
     fms, fdec = f8.time_device(args.steps, args.warmup, world)
@@ -590,6 +630,7 @@ def run_gpu_arm(args):
         "gpu_launches": launches,
         "clocks": clock_info,
         "mixed": mixed_info,
+        "prefill_chunks": prefill_info,
         "tinyllama_decode": small_info,
         "fp8_kv": fp8_info,
     }
