@@ -61,6 +61,8 @@ struct PfCfg {
   static constexpr int kQOff = 0;
   static constexpr int kKOff = kQOff + kTileBytes;      // K0, K1
   static constexpr int kVOff = kKOff + 2 * kTileBytes;  // V0, V1
+  // a V tile is stored per 16-token block: [block][64-column half][16 rows][128 B]
+  static constexpr int kVBlockBytes = kBlockSize * 128 * (D / 64);
   static constexpr int kPOff = kVOff + 2 * kTileBytes;  // P0, P1
   static constexpr int kSmemBytes = kPOff + 2 * kPBytes + 1024;  // + alignment slack
   static constexpr int kTmemCols = 512;  // S0, S1 at 0 / 128; O0, O1 at 256 / 384
@@ -102,7 +104,7 @@ __device__ __forceinline__ int tile_of(const UnitInfo& u, int s) {
 struct PfMaps {
   CUtensorMap q;  // q [T][Hq][D] as 3-D (D, Hq, T), box (64, G, 128/G)
   CUtensorMap k;  // k_cache [NB][16][Hkv][D] as 4-D (D, Hkv, 16, NB), box (64, 1, 16, 1)
-  CUtensorMap v;
+  CUtensorMap v;  // v_cache as 5-D (64, 16 rows, D/64 halves, Hkv, NB), box (64, 16, D/64, 1, 1)
 };
 
 // Byte offset of 16-byte chunk c of row r in a 128-byte-swizzled tile whose
@@ -201,9 +203,12 @@ __global__ void __launch_bounds__(kPfThreads, 1)
     return -1;
   };
   // TMA copy of KV tile t of unit u into the swizzled buffer at dst: lane
-  // b < 8 copies block b (one box per 64 columns); a block past the unit's
-  // keys or with a bad table entry is read at index num_blocks (zeros).
-  auto copy_kv_tile = [&](const UnitInfo& u, int t, int ph, const CUtensorMap* map, uint32_t dst,
+  // b < 8 copies block b; a block past the unit's keys or with a bad table
+  // entry is read at index num_blocks (zeros).  K tiles take one box per 64
+  // columns (rows of a K tile are the N dimension of S = Q K^T and must sit
+  // 128 bytes apart); V tiles take one box per block (both halves), half the
+  // boxes, laid out [block][half][row] for the MN-major PV operand.
+  auto copy_kv_tile = [&](const UnitInfo& u, int t, int ph, bool is_v, uint32_t dst,
                           uint32_t full) {
     if (lane < kTileN / kBlockSize && ph != -1 && (ph < 0 || ph >= p.num_blocks)) {
       flag_error(p.status, PA_DEV_BLOCK_RANGE);
@@ -213,10 +218,14 @@ __global__ void __launch_bounds__(kPfThreads, 1)
     __syncwarp();
     if (lane < kTileN / kBlockSize) {
       const int coord = ph < 0 ? p.num_blocks : ph;
+      if (is_v) {
+        tma_load_5d(dst + lane * C::kVBlockBytes, &maps.v, 0, 0, 0, u.g, coord, full);
+      } else {
 #pragma unroll
-      for (int h = 0; h < D / 64; ++h)
-        tma_load_4d(dst + h * C::kRegionBytes + lane * (kBlockSize * 128), map, h * 64, u.g, 0,
-                    coord, full);
+        for (int h = 0; h < D / 64; ++h)
+          tma_load_4d(dst + h * C::kRegionBytes + lane * (kBlockSize * 128), &maps.k, h * 64, u.g,
+                      0, coord, full);
+      }
     }
   };
 
@@ -276,7 +285,7 @@ __global__ void __launch_bounds__(kPfThreads, 1)
           ok = false;
           break;
         }
-        copy_kv_tile(u, tile_of(u, sq), ph, &maps.k, sbase + C::kKOff + w * C::kTileBytes,
+        copy_kv_tile(u, tile_of(u, sq), ph, false, sbase + C::kKOff + w * C::kTileBytes,
                      bar(kKFull + w));
         ++nk[w];
         if (sq + 1 < u.n_kv) ph = tile_phys(u, tile_of(u, sq + 1));
@@ -307,7 +316,7 @@ __global__ void __launch_bounds__(kPfThreads, 1)
           ok = false;
           break;
         }
-        copy_kv_tile(u, tile_of(u, sq), ph, &maps.v, sbase + C::kVOff + w * C::kTileBytes,
+        copy_kv_tile(u, tile_of(u, sq), ph, true, sbase + C::kVOff + w * C::kTileBytes,
                      bar(kVFull + w));
         ++nv[w];
         if (sq + 1 < u.n_kv) ph = tile_phys(u, tile_of(u, sq + 1));
@@ -368,7 +377,7 @@ __global__ void __launch_bounds__(kPfThreads, 1)
           for (int kk = 0; kk < kTileN / 16; ++kk)
             tc_mma_f16(tmem + 256 + w * 128,
                        smem_desc_sw128(pa + (kk >> 2) * C::kRegionBytes + (kk & 3) * 32, 16, 1024),
-                       smem_desc_sw128(vb + kk * 2048, C::kRegionBytes, 1024),
+                       smem_desc_sw128(vb + kk * C::kVBlockBytes, kBlockSize * 128, 1024),
                        idesc_bf16(kTileM, D, 1), (t >= 2 || kk > 0) ? 1u : 0u);
           tc_commit(bar(kPVDone + w));
         }
@@ -530,7 +539,8 @@ __global__ void __launch_bounds__(kPfThreads, 1)
           for (int idx = i; idx < (r1 - r0) * per_row; idx += 128) {
             const int row = r0 + idx / per_row, c = idx % per_row;
             asm volatile("st.shared.v4.b32 [%0], {%1,%1,%1,%1};\n" ::"r"(
-                             vb + (c >> 3) * C::kRegionBytes + row * 128 + (c & 7) * 16),
+                             vb + (row >> 4) * C::kVBlockBytes + (c >> 3) * (kBlockSize * 128) +
+                             (row & 15) * 128 + (c & 7) * 16),
                          "r"(0u)
                          : "memory");
           }
@@ -619,7 +629,7 @@ bool encode_map(CUtensorMap* m, const void* base, int rank, const cuuint64_t* di
                 const cuuint64_t* strides_bytes, const cuuint32_t* box) {
   const auto enc = tensor_map_encoder();
   if (!enc) return false;
-  const cuuint32_t estride[4] = {1, 1, 1, 1};
+  const cuuint32_t estride[5] = {1, 1, 1, 1, 1};
   return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, static_cast<cuuint32_t>(rank),
              const_cast<void*>(base), dims, strides_bytes, box, estride,
              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
@@ -657,7 +667,15 @@ cudaError_t launch_pf(const AttnParams& p, int num_sms, cudaStream_t stream) {
     const cuuint64_t strides[3] = {D * e2, hkv * D * e2, kBlockSize * hkv * D * e2};
     const cuuint32_t box[4] = {64, 1, static_cast<cuuint32_t>(kBlockSize), 1};
     if (!encode_map(&maps.k, p.k_cache, 4, dims, strides, box)) return cudaErrorInvalidValue;
-    if (!encode_map(&maps.v, p.v_cache, 4, dims, strides, box)) return cudaErrorInvalidValue;
+    // V: (64 columns, 16 rows, D/64 halves, kv head, block); the halves
+    // dimension's stride (128 B) is below the rows' (Hkv x D x 2 B)
+    const cuuint64_t vdims[5] = {64, static_cast<cuuint64_t>(kBlockSize),
+                                 static_cast<cuuint64_t>(D / 64), hkv,
+                                 static_cast<cuuint64_t>(p.num_blocks)};
+    const cuuint64_t vstrides[4] = {hkv * D * e2, 128, D * e2, kBlockSize * hkv * D * e2};
+    const cuuint32_t vbox[5] = {64, static_cast<cuuint32_t>(kBlockSize),
+                                static_cast<cuuint32_t>(D / 64), 1, 1};
+    if (!encode_map(&maps.v, p.v_cache, 5, vdims, vstrides, vbox)) return cudaErrorInvalidValue;
   }
   prefill_tc_kernel<D, G><<<num_sms, kPfThreads, C::kSmemBytes, stream>>>(p, maps);
   return cudaGetLastError();
