@@ -43,6 +43,12 @@
 #define PA_QK_SPLIT_ACC 0  // 1: two accumulator sets per score tile (shorter MMA chains)
 #endif
 
+// Prefetch each warp's next KV block into L2 while the cp.async ring streams
+// the current one (1) or not (0).
+#ifndef PA_L2_PREFETCH
+#define PA_L2_PREFETCH 1
+#endif
+
 namespace pa {
 
 struct UnitMeta {
@@ -320,6 +326,22 @@ __global__ void __launch_bounds__(MmaCfg<D, G, P, NW, NS, F8>::kThreads,
     cp_async_commit();
     ++issued;
     ++iss_i;
+    // Start the warp's next block of this unit towards L2 as well: one row per
+    // lane (lanes 0-15 K, 16-31 V).  With the cp.async ring this keeps two
+    // blocks per warp in flight from HBM without more shared memory (measured
+    // on head size 128: +5.5 % decode bandwidth; head size 64 lost 8 %).
+    if (PA_L2_PREFETCH && D == 128 && iss_i < share(m)) {
+      const int nphys = m.bt[warp + iss_i * NW];
+      if (nphys >= 0 && nphys < p.num_blocks) {
+        const int t = lane & (kBlockSize - 1);
+        const unsigned char* src = (lane < kBlockSize ? kc : vc) +
+                                   static_cast<long long>(nphys) * kBlockSize * row_stride +
+                                   static_cast<long long>(m.g) * C::kCacheRowBytes + t * row_stride;
+#pragma unroll
+        for (int l = 0; l < (C::kCacheRowBytes + 127) / 128; ++l)
+          asm volatile("prefetch.global.L2 [%0];\n" ::"l"(src + l * 128));
+      }
+    }
     return true;
   };
   auto wait_for = [&](int idx) {  // block `idx` of the stream has landed
