@@ -113,6 +113,32 @@ __device__ __forceinline__ uint32_t sw128(int r, int c) {
   return static_cast<uint32_t>((c >> 3) * (kTileM * 128) + r * 128 + (((c & 7) ^ (r & 7)) << 4));
 }
 
+// max of three floats in one instruction (NaN-free operands here)
+__device__ __forceinline__ float max3(float a, float b, float c) {
+  float r;
+  asm("max.f32 %0, %1, %2, %3;\n" : "=f"(r) : "f"(a), "f"(b), "f"(c));
+  return r;
+}
+__device__ __forceinline__ float min3(float a, float b, float c) {
+  float r;
+  asm("min.f32 %0, %1, %2, %3;\n" : "=f"(r) : "f"(a), "f"(b), "f"(c));
+  return r;
+}
+// (d0, d1) = (a0, a1) * b + c, one packed instruction for two lanes of work
+__device__ __forceinline__ void fma2(float& d0, float& d1, float a0, float a1, float b, float c) {
+  asm("{\n .reg .b64 ra, rb, rc, rd;\n mov.b64 ra, {%2, %3};\n mov.b64 rb, {%4, %4};\n"
+      " mov.b64 rc, {%5, %5};\n fma.rn.f32x2 rd, ra, rb, rc;\n mov.b64 {%0, %1}, rd;\n}\n"
+      : "=f"(d0), "=f"(d1)
+      : "f"(a0), "f"(a1), "f"(b), "f"(c));
+}
+// (d0, d1) += (a0, a1)
+__device__ __forceinline__ void add2(float& d0, float& d1, float a0, float a1) {
+  asm("{\n .reg .b64 ra, rd;\n mov.b64 ra, {%2, %3};\n mov.b64 rd, {%0, %1};\n"
+      " add.rn.f32x2 rd, rd, ra;\n mov.b64 {%0, %1}, rd;\n}\n"
+      : "+f"(d0), "+f"(d1)
+      : "f"(a0), "f"(a1));
+}
+
 __device__ __forceinline__ float ex2(float x) {
   float y;
   asm("ex2.approx.ftz.f32 %0, %1;\n" : "=f"(y) : "f"(x));
@@ -465,24 +491,28 @@ __global__ void __launch_bounds__(kPfThreads, 1)
           for (int e = 0; e < 4; ++e) m4[e] = __uint_as_float(sr[e]);
           if (sl2 >= 0.f) {
 #pragma unroll
-            for (int c = 4; c < 64; ++c) m4[c & 3] = fmaxf(m4[c & 3], __uint_as_float(sr[c]));
+            for (int c = 4; c < 64; c += 2)
+              m4[(c >> 1) & 3] = max3(m4[(c >> 1) & 3], __uint_as_float(sr[c]), __uint_as_float(sr[c + 1]));
             return fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3])) * sl2;
           }
 #pragma unroll
-          for (int c = 4; c < 64; ++c) m4[c & 3] = fminf(m4[c & 3], __uint_as_float(sr[c]));
+          for (int c = 4; c < 64; c += 2)
+            m4[(c >> 1) & 3] = min3(m4[(c >> 1) & 3], __uint_as_float(sr[c]), __uint_as_float(sr[c + 1]));
           return fminf(fminf(m4[0], m4[1]), fminf(m4[2], m4[3])) * sl2;
         };
         // P = exp2(logit - m) as bf16 for 64 keys, stored 8 keys (16 bytes) at a time
         auto emit_half = [&](int h, const uint32_t* sr, float m_sub) {
-          float ps4[4] = {0.f, 0.f, 0.f, 0.f};
+          float ps4[4] = {0.f, 0.f, 0.f, 0.f};  // two packed pair sums
 #pragma unroll
           for (int c = 0; c < 8; ++c) {
             uint32_t pw[4];
 #pragma unroll
             for (int e = 0; e < 4; ++e) {
-              const float p0 = ex2(fmaf(__uint_as_float(sr[8 * c + 2 * e]), mul, -m_sub));
-              const float p1 = ex2(fmaf(__uint_as_float(sr[8 * c + 2 * e + 1]), mul, -m_sub));
-              ps4[e] += p0 + p1;
+              float x0, x1;
+              fma2(x0, x1, __uint_as_float(sr[8 * c + 2 * e]), __uint_as_float(sr[8 * c + 2 * e + 1]),
+                   mul, -m_sub);
+              const float p0 = ex2(x0), p1 = ex2(x1);
+              add2(ps4[2 * (e & 1)], ps4[2 * (e & 1) + 1], p0, p1);
               pw[e] = pack_bf16(p0, p1);
             }
             asm volatile("st.shared.v4.b32 [%0], {%1,%2,%3,%4};\n" ::"r"(pbuf + sw128(i, h * 8 + c)),
