@@ -196,3 +196,40 @@ def test_prefill_shapes(case):
     dtype, D, G, q_lens, seq_lens = PREFILL_SHAPES[case]
     spec = W.custom_spec(f"prefill-{case}", dtype, 2 * G, 2, D, q_lens, seq_lens, seed=200 + case)
     _full_parity(W.make_step(spec))
+
+
+def _rising_logits(step, slope_log2: float, qmag: float = 8.0, seed: int = 5):
+    """Make every row's logits grow along the key positions: keys of position
+    p are u * c * p and query rows u * qmag for one unit vector u, so the base-2
+    logit of key p is slope_log2 * p.  The running maximum then moves by more
+    than the kernels' lazy-rescale threshold within 64 keys, which drives the
+    rescale paths."""
+    import math
+    spec = step.spec
+    D = spec.head_size
+    u = torch.randn(D, generator=torch.Generator().manual_seed(seed))
+    u = u / u.norm()
+    c = slope_log2 / (step.scale * math.log2(math.e) * qmag)
+    dt = step.q.dtype
+    step.q[:] = (u * qmag).to(dt)
+    bt = step.block_tables.numpy()
+    qsl = step.query_start_loc.numpy()
+    flat_k = step.k_cache.view(-1, spec.num_kv_heads, D)
+    for r in range(spec.num_seqs):
+        S, L = int(spec.seq_lens[r]), int(spec.q_lens[r])
+        for pos in range(S):
+            key = (u * (c * pos)).to(dt)
+            if pos < S - L:
+                slot = int(bt[r, pos // 16]) * 16 + pos % 16
+                flat_k[slot] = key
+            else:
+                step.k[int(qsl[r]) + pos - (S - L)] = key
+    return step
+
+
+def test_rescale_paths_rising_logits():
+    """Logits rising by 0.2 (base 2) per key: the prefill kernel's O rescale and
+    its second-half P fix-up, and the decode kernel's running-maximum updates,
+    all run; the result still matches the oracle."""
+    spec = W.custom_spec("rising", "bf16", 8, 2, 128, [300, 1], [1200, 700], seed=41)
+    _full_parity(_rising_logits(W.make_step(spec), slope_log2=0.2))
