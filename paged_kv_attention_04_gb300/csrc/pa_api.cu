@@ -169,12 +169,6 @@ WsLayout ws_layout(const Capacity& cap, int B, int Hkv, int D, int group) {
   const size_t rows_d = static_cast<size_t>(group);
   const size_t rows_s = static_cast<size_t>(kSmallRows);
   w.hdr = take(kHdrWords * sizeof(int));
-  w.req_class = take(sizeof(int) * B);
-  w.pfx_d_items = take(sizeof(int) * (B + 1));
-  w.pfx_d_tiles = take(sizeof(int) * (B + 1));
-  w.pfx_s_items = take(sizeof(int) * (B + 1));
-  w.pfx_s_tiles = take(sizeof(int) * (B + 1));
-  w.pfx_p_tiles = take(sizeof(int) * (B + 1));
   w.items_d = take(sizeof(int4) * cap.decode_items);
   w.tiles_d = take(sizeof(int4) * cap.decode_tiles);
   w.items_s = take(sizeof(int4) * cap.small_items);

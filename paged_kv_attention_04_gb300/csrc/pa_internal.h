@@ -35,7 +35,7 @@ struct Capacity {
 
 // Byte offsets of every workspace region (all 256-byte aligned).
 struct WsLayout {
-  size_t hdr, req_class, pfx_d_items, pfx_d_tiles, pfx_s_items, pfx_s_tiles, pfx_p_tiles;
+  size_t hdr;
   size_t items_d, tiles_d, items_s, tiles_s, tiles_p;
   size_t recs_d, recs_s;  // per item: 3 x int4 unit records (see UnitRec)
   size_t cnt_d, cnt_s;

@@ -80,16 +80,6 @@ __device__ __forceinline__ int splits_for(int pos_last, int bps) {
   return ceil_div(ceil_div(pos_last + 1, kBlockSize), bps);
 }
 
-// Largest r with pfx[r] <= i (pfx nondecreasing, pfx[0] = 0).
-__device__ int find_owner(const int* pfx, int n, int i) {
-  int lo = 0, hi = n - 1;
-  while (lo < hi) {
-    const int mid = (lo + hi + 1) >> 1;
-    if (pfx[mid] <= i) lo = mid; else hi = mid - 1;
-  }
-  return lo;
-}
-
 }  // namespace
 
 __global__ void __launch_bounds__(kPlanThreads, 1) plan_kernel(PlanParams p) {
@@ -99,12 +89,6 @@ __global__ void __launch_bounds__(kPlanThreads, 1) plan_kernel(PlanParams p) {
   const int B = p.num_seqs;
   char* ws = p.ws;
   int* hdr = reinterpret_cast<int*>(ws + p.lay.hdr);
-  int* cls = reinterpret_cast<int*>(ws + p.lay.req_class);
-  int* pfx_di = reinterpret_cast<int*>(ws + p.lay.pfx_d_items);
-  int* pfx_dt = reinterpret_cast<int*>(ws + p.lay.pfx_d_tiles);
-  int* pfx_si = reinterpret_cast<int*>(ws + p.lay.pfx_s_items);
-  int* pfx_st = reinterpret_cast<int*>(ws + p.lay.pfx_s_tiles);
-  int* pfx_pt = reinterpret_cast<int*>(ws + p.lay.pfx_p_tiles);
   int4* items_d = reinterpret_cast<int4*>(ws + p.lay.items_d);
   int4* tiles_d = reinterpret_cast<int4*>(ws + p.lay.tiles_d);
   int4* items_s = reinterpret_cast<int4*>(ws + p.lay.items_s);
@@ -113,6 +97,7 @@ __global__ void __launch_bounds__(kPlanThreads, 1) plan_kernel(PlanParams p) {
   UnitRec* recs_s = reinterpret_cast<UnitRec*>(ws + p.lay.recs_s);
   int* cnt_d = reinterpret_cast<int*>(ws + p.lay.cnt_d);
   int* cnt_s = reinterpret_cast<int*>(ws + p.lay.cnt_s);
+  int4* tiles_p = reinterpret_cast<int4*>(ws + p.lay.tiles_p);
 
   if (threadIdx.x == 0) {
     err = 0;
@@ -122,16 +107,20 @@ __global__ void __launch_bounds__(kPlanThreads, 1) plan_kernel(PlanParams p) {
   }
   __syncthreads();
 
-  // Pass 1: classify and count, with a running exclusive scan per list.
+  // One pass: classify and count, exclusive-scan the counts across the CTA,
+  // and let each request's thread write its own items and tiles at its
+  // offsets (every write checked against the list's capacity).
   int carry_r[kLists] = {0, 0, 0, 0, 0};
   for (int base = 0; base < B; base += kPlanThreads) {
     const int r = base + threadIdx.x;
     int c = kClassNone;
     int cnt[kLists] = {0, 0, 0, 0, 0};
+    int S = 0, a = 0, L = 0;
     if (r < B) {
-      const int S = __ldg(p.seq_lens + r);
-      const int a = __ldg(p.qsl + r), b = __ldg(p.qsl + r + 1);
-      const int L = b - a;
+      S = __ldg(p.seq_lens + r);
+      a = __ldg(p.qsl + r);
+      const int b = __ldg(p.qsl + r + 1);
+      L = b - a;
       int e = 0;
       if (L < 0 || a < 0 || b > p.num_tokens) e |= PA_DEV_QSL;
       else if (L < 1 || L > S || S > p.max_seq_len || L > p.max_query_len ||
@@ -155,14 +144,55 @@ __global__ void __launch_bounds__(kPlanThreads, 1) plan_kernel(PlanParams p) {
           cnt[2] += splits_for(S - L + last, rb);
         }
       }
-      cls[r] = c;
     }
-    int tot[kLists];
-    block_exclusive_scan(cnt, warp_sums, tot);
-    if (r < B) {
-      pfx_di[r] = carry_r[0] + cnt[0]; pfx_dt[r] = carry_r[1] + cnt[1];
-      pfx_si[r] = carry_r[2] + cnt[2]; pfx_st[r] = carry_r[3] + cnt[3];
-      pfx_pt[r] = carry_r[4] + cnt[4];
+    int off[kLists], tot[kLists];
+#pragma unroll
+    for (int k = 0; k < kLists; ++k) off[k] = cnt[k];
+    block_exclusive_scan(off, warp_sums, tot);
+#pragma unroll
+    for (int k = 0; k < kLists; ++k) off[k] += carry_r[k];
+    if (c == kClassDecode) {
+      // items off[0] .. off[0] + cnt[0] - 1: one split of the request each
+      const int tile = off[1];
+      const int nb = ceil_div(S, kBlockSize);
+      const int rb = request_bps(nb, p.bps);
+      const int ns = cnt[0];
+      if (tile < p.cap.decode_tiles) tiles_d[tile] = make_int4(off[0], ns, rb, 0);
+      for (int s = 0; s < ns; ++s) {
+        const int i = off[0] + s;
+        if (i >= p.cap.decode_items) break;
+        items_d[i] = make_int4(r, 0, s * rb, tile);
+        const int b0 = s * rb, b1 = min(b0 + rb, nb);
+        recs_d[i].a = make_int4(r, 0, b0, b1);
+        recs_d[i].b = make_int4(tile, off[0], ns, a);
+        recs_d[i].c = make_int4(1, S - 1, min(b1 * kBlockSize, S), 0);
+      }
+    } else if (c == kClassSmall) {
+      // tiles of small_positions positions, each expanded into its splits
+      const int rb = request_bps(ceil_div(S, kBlockSize), p.bps);
+      const int P = p.small_positions;
+      int first = off[2];
+      for (int m = 0; m < cnt[3]; ++m) {
+        const int tile = off[3] + m;
+        const int ns = splits_for(S - L + min(L, (m + 1) * P) - 1, rb);
+        const int npos = min(P, L - m * P);
+        const int pos0 = S - L + m * P;
+        const int kv_end = pos0 + npos;
+        const int nblk = ceil_div(kv_end, kBlockSize);
+        if (tile < p.cap.small_tiles) tiles_s[tile] = make_int4(first, ns, rb, 0);
+        for (int s = 0; s < ns && first + s < p.cap.small_items; ++s) {
+          items_s[first + s] = make_int4(r, m, s * rb, tile);
+          const int b0 = s * rb, b1 = min(b0 + rb, nblk);
+          recs_s[first + s].a = make_int4(r, m * P, b0, b1);
+          recs_s[first + s].b = make_int4(tile, first, ns, a);
+          recs_s[first + s].c = make_int4(npos, pos0, min(b1 * kBlockSize, kv_end), 0);
+        }
+        first += ns;
+      }
+    } else if (c == kClassPrefill) {
+      // tensor-core tiles of prefill_rows query rows (positions x grouped heads)
+      for (int m = 0; m < cnt[4] && off[4] + m < p.cap.prefill_tiles; ++m)
+        tiles_p[off[4] + m] = make_int4(r, m, 0, 0);
     }
 #pragma unroll
     for (int k = 0; k < kLists; ++k) carry_r[k] += tot[k];
@@ -173,8 +203,6 @@ __global__ void __launch_bounds__(kPlanThreads, 1) plan_kernel(PlanParams p) {
   }
   __syncthreads();
   if (threadIdx.x == 0) {
-    pfx_di[B] = carry[0]; pfx_dt[B] = carry[1]; pfx_si[B] = carry[2];
-    pfx_st[B] = carry[3]; pfx_pt[B] = carry[4];
     if (carry[0] > p.cap.decode_items || carry[1] > p.cap.decode_tiles ||
         carry[2] > p.cap.small_items || carry[3] > p.cap.small_tiles ||
         carry[4] > p.cap.prefill_tiles)
@@ -190,55 +218,6 @@ __global__ void __launch_bounds__(kPlanThreads, 1) plan_kernel(PlanParams p) {
     return;
   }
   const int n_di = carry[0], n_dt = carry[1], n_si = carry[2], n_st = carry[3], n_pt = carry[4];
-
-  // Pass 2: decode items, one split of one request each.
-  for (int i = threadIdx.x; i < n_di; i += kPlanThreads) {
-    const int r = find_owner(pfx_di, B, i);
-    const int s = i - pfx_di[r];
-    const int tile = pfx_dt[r];
-    const int S = __ldg(p.seq_lens + r);
-    const int nb = ceil_div(S, kBlockSize);
-    const int rb = request_bps(nb, p.bps);
-    const int ns = pfx_di[r + 1] - pfx_di[r];
-    items_d[i] = make_int4(r, 0, s * rb, tile);
-    if (s == 0) tiles_d[tile] = make_int4(i, ns, rb, 0);
-    const int b0 = s * rb, b1 = min(b0 + rb, nb);
-    recs_d[i].a = make_int4(r, 0, b0, b1);
-    recs_d[i].b = make_int4(tile, i - s, ns, __ldg(p.qsl + r));
-    recs_d[i].c = make_int4(1, S - 1, min(b1 * kBlockSize, S), 0);
-  }
-  // Small-q tiles: each thread expands one tile into its splits.
-  for (int tile = threadIdx.x; tile < n_st; tile += kPlanThreads) {
-    const int r = find_owner(pfx_st, B, tile);
-    const int m = tile - pfx_st[r];
-    const int S = __ldg(p.seq_lens + r);
-    const int L = __ldg(p.qsl + r + 1) - __ldg(p.qsl + r);
-    const int rb = request_bps(ceil_div(S, kBlockSize), p.bps);
-    int first = pfx_si[r];
-    for (int mm = 0; mm < m; ++mm)
-      first += splits_for(S - L + min(L, (mm + 1) * p.small_positions) - 1, rb);
-    const int ns = splits_for(S - L + min(L, (m + 1) * p.small_positions) - 1, rb);
-    const int P = p.small_positions;
-    const int npos = min(P, L - m * P);
-    const int pos0 = S - L + m * P;
-    const int kv_end = pos0 + npos;
-    const int nblk = ceil_div(kv_end, kBlockSize);
-    const int a = __ldg(p.qsl + r);
-    for (int s = 0; s < ns; ++s) {
-      items_s[first + s] = make_int4(r, m, s * rb, tile);
-      const int b0 = s * rb, b1 = min(b0 + rb, nblk);
-      recs_s[first + s].a = make_int4(r, m * P, b0, b1);
-      recs_s[first + s].b = make_int4(tile, first, ns, a);
-      recs_s[first + s].c = make_int4(npos, pos0, min(b1 * kBlockSize, kv_end), 0);
-    }
-    tiles_s[tile] = make_int4(first, ns, rb, 0);
-  }
-  // Prefill tiles: 128 query rows (positions x grouped heads) each.
-  int4* tiles_p = reinterpret_cast<int4*>(ws + p.lay.tiles_p);
-  for (int tile = threadIdx.x; tile < n_pt; tile += kPlanThreads) {
-    const int r = find_owner(pfx_pt, B, tile);
-    tiles_p[tile] = make_int4(r, tile - pfx_pt[r], 0, 0);
-  }
   for (int i = threadIdx.x; i < n_dt * p.num_kv_heads; i += kPlanThreads) cnt_d[i] = 0;
   for (int i = threadIdx.x; i < n_st * p.num_kv_heads; i += kPlanThreads) cnt_s[i] = 0;
   if (threadIdx.x == 0) {
