@@ -354,7 +354,8 @@ int pa_forward(const void* q, const void* k_cache, const void* v_cache,
     if (e != cudaSuccess) return fail_cuda(e, "side stream join");
   }
 
-  // decode rows (q_len == 1)
+  // decode rows (q_len == 1); the launch may overlap the plan's tail
+  ap.after_plan = 1;
   ap.n_items = hdr + kHdrDecodeItems;
   ap.next = hdr + kHdrDecodeNext;
   ap.items = reinterpret_cast<const int4*>(ws + lay.items_d);
@@ -371,6 +372,7 @@ int pa_forward(const void* q, const void* k_cache, const void* v_cache,
   if (g_prof_stop) cudaEventRecord(g_prof_stop, st);
 
   if (max_query_len > 1) {
+    ap.after_plan = 0;
     ap.n_items = hdr + kHdrSmallItems;
     ap.next = hdr + kHdrSmallNext;
     ap.items = reinterpret_cast<const int4*>(ws + lay.items_s);

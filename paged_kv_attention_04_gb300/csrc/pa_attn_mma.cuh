@@ -174,6 +174,7 @@ __global__ void __launch_bounds__(MmaCfg<D, G, P, NW, NS, F8>::kThreads,
   const unsigned char* vc = static_cast<const unsigned char*>(p.v_cache);
   const __nv_bfloat16* q = static_cast<const __nv_bfloat16*>(p.q);
   __nv_bfloat16* out = static_cast<__nv_bfloat16*>(p.out);
+  wait_prior_grid();  // the plan's work lists
   const int n_units = __ldg(p.n_items) * Hkv;
 
   // ---- scheduler-warp helpers -------------------------------------------
@@ -752,9 +753,19 @@ cudaError_t launch_mma(const AttnParams& p, int num_sms, cudaStream_t stream) {
     if (e != cudaSuccess) return e;
     ctas_per_sm[dev] = n > 0 ? n : 1;
   }
-  attn_mma_kernel<D, G, P, NW, NS, F8>
-      <<<num_sms * ctas_per_sm[dev], C::kThreads, C::kSmemBytes, stream>>>(p);
-  return cudaGetLastError();
+  // right after the plan kernel the launch may overlap its tail (the kernel
+  // waits for the plan before reading the work lists)
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(num_sms * ctas_per_sm[dev]);
+  cfg.blockDim = dim3(C::kThreads);
+  cfg.dynamicSmemBytes = C::kSmemBytes;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = p.after_plan ? 1 : 0;
+  return cudaLaunchKernelEx(&cfg, attn_mma_kernel<D, G, P, NW, NS, F8>, p);
 }
 
 }  // namespace pa

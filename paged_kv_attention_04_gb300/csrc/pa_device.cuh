@@ -30,6 +30,18 @@ __device__ __forceinline__ void cp_async_wait() {
 __device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
 __device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xffff0000u); }
 
+// Programmatic dependent launch: a kernel launched with programmatic stream
+// serialization may start while the previous kernel in its stream runs; it
+// waits here until that kernel has completed and its writes are visible (a
+// no-op for an ordinary launch).  The previous kernel lets it start early
+// with launch_dependents().
+__device__ __forceinline__ void wait_prior_grid() {
+  asm volatile("griddepcontrol.wait;\n" ::: "memory");
+}
+__device__ __forceinline__ void launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;\n" ::: "memory");
+}
+
 __device__ __forceinline__ void flag_error(int32_t* status, int bit) {
   if (status) atomicOr(reinterpret_cast<int*>(status), bit);
 }

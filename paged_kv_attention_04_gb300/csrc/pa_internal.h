@@ -84,6 +84,7 @@ struct AttnParams {
   float scale_log2;      // softmax scale * log2(e) (times k_scale for an FP8 cache)
   float out_scale;       // applied to the normalised output (v_scale for an FP8 cache)
   const int* n_items;    // device count of work items (x num_kv_heads units)
+  int after_plan;        // host side: launch with a programmatic dependency on the plan
   int* next;             // device work counter (zeroed by the plan kernel)
   const int4* items;     // {r, m, first KV block, tile}
   const UnitRec* recs;   // per item, the same fully decoded

@@ -86,6 +86,9 @@ __global__ void __launch_bounds__(kPlanThreads, 1) plan_kernel(PlanParams p) {
   __shared__ int warp_sums[32][kLists];
   __shared__ int carry[kLists];
   __shared__ int err;
+  // the attention kernel that follows may become resident now; it waits for
+  // this grid to finish before it reads the work lists
+  launch_dependents();
   const int B = p.num_seqs;
   char* ws = p.ws;
   int* hdr = reinterpret_cast<int*>(ws + p.lay.hdr);
