@@ -35,6 +35,7 @@ __global__ void __launch_bounds__(256) cache_write_kernel(
     const uint4* __restrict__ k, const uint4* __restrict__ v, const int64_t* __restrict__ slots,
     int num_tokens, uint4* __restrict__ k_cache, uint4* __restrict__ v_cache, int row_chunks,
     long long num_slots, int32_t* status) {
+  launch_dependents();  // a following plan kernel may start; it waits for this grid
   const long long total = static_cast<long long>(num_tokens) * row_chunks;
   for (long long i = blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x; i < total;
        i += static_cast<long long>(gridDim.x) * blockDim.x) {
@@ -62,6 +63,7 @@ __global__ void __launch_bounds__(256) cache_write_fp8_kernel(
     const uint4* __restrict__ k, const uint4* __restrict__ v, const int64_t* __restrict__ slots,
     int num_tokens, uint2* __restrict__ k_cache, uint2* __restrict__ v_cache, int row_chunks,
     long long num_slots, float k_scale, float v_scale, int32_t* status) {
+  launch_dependents();  // a following plan kernel may start; it waits for this grid
   const long long total = static_cast<long long>(num_tokens) * row_chunks;
   for (long long i = blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x; i < total;
        i += static_cast<long long>(gridDim.x) * blockDim.x) {

@@ -87,8 +87,11 @@ __global__ void __launch_bounds__(kPlanThreads, 1) plan_kernel(PlanParams p) {
   __shared__ int carry[kLists];
   __shared__ int err;
   // the attention kernel that follows may become resident now; it waits for
-  // this grid to finish before it reads the work lists
+  // this grid to finish before it reads the work lists.  This grid itself may
+  // have started early (programmatic launch): wait for the previous kernel in
+  // the stream before reading anything it might have written.
   launch_dependents();
+  wait_prior_grid();
   const int B = p.num_seqs;
   char* ws = p.ws;
   int* hdr = reinterpret_cast<int*>(ws + p.lay.hdr);
@@ -237,8 +240,16 @@ __global__ void __launch_bounds__(kPlanThreads, 1) plan_kernel(PlanParams p) {
 }
 
 cudaError_t launch_plan(const PlanParams& p, cudaStream_t stream) {
-  plan_kernel<<<1, kPlanThreads, 0, stream>>>(p);
-  return cudaGetLastError();
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(1);
+  cfg.blockDim = dim3(kPlanThreads);
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, plan_kernel, p);
 }
 
 }  // namespace pa
