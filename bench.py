@@ -211,12 +211,14 @@ class ClockSampler:
 # ---------------------------------------------------------------------------
 
 def oracle_worker(name: str, min_seconds: float, stride: int, steps: int, warmup: int,
-                  step_budget: float) -> None:
+                  step_budget: float, offset: int = 0, sync: bool = False) -> None:
     """Time the fp64 oracle on a sample of workload `name`: every `stride`-th
-    request (stride 0: chosen so one pass fits `step_budget` seconds), each
+    request from `offset` (stride 0: chosen so one pass fits `step_budget` seconds), each
     with a private copy of its blocks; one pass = slot write + attention of the
     sampled requests.  With steps > 0, times warmup + steps passes and reports
-    the timed ones; else repeats passes until min_seconds.  Prints JSON."""
+    the timed ones; else repeats passes until min_seconds.  With sync, prints
+    "ready" once the sample is prepared and starts timing when a line arrives
+    on stdin (so that concurrent workers time the same interval).  Prints JSON."""
     import numpy as np
 
     import oracle
@@ -251,12 +253,15 @@ def oracle_worker(name: str, min_seconds: float, stride: int, steps: int, warmup
         per_req = (time.perf_counter() - t) / len(probe)
         n = int(max(1, min(spec.num_seqs, step_budget / max(per_req, 1e-6))))
         stride = max(1, spec.num_seqs // n)
-    reqs = list(range(0, spec.num_seqs, stride))
+    reqs = list(range(offset, spec.num_seqs, stride))
     samples = [prep(r) for r in reqs]
     sub = W.custom_spec("sample", spec.dtype, spec.num_q_heads, spec.num_kv_heads, spec.head_size,
                         [s["L"] for s in samples], [s["S"] for s in samples])
     work = step_work(sub, W.make_meta(sub))
     del st
+    if sync:
+        print("ready", flush=True)
+        sys.stdin.readline()
     times = []
     if steps > 0:
         for i in range(warmup + steps):
@@ -276,8 +281,7 @@ def oracle_worker(name: str, min_seconds: float, stride: int, steps: int, warmup
                       "tokens_per_rep": work["tokens"]}))
 
 
-def time_oracle(name: str, min_seconds: float = 10.0, stride: int = 1, steps: int = 0,
-                warmup: int = 0, step_budget: float = 1.0) -> dict:
+def _oracle_cmd_env(name, min_seconds, stride, steps, warmup, step_budget, offset=0, sync=False):
     env = dict(os.environ)
     for k in ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS", "MKL_NUM_THREADS", "NUMEXPR_NUM_THREADS"):
         env[k] = "1"
@@ -286,11 +290,57 @@ def time_oracle(name: str, min_seconds: float = 10.0, stride: int = 1, steps: in
         env.pop(k, None)
     cmd = [sys.executable, os.path.abspath(__file__), "--oracle-worker", name,
            "--oracle-seconds", str(min_seconds), "--oracle-stride", str(stride),
+           "--oracle-offset", str(offset),
+           *(["--oracle-sync"] if sync else []),
            "--steps", str(steps), "--warmup", str(warmup), "--oracle-budget", str(step_budget)]
+    return cmd, env
+
+
+def time_oracle(name: str, min_seconds: float = 10.0, stride: int = 1, steps: int = 0,
+                warmup: int = 0, step_budget: float = 1.0) -> dict:
+    cmd, env = _oracle_cmd_env(name, min_seconds, stride, steps, warmup, step_budget)
     res = subprocess.run(cmd, capture_output=True, text=True, env=env, cwd=ROOT)
     if res.returncode != 0:
         raise RuntimeError(f"oracle worker failed: {res.stderr[-2000:]}")
     return json.loads(res.stdout.strip().splitlines()[-1])
+
+
+def time_oracle_all_cores(name: str, min_seconds: float = 10.0) -> dict:
+    """The same single-threaded oracle in one process per host core, each on a
+    disjoint share of the requests (every n-th from its own offset), all at
+    once: every worker prepares its sample, then all start timing together.
+    Returns the summed bytes per second, the cores used and the requests."""
+    from paged_kv_attention_04_gb300 import workloads as W
+    n_req = W.CONFIGS[name]().num_seqs
+    n = len(os.sched_getaffinity(0)) if hasattr(os, "sched_getaffinity") else os.cpu_count()
+    n = max(1, min(n or 1, n_req))
+    procs = []
+    for j in range(n):
+        cmd, env = _oracle_cmd_env(name, min_seconds, n, 0, 0, 1.0, offset=j, sync=True)
+        procs.append(subprocess.Popen(cmd, stdin=subprocess.PIPE, stdout=subprocess.PIPE,
+                                      stderr=subprocess.PIPE, text=True, env=env, cwd=ROOT))
+    try:
+        for pr in procs:
+            if pr.stdout.readline().strip() != "ready":
+                raise RuntimeError(f"oracle worker failed: {pr.stderr.read()[-2000:]}")
+        for pr in procs:
+            pr.stdin.write("go\n")
+            pr.stdin.flush()
+        gbs, reqs, secs = 0.0, 0, []
+        for pr in procs:
+            out, err = pr.communicate()
+            if pr.returncode != 0:
+                raise RuntimeError(f"oracle worker failed: {err[-2000:]}")
+            o = json.loads(out.strip().splitlines()[-1])
+            gbs += o["bytes_per_rep"] * o["reps"] / o["seconds"] / 1e9
+            reqs += o["requests"]
+            secs.append(o["seconds"])
+    finally:
+        for pr in procs:
+            if pr.poll() is None:
+                pr.kill()
+                pr.wait()
+    return {"gbs": gbs, "cores": n, "requests": reqs, "seconds": min(secs)}
 
 
 # ---------------------------------------------------------------------------
@@ -642,6 +692,12 @@ def run_gpu_arm(args):
             "sample": f"{o['requests']} of 256 requests (every {o['stride']}th), each with its own "
                       f"blocks: fp64 slot write + attention, {o['reps']} passes, "
                       f"{o['seconds']:.1f} s on 1 core"}
+        a = time_oracle_all_cores(HEADLINE, min_seconds=args.oracle_seconds)
+        line["cpu_baseline_all_cores"] = {
+            "value": a["gbs"], "unit": "GB/s", "cores": a["cores"], "kind": "oracle",
+            "sample": f"all 256 requests split over {a['cores']} single-threaded processes "
+                      f"(every {a['cores']}th request each, {a['requests']} in all), timed "
+                      f"together for at least {a['seconds']:.1f} s"}
     if rank == 0:
         print(json.dumps(line))
     if world > 1:
@@ -721,6 +777,8 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--oracle-seconds", type=float, default=10.0)
     ap.add_argument("--oracle-stride", type=int, default=1)
+    ap.add_argument("--oracle-offset", type=int, default=0, help=argparse.SUPPRESS)
+    ap.add_argument("--oracle-sync", action="store_true", help=argparse.SUPPRESS)
     ap.add_argument("--ncu-case", default=None,
                     help="run a small step for a profiler: NAME, NAME:N (first N requests) "
                          "or NAME:-N (last N)")
@@ -733,7 +791,7 @@ def main():
         return
     if args.oracle_worker:
         oracle_worker(args.oracle_worker, args.oracle_seconds, args.oracle_stride, args.steps,
-                      args.warmup, args.oracle_budget)
+                      args.warmup, args.oracle_budget, args.oracle_offset, args.oracle_sync)
         return
     if args.warmup < 3:
         args.warmup = 3
