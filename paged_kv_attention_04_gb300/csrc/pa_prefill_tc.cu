@@ -71,23 +71,26 @@ struct PfCfg {
   static_assert(kSmemBytes <= 227 * 1024, "shared memory per CTA exceeds 227 KB");
 };
 
-// mbarriers.  [2] = one per softmax warpgroup (or ring slot).
+// mbarriers.  [2] = one per softmax warpgroup (or ring slot).  The MMA warp
+// waits once per KV tile t: kGo gathers everything O += P V over t and
+// S = Q K^T over t + 2 (same group, same buffers) need, so the tensor cores
+// are not left idle between hand-offs.
 enum Bar : int {
   kUnitFull = 0,    // [2] unit info published (loader)
   kUnitEmpty = 2,   // [2] unit info read (8 softmax warps, MMA warp, V loader)
   kQFull = 4,       // Q tile landed (TMA)
   kQEmpty = 5,      // every S of the unit done (MMA commit)
-  kKFull = 6,       // [2] K tile landed (TMA)
+  kKFirst = 6,      // [2] the unit's first K tile of the group landed (TMA)
   kSFull = 8,       // [2] S = Q K^T done (MMA commit); also frees the K buffer
-  kSEmpty = 10,     // [2] S read into registers (4 warps)
-  kVFull = 12,      // [2] V tile landed (TMA)
-  kPFull = 14,      // [2] P written (4 warps)
-  kPVDone = 16,     // [2] O += P V done (MMA commit); frees V and P, O stable
-  kMlFull = 18,     // row (m, l) of both groups published (8 warps)
-  kMlRead = 19,     // ... and read (8 warps)
-  kOFree = 20,      // O of both groups read by the epilogue (8 warps)
-  kDrain = 21,      // teardown after a timeout
-  kNumBars = 22
+  kGo = 10,         // [2] tile t: P written and S read (4 softmax warps), V of t landed
+                    //     (V loader), K of t + 2 landed or none due (K loader)
+  kVLand = 12,      // [2] V tile landed, for a tile whose last block the V loader trims
+  kPVDone = 14,     // [2] O += P V done (MMA commit); frees V and P, O stable
+  kMlFull = 16,     // row (m, l) of both groups published (8 warps)
+  kMlRead = 17,     // ... and read (8 warps)
+  kOFree = 18,      // O of both groups read by the epilogue (8 warps)
+  kDrain = 19,      // teardown after a timeout
+  kNumBars = 20
 };
 
 struct UnitInfo {
@@ -165,16 +168,20 @@ __device__ __forceinline__ bool wait_bar(uint32_t bar, uint32_t parity, volatile
 // Arrivals that complete a phase of each barrier.
 __device__ __forceinline__ uint32_t bar_count(int i) {
   if (i == kUnitEmpty || i == kUnitEmpty + 1) return 10;  // 8 softmax warps, MMA, V loader
-  if (i == kSEmpty || i == kSEmpty + 1 || i == kPFull || i == kPFull + 1) return 4;
+  if (i == kGo || i == kGo + 1) return 6;  // 4 softmax warps, V loader, K loader
   if (i == kMlFull || i == kMlRead || i == kOFree) return 8;
   return 1;  // TMA (arrive + bytes) or tcgen05.commit
 }
 
-// Teardown wait (warp-uniform, bounded, ignores the abort flag).
-__device__ __forceinline__ void drain_wait(uint32_t bar, uint32_t parity) {
-  for (uint32_t i = 0; i < kWaitLimit; ++i)
+// Teardown wait (warp-uniform, bounded, ignores the abort flag).  A kGo
+// phase that carried a copy may never complete after an abort (other roles
+// stop arriving): the shorter limit still outlasts the copy.
+__device__ __forceinline__ void drain_wait(uint32_t bar, uint32_t parity,
+                                           uint32_t limit = kWaitLimit) {
+  for (uint32_t i = 0; i < limit; ++i)
     if (__all_sync(0xffffffffu, mbar_try_wait(bar, parity))) return;
 }
+constexpr uint32_t kGoDrainLimit = 1u << 20;
 
 // One arrival per warp, after every lane's preceding work.
 __device__ __forceinline__ void warp_arrive(uint32_t bar) {
@@ -259,7 +266,10 @@ __global__ void __launch_bounds__(kPfThreads, 1)
     // ------------------------------------------------------------ units, Q, K
     const int Hkv = p.num_kv_heads;
     const int n_units = __ldg(p.n_items) * Hkv;
-    uint32_t nk[2] = {0, 0}, nq = 0;
+    // nf: first-K copies per group; sw: S phases waited per group; ga: kGo
+    // arrivals per group (one per tile of the group), gk: the last one that
+    // carried a copy, plus one
+    uint32_t nf[2] = {0, 0}, sw[2] = {0, 0}, ga[2] = {0, 0}, gk[2] = {0, 0}, nq = 0;
     for (int uc = 0;; ++uc) {
       int unit = 0;
       if (lane == 0) unit = atomicAdd(p.next, 1);
@@ -304,29 +314,49 @@ __global__ void __launch_bounds__(kPfThreads, 1)
       }
       ++nq;
       bool ok = true;
+      // K of tile sq goes into buffer w = sq & 1.  The first two were freed
+      // by the previous unit (its last S of each group was waited below);
+      // later ones wait for S of tile sq - 2 and then count as that tile's
+      // kGo arrival (bytes included)
       for (int sq = 0; sq < u.n_kv; ++sq) {
         const int w = sq & 1;
-        // K buffer w is free once S of the group's previous tile is done
-        if (nk[w] > 0 && !wait_bar(bar(kSFull + w), (nk[w] - 1) & 1, abort, p.status)) {
-          ok = false;
-          break;
+        uint32_t full = bar(kKFirst + w);
+        if (sq >= 2) {
+          if (!wait_bar(bar(kSFull + w), sw[w] & 1, abort, p.status)) { ok = false; break; }
+          ++sw[w];
+          full = bar(kGo + w);
+          gk[w] = ++ga[w];
+        } else {
+          ++nf[w];
         }
-        copy_kv_tile(u, tile_of(u, sq), ph, false, sbase + C::kKOff + w * C::kTileBytes,
-                     bar(kKFull + w));
-        ++nk[w];
+        copy_kv_tile(u, tile_of(u, sq), ph, false, sbase + C::kKOff + w * C::kTileBytes, full);
         if (sq + 1 < u.n_kv) ph = tile_phys(u, tile_of(u, sq + 1));
+      }
+      // tiles with no K two places on: a plain kGo arrival once their S is done
+      for (int t = max(0, u.n_kv - 2); ok && t < u.n_kv; ++t) {
+        const int w = t & 1;
+        if (!wait_bar(bar(kSFull + w), sw[w] & 1, abort, p.status)) { ok = false; break; }
+        ++sw[w];
+        ++ga[w];
+        warp_arrive(bar(kGo + w));
       }
       if (!ok) break;
     }
     if (*abort) {  // let every copy issued land before the CTA ends
       if (nq > 0) drain_wait(bar(kQFull), (nq - 1) & 1);
-      for (int w = 0; w < 2; ++w)
-        if (nk[w] > 0) drain_wait(bar(kKFull + w), (nk[w] - 1) & 1);
+      for (int w = 0; w < 2; ++w) {
+        if (nf[w] > 0) drain_wait(bar(kKFirst + w), (nf[w] - 1) & 1);
+        if (gk[w] > 0) drain_wait(bar(kGo + w), (gk[w] - 1) & 1, kGoDrainLimit);
+      }
     }
     __syncwarp();
   } else if (warp == kVLoadWarp) {
     // ------------------------------------------------------------ V
-    uint32_t nv[2] = {0, 0};
+    // nv: V tiles per group (= kGo arrivals); gv: the last kGo phase that
+    // carried a copy, plus one; nl: kVLand copies per group
+    uint32_t nv[2] = {0, 0}, gv[2] = {0, 0}, nl[2] = {0, 0};
+    bool landing = false;  // a kVLand copy not yet waited for
+    int land_w = 0;
     for (int uc = 0;; ++uc) {
       const int slot = uc & 1;
       if (!wait_bar(bar(kUnitFull + slot), (uc >> 1) & 1, abort, p.status)) break;
@@ -337,26 +367,55 @@ __global__ void __launch_bounds__(kPfThreads, 1)
       bool ok = true;
       for (int sq = 0; sq < u.n_kv; ++sq) {
         const int w = sq & 1;
+        const int kt = tile_of(u, sq);
         // V buffer w is free once PV of the group's previous tile is done
         if (nv[w] > 0 && !wait_bar(bar(kPVDone + w), (nv[w] - 1) & 1, abort, p.status)) {
           ok = false;
           break;
         }
-        copy_kv_tile(u, tile_of(u, sq), ph, true, sbase + C::kVOff + w * C::kTileBytes,
-                     bar(kVFull + w));
+        const uint32_t vb = sbase + C::kVOff + w * C::kTileBytes;
+        if (kt != u.n_kv - 1 || (u.kv_end & (kBlockSize - 1)) == 0) {
+          copy_kv_tile(u, kt, ph, true, vb, bar(kGo + w));  // this tile's kGo arrival
+          gv[w] = nv[w] + 1;
+        } else {
+          // the unit's last block is partial: its rows past the last key
+          // (unwritten slots) are zeroed once the tile has landed, so that
+          // p = 0 never meets a NaN there; then the kGo arrival
+          copy_kv_tile(u, kt, ph, true, vb, bar(kVLand + w));
+          landing = true;
+          land_w = w;
+          if (!wait_bar(bar(kVLand + w), nl[w] & 1, abort, p.status)) { ok = false; break; }
+          landing = false;
+          ++nl[w];
+          const int tok0 = kt * kTileN;
+          const int r0 = u.kv_end - tok0;
+          const int r1 = ((u.kv_end + kBlockSize - 1) & ~(kBlockSize - 1)) - tok0;
+          constexpr int per_row = (D / 64) * 8;  // 16-byte chunks per row
+          for (int idx = lane; idx < (r1 - r0) * per_row; idx += 32) {
+            const int row = r0 + idx / per_row, c = idx % per_row;
+            asm volatile("st.shared.v4.b32 [%0], {%1,%1,%1,%1};\n" ::"r"(
+                             vb + (row >> 4) * C::kVBlockBytes + (c >> 3) * (kBlockSize * 128) +
+                             (row & 15) * 128 + (c & 7) * 16),
+                         "r"(0u)
+                         : "memory");
+          }
+          fence_proxy_async_smem();
+          warp_arrive(bar(kGo + w));
+        }
         ++nv[w];
         if (sq + 1 < u.n_kv) ph = tile_phys(u, tile_of(u, sq + 1));
       }
       if (!ok) break;
     }
     if (*abort) {
+      if (landing) drain_wait(bar(kVLand + land_w), nl[land_w] & 1);
       for (int w = 0; w < 2; ++w)
-        if (nv[w] > 0) drain_wait(bar(kVFull + w), (nv[w] - 1) & 1);
+        if (gv[w] > 0) drain_wait(bar(kGo + w), (gv[w] - 1) & 1, kGoDrainLimit);
     }
     __syncwarp();
   } else if (warp == kMmaWarp) {
     // ------------------------------------------------------------ MMA issue
-    uint32_t ns[2] = {0, 0}, npv[2] = {0, 0};
+    uint32_t ns[2] = {0, 0}, npv[2] = {0, 0}, nf[2] = {0, 0};
     bool ok = true;
     for (int uc = 0; ok; ++uc) {
       const int slot = uc & 1;
@@ -367,12 +426,17 @@ __global__ void __launch_bounds__(kPfThreads, 1)
       if (!wait_bar(bar(kQFull), uc & 1, abort, p.status)) break;
       tc_fence_after();
 
+      // S(t): for t >= 2 its K and a free S were covered by kGo of t - 2,
+      // waited just before; the unit's first two wait for their K copy (S of
+      // the previous unit was read before that unit's last kGo)
       auto issue_s = [&](int t) {
         const int w = t & 1;
         const uint32_t n = ns[w];
-        if (!wait_bar(bar(kKFull + w), n & 1, abort, p.status)) return false;
-        if (n > 0 && !wait_bar(bar(kSEmpty + w), (n - 1) & 1, abort, p.status)) return false;
-        tc_fence_after();
+        if (t < 2) {
+          if (!wait_bar(bar(kKFirst + w), nf[w] & 1, abort, p.status)) return false;
+          ++nf[w];
+          tc_fence_after();
+        }
         if (lane == 0) {
           const uint32_t qa = sbase + C::kQOff, kb = sbase + C::kKOff + w * C::kTileBytes;
 #pragma unroll
@@ -391,8 +455,7 @@ __global__ void __launch_bounds__(kPfThreads, 1)
       auto issue_pv = [&](int t) {
         const int w = t & 1;
         const uint32_t n = npv[w];
-        if (!wait_bar(bar(kPFull + w), n & 1, abort, p.status)) return false;
-        if (!wait_bar(bar(kVFull + w), n & 1, abort, p.status)) return false;
+        if (!wait_bar(bar(kGo + w), n & 1, abort, p.status)) return false;
         // the previous unit's epilogue must have read O before it is overwritten
         if (t == 0 && uc > 0 && !wait_bar(bar(kOFree), (uc - 1) & 1, abort, p.status)) return false;
         tc_fence_after();
@@ -460,10 +523,9 @@ __global__ void __launch_bounds__(kPfThreads, 1)
       for (int t = w; t < u.n_kv; t += 2, ++n) {  // t: place in the unit's order
         const int kt = tile_of(u, t);
         const int tok0 = kt * kTileN;
+        // S of this tile was issued after the group's previous PV, and a
+        // commit covers every earlier MMA: P and O are free as well
         if (!wait_bar(bar(kSFull + w), n & 1, abort, p.status)) { ok = false; break; }
-        // this group's previous PV is complete as well (S of this tile was
-        // issued after it), so P and O are free
-        if (n > 0 && !wait_bar(bar(kPVDone + w), (n - 1) & 1, abort, p.status)) { ok = false; break; }
         tc_fence_after();
 
         // causal edge (or a padding row): keys c > lim are masked
@@ -558,27 +620,9 @@ __global__ void __launch_bounds__(kPfThreads, 1)
           }
           tmem_wait_st();
         }
-        // last tile: V rows past the last key (unwritten slots of the final
-        // block) are zeroed, so p = 0 never meets a NaN there
-        if (kt == u.n_kv - 1 && (u.kv_end & (kBlockSize - 1))) {
-          if (!wait_bar(bar(kVFull + w), n & 1, abort, p.status)) { ok = false; break; }
-          const int r0 = u.kv_end - tok0;
-          const int r1 = ((u.kv_end + kBlockSize - 1) & ~(kBlockSize - 1)) - tok0;
-          const int per_row = (D / 64) * 8;
-          const uint32_t vb = sbase + C::kVOff + w * C::kTileBytes;
-          for (int idx = i; idx < (r1 - r0) * per_row; idx += 128) {
-            const int row = r0 + idx / per_row, c = idx % per_row;
-            asm volatile("st.shared.v4.b32 [%0], {%1,%1,%1,%1};\n" ::"r"(
-                             vb + (row >> 4) * C::kVBlockBytes + (c >> 3) * (kBlockSize * 128) +
-                             (row & 15) * 128 + (c & 7) * 16),
-                         "r"(0u)
-                         : "memory");
-          }
-        }
         fence_proxy_async_smem();
         tc_fence_before();
-        warp_arrive(bar(kSEmpty + w));
-        warp_arrive(bar(kPFull + w));
+        warp_arrive(bar(kGo + w));  // S read, P written, O rescaled
       }
       if (!ok) break;
 
