@@ -415,7 +415,39 @@ __global__ void __launch_bounds__(kPfThreads, 1)
     __syncwarp();
   } else if (warp == kMmaWarp) {
     // ------------------------------------------------------------ MMA issue
-    uint32_t ns[2] = {0, 0}, npv[2] = {0, 0}, nf[2] = {0, 0};
+    // Kept lean: every cycle this warp spends between products is tensor-core
+    // idle time (the issue queue is shallow).  Counters live in registers,
+    // descriptors are built once and advanced by their address field.
+    constexpr uint32_t kIdS = idesc_bf16(kTileM, kTileN, 0);
+    constexpr uint32_t kIdPV = idesc_bf16(kTileM, D, 1);
+    const uint64_t dq = smem_desc_sw128(sbase + C::kQOff, 16, 1024);
+    const uint64_t dk = smem_desc_sw128(sbase + C::kKOff, 16, 1024);
+    const uint64_t dp = smem_desc_sw128(sbase + C::kPOff, 16, 1024);
+    const uint64_t dv = smem_desc_sw128(sbase + C::kVOff, kBlockSize * 128, 1024);
+    // byte offset -> descriptor start-address field (16-byte units; no carry:
+    // shared addresses stay below 2^18)
+    auto adv = [](uint64_t d, uint32_t bytes) { return d + (bytes >> 4); };
+    // S = Q K^T of tile t into S buffer w (K buffer w)
+    auto mma_s = [&](int w) {
+      const uint64_t kb = adv(dk, w * C::kTileBytes);
+#pragma unroll
+      for (int kk = 0; kk < D / 16; ++kk) {
+        const uint32_t koff = (kk >> 2) * C::kRegionBytes + (kk & 3) * 32;
+        tc_mma_f16(tmem + w * kTileN, adv(dq, koff), adv(kb, koff), kIdS, kk > 0);
+      }
+      tc_commit(bar(kSFull + w));
+    };
+    // O += P V of group w's tile (P and V buffers w); first: O is overwritten
+    auto mma_pv = [&](int w, bool first) {
+      const uint64_t pb = adv(dp, w * C::kPBytes), vb = adv(dv, w * C::kTileBytes);
+#pragma unroll
+      for (int kk = 0; kk < kTileN / 16; ++kk)
+        tc_mma_f16(tmem + 256 + w * 128, adv(pb, (kk >> 2) * C::kRegionBytes + (kk & 3) * 32),
+                   adv(vb, kk * C::kVBlockBytes), kIdPV, (first && kk == 0) ? 0u : 1u);
+      tc_commit(bar(kPVDone + w));
+    };
+    uint32_t g0 = 0, g1 = 0;    // tiles per group so far (kGo phases)
+    uint32_t nf0 = 0, nf1 = 0;  // first-K copies per group so far
     bool ok = true;
     for (int uc = 0; ok; ++uc) {
       const int slot = uc & 1;
@@ -423,72 +455,49 @@ __global__ void __launch_bounds__(kPfThreads, 1)
       const UnitInfo u = s_units[slot];
       warp_arrive(bar(kUnitEmpty + slot));
       if (u.r < 0) break;
+      const int nkv = u.n_kv;
       if (!wait_bar(bar(kQFull), uc & 1, abort, p.status)) break;
+      // The unit's first two S wait for their K copies (S of the previous
+      // unit was read before that unit's last kGo); later S(t + 2) go right
+      // behind PV(t), both covered by kGo of t.
+      if (!wait_bar(bar(kKFirst), nf0 & 1, abort, p.status)) break;
+      ++nf0;
       tc_fence_after();
-
-      // S(t): for t >= 2 its K and a free S were covered by kGo of t - 2,
-      // waited just before; the unit's first two wait for their K copy (S of
-      // the previous unit was read before that unit's last kGo)
-      auto issue_s = [&](int t) {
-        const int w = t & 1;
-        const uint32_t n = ns[w];
-        if (t < 2) {
-          if (!wait_bar(bar(kKFirst + w), nf[w] & 1, abort, p.status)) return false;
-          ++nf[w];
-          tc_fence_after();
-        }
-        if (lane == 0) {
-          const uint32_t qa = sbase + C::kQOff, kb = sbase + C::kKOff + w * C::kTileBytes;
-#pragma unroll
-          for (int kk = 0; kk < D / 16; ++kk) {
-            const uint32_t koff = (kk >> 2) * C::kRegionBytes + (kk & 3) * 32;
-            tc_mma_f16(tmem + w * kTileN, smem_desc_sw128(qa + koff, 16, 1024),
-                       smem_desc_sw128(kb + koff, 16, 1024), idesc_bf16(kTileM, kTileN, 0),
-                       kk > 0);
-          }
-          tc_commit(bar(kSFull + w));
-        }
-        __syncwarp();
-        ns[w] = n + 1;
-        return true;
-      };
-      auto issue_pv = [&](int t) {
-        const int w = t & 1;
-        const uint32_t n = npv[w];
-        if (!wait_bar(bar(kGo + w), n & 1, abort, p.status)) return false;
-        // the previous unit's epilogue must have read O before it is overwritten
-        if (t == 0 && uc > 0 && !wait_bar(bar(kOFree), (uc - 1) & 1, abort, p.status)) return false;
+      if (lane == 0) mma_s(0);
+      __syncwarp();
+      if (nkv > 1) {
+        if (!wait_bar(bar(kKFirst + 1), nf1 & 1, abort, p.status)) break;
+        ++nf1;
         tc_fence_after();
-        if (lane == 0) {
-          const uint32_t pa = sbase + C::kPOff + w * C::kPBytes;
-          const uint32_t vb = sbase + C::kVOff + w * C::kTileBytes;
-#pragma unroll
-          for (int kk = 0; kk < kTileN / 16; ++kk)
-            tc_mma_f16(tmem + 256 + w * 128,
-                       smem_desc_sw128(pa + (kk >> 2) * C::kRegionBytes + (kk & 3) * 32, 16, 1024),
-                       smem_desc_sw128(vb + kk * C::kVBlockBytes, kBlockSize * 128, 1024),
-                       idesc_bf16(kTileM, D, 1), (t >= 2 || kk > 0) ? 1u : 0u);
-          tc_commit(bar(kPVDone + w));
-        }
+        if (lane == 0) mma_s(1);
         __syncwarp();
-        npv[w] = n + 1;
-        return true;
-      };
-      auto release_q = [&]() {
+      }
+      if (nkv <= 2) {
         if (lane == 0) tc_commit(bar(kQEmpty));
         __syncwarp();
-      };
+      }
       // PV(t) goes before S(t + 2): when a group's next S is done, so is its
       // previous PV (a commit covers every earlier MMA), so its softmax never
       // waits for P or O to be free; the other group keeps the tensor cores busy
-      ok = issue_s(0) && (u.n_kv < 2 || issue_s(1));
-      if (ok && u.n_kv <= 2) release_q();
-      for (int t = 0; ok && t < u.n_kv; ++t) {
-        ok = issue_pv(t);
-        if (ok && t + 2 < u.n_kv) {
-          ok = issue_s(t + 2);
-          if (ok && t + 2 == u.n_kv - 1) release_q();
+      for (int t = 0; t < nkv; ++t) {
+        const int w = t & 1;
+        const uint32_t g = w ? g1 : g0;
+        if (!wait_bar(bar(kGo + w), g & 1, abort, p.status)) { ok = false; break; }
+        // the previous unit's epilogue must have read O before it is overwritten
+        if (t == 0 && uc > 0 && !wait_bar(bar(kOFree), (uc - 1) & 1, abort, p.status)) {
+          ok = false;
+          break;
         }
+        tc_fence_after();
+        if (lane == 0) {
+          mma_pv(w, t < 2);
+          if (t + 2 < nkv) {
+            mma_s(w);
+            if (t + 2 == nkv - 1) tc_commit(bar(kQEmpty));
+          }
+        }
+        __syncwarp();
+        if (w) ++g1; else ++g0;
       }
     }
     if (*abort) {  // every MMA issued must finish before TMEM is released
