@@ -61,8 +61,13 @@ struct PfCfg {
   static constexpr int kQOff = 0;
   static constexpr int kKOff = kQOff + kTileBytes;      // K0, K1
   static constexpr int kVOff = kKOff + 2 * kTileBytes;  // V0, V1
-  // a V tile is stored per 16-token block: [block][64-column half][16 rows][128 B]
+  // K and V tiles are stored per 16-token block (one TMA box each):
+  //   K [block][8-row group][64-column half][8 rows][128 B]: every 8-key core
+  //     group of a column half sits kKGroupBytes after the previous one, as
+  //     the K-major operand of S = Q K^T requires;
+  //   V [block][64-column half][16 rows][128 B] (MN-major operand of P V).
   static constexpr int kVBlockBytes = kBlockSize * 128 * (D / 64);
+  static constexpr int kKGroupBytes = 8 * 128 * (D / 64);
   static constexpr int kPOff = kVOff + 2 * kTileBytes;  // P0, P1
   static constexpr int kSmemBytes = kPOff + 2 * kPBytes + 1024;  // + alignment slack
   static constexpr int kTmemCols = 512;  // S0, S1 at 0 / 128; O0, O1 at 256 / 384
@@ -106,7 +111,8 @@ __device__ __forceinline__ int tile_of(const UnitInfo& u, int s) {
 
 struct PfMaps {
   CUtensorMap q;  // q [T][Hq][D] as 3-D (D, Hq, T), box (64, G, 128/G)
-  CUtensorMap k;  // k_cache [NB][16][Hkv][D] as 4-D (D, Hkv, 16, NB), box (64, 1, 16, 1)
+  CUtensorMap k;  // k_cache as 5-D (64, 8 rows, D/64 halves, 2 row groups, NB x 16 x Hkv),
+                  // box (64, 8, D/64, 2, 1) at block x 16 x Hkv + head
   CUtensorMap v;  // v_cache as 5-D (64, 16 rows, D/64 halves, Hkv, NB), box (64, 16, D/64, 1, 1)
 };
 
@@ -236,11 +242,9 @@ __global__ void __launch_bounds__(kPfThreads, 1)
     return -1;
   };
   // TMA copy of KV tile t of unit u into the swizzled buffer at dst: lane
-  // b < 8 copies block b; a block past the unit's keys or with a bad table
-  // entry is read at index num_blocks (zeros).  K tiles take one box per 64
-  // columns (rows of a K tile are the N dimension of S = Q K^T and must sit
-  // 128 bytes apart); V tiles take one box per block (both halves), half the
-  // boxes, laid out [block][half][row] for the MN-major PV operand.
+  // b < 8 copies block b, one box (all D columns) per block, in the layouts
+  // given with PfCfg; a block past the unit's keys or with a bad table entry
+  // is read at index num_blocks (out of bounds: zeros).
   auto copy_kv_tile = [&](const UnitInfo& u, int t, int ph, bool is_v, uint32_t dst,
                           uint32_t full) {
     if (lane < kTileN / kBlockSize && ph != -1 && (ph < 0 || ph >= p.num_blocks)) {
@@ -251,14 +255,11 @@ __global__ void __launch_bounds__(kPfThreads, 1)
     __syncwarp();
     if (lane < kTileN / kBlockSize) {
       const int coord = ph < 0 ? p.num_blocks : ph;
-      if (is_v) {
+      if (is_v)
         tma_load_5d(dst + lane * C::kVBlockBytes, &maps.v, 0, 0, 0, u.g, coord, full);
-      } else {
-#pragma unroll
-        for (int h = 0; h < D / 64; ++h)
-          tma_load_4d(dst + h * C::kRegionBytes + lane * (kBlockSize * 128), &maps.k, h * 64, u.g,
-                      0, coord, full);
-      }
+      else
+        tma_load_5d(dst + lane * C::kVBlockBytes, &maps.k, 0, 0, 0, 0,
+                    coord * kBlockSize * p.num_kv_heads + u.g, full);
     }
   };
 
@@ -421,7 +422,7 @@ __global__ void __launch_bounds__(kPfThreads, 1)
     constexpr uint32_t kIdS = idesc_bf16(kTileM, kTileN, 0);
     constexpr uint32_t kIdPV = idesc_bf16(kTileM, D, 1);
     const uint64_t dq = smem_desc_sw128(sbase + C::kQOff, 16, 1024);
-    const uint64_t dk = smem_desc_sw128(sbase + C::kKOff, 16, 1024);
+    const uint64_t dk = smem_desc_sw128(sbase + C::kKOff, 16, C::kKGroupBytes);
     const uint64_t dp = smem_desc_sw128(sbase + C::kPOff, 16, 1024);
     const uint64_t dv = smem_desc_sw128(sbase + C::kVOff, kBlockSize * 128, 1024);
     // byte offset -> descriptor start-address field (16-byte units; no carry:
@@ -432,8 +433,10 @@ __global__ void __launch_bounds__(kPfThreads, 1)
       const uint64_t kb = adv(dk, w * C::kTileBytes);
 #pragma unroll
       for (int kk = 0; kk < D / 16; ++kk) {
-        const uint32_t koff = (kk >> 2) * C::kRegionBytes + (kk & 3) * 32;
-        tc_mma_f16(tmem + w * kTileN, adv(dq, koff), adv(kb, koff), kIdS, kk > 0);
+        // 16 columns: column half kk / 4 (a Q region, or 1 KB into a K group)
+        const uint32_t c32 = (kk & 3) * 32;
+        tc_mma_f16(tmem + w * kTileN, adv(dq, (kk >> 2) * C::kRegionBytes + c32),
+                   adv(kb, (kk >> 2) * 1024 + c32), kIdS, kk > 0);
       }
       tc_commit(bar(kSFull + w));
     };
@@ -745,11 +748,17 @@ cudaError_t launch_pf(const AttnParams& p, int num_sms, cudaStream_t stream) {
   }
   {
     const cuuint64_t hkv = static_cast<cuuint64_t>(p.num_kv_heads);
-    const cuuint64_t dims[4] = {static_cast<cuuint64_t>(D), hkv, static_cast<cuuint64_t>(kBlockSize),
-                                static_cast<cuuint64_t>(p.num_blocks)};
-    const cuuint64_t strides[3] = {D * e2, hkv * D * e2, kBlockSize * hkv * D * e2};
-    const cuuint32_t box[4] = {64, 1, static_cast<cuuint32_t>(kBlockSize), 1};
-    if (!encode_map(&maps.k, p.k_cache, 4, dims, strides, box)) return cudaErrorInvalidValue;
+    const cuuint64_t row = hkv * D * e2;  // bytes between a block's rows
+    // K: (64 columns, 8 rows, D/64 halves, 2 row groups, block x 16 x Hkv + head);
+    // the last index steps one head (D x 2 bytes), so a block's box for head
+    // g starts at block x 16 x Hkv + g and a block index past the pool reads
+    // out of bounds.  Coordinates are 32-bit.
+    const cuuint64_t kdims[5] = {64, 8, static_cast<cuuint64_t>(D / 64), 2,
+                                 static_cast<cuuint64_t>(p.num_blocks) * kBlockSize * hkv};
+    if (kdims[4] + hkv > 0x7fffffffull) return cudaErrorInvalidValue;
+    const cuuint64_t kstrides[4] = {row, 128, 8 * row, D * e2};
+    const cuuint32_t kbox[5] = {64, 8, static_cast<cuuint32_t>(D / 64), 2, 1};
+    if (!encode_map(&maps.k, p.k_cache, 5, kdims, kstrides, kbox)) return cudaErrorInvalidValue;
     // V: (64 columns, 16 rows, D/64 halves, kv head, block); the halves
     // dimension's stride (128 B) is below the rows' (Hkv x D x 2 B)
     const cuuint64_t vdims[5] = {64, static_cast<cuuint64_t>(kBlockSize),
