@@ -628,6 +628,26 @@ def run_gpu_arm(args):
     del pf
     torch.cuda.empty_cache()
 
+    # one long chunk: the tensor-core kernel in its steady state (56 KV tiles a unit)
+    pl = StepRunner("long_prefill_chunk", seed_offset=rank * 1000 if world > 1 else 0)
+    lms, _ = pl.time_device(max(3, args.steps // 2), args.warmup, world, flush=True)
+    lms = dist_max(lms, world)
+    pl_tflops = pl.work["chunk_flops"] / (lms * 1e-3) / 1e12
+    prefill_long_info = {
+        "workload": "one 2048-token prefill chunk at prior context 6144 (rows see up to 8192 "
+                    "keys), Llama-3-8B heads, bf16",
+        "ms_per_step": lms,
+        "tflops": pl_tflops,
+        "frac_of_bf16_peak": pl_tflops / bf16_peak[0] if bf16_peak[0] else None,
+        "peak_tflops": bf16_peak[0], "peak_source": bf16_peak[1],
+        "flops": pl.work["chunk_flops"],
+        "timed": "as prefill_chunks",
+    }
+    if int(pl.status.item()) != 0:
+        raise RuntimeError(f"long prefill device status {int(pl.status.item())}")
+    del pl
+    torch.cuda.empty_cache()
+
     # the headline shape over an 8-bit (E4M3) KV cache: half the KV bytes per token
     f8 = StepRunner(HEADLINE, seed_offset=rank * 1000 if world > 1 else 0, fp8_scales=(0.01, 0.01))
     fms, fdec = f8.time_device(args.steps, args.warmup, world)
@@ -681,6 +701,7 @@ def run_gpu_arm(args):
         "clocks": clock_info,
         "mixed": mixed_info,
         "prefill_chunks": prefill_info,
+        "prefill_long": prefill_long_info,
         "tinyllama_decode": small_info,
         "fp8_kv": fp8_info,
     }

@@ -151,12 +151,20 @@ def spec_long_context_decode(seed: int = 4) -> StepSpec:
                     num_blocks=int(9e9 // 65536), seed=seed)
 
 
+def spec_long_prefill_chunk(seed: int = 5) -> StepSpec:
+    """One 2048-token prefill chunk of a long prompt: prior context 6144, so
+    the chunk's rows see up to 8192 keys; Llama-3-8B heads, bf16."""
+    return StepSpec("long_prefill_chunk", "bf16", 32, 8, 128, np.array([2048], np.int64),
+                    np.array([8192], np.int64), seed=seed)
+
+
 CONFIGS = {
     "tiny_decode_f32": spec_tiny_decode_f32,
     "tinyllama_decode": spec_tinyllama_decode,
     "llama3_8b_decode": spec_llama3_8b_decode,
     "mixed_step": spec_mixed_step,
     "long_context_decode": spec_long_context_decode,
+    "long_prefill_chunk": spec_long_prefill_chunk,
 }
 
 

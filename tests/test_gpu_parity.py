@@ -77,6 +77,29 @@ def test_long_context_sampled_parity():
         del mk, mv
 
 
+def test_long_prefill_chunk_sampled_parity():
+    """One 2048-token chunk over 8192 keys (the tensor-core kernel's steady
+    state, as bench.py times it): the whole cache write is checked bit for
+    bit, attention on sampled (token, head) rows that the oracle evaluates
+    one by one (first and last rows of query tiles, every kv head)."""
+    spec = W.spec_long_prefill_chunk()
+    step = W.make_step(spec, device="cuda")
+    out, kc, vc, status = run_gpu(step)
+    assert status == 0
+    nb = oracle.blocks_needed(int(spec.seq_lens[0]))
+    blocks = torch.from_numpy(step.block_tables.cpu().numpy()[0, :nb].astype(np.int64)).cuda()
+    mk, mv = oracle.cache_write(bits(step.k), bits(step.v), step.slot_mapping.cpu().numpy(),
+                                bits(step.k_cache), bits(step.v_cache))
+    assert np.array_equal(bits(kc), mk) and np.array_equal(bits(vc), mv)
+    rows = [(0, 0), (31, 3), (32, 4), (1023, 17), (1024, 18), (2016, 26), (2047, 31), (777, 9)]
+    ref = oracle.paged_attention_rows(bits(step.q), mk[blocks.cpu().numpy()],
+                                      mv[blocks.cpu().numpy()], np.arange(nb)[None, :],
+                                      spec.seq_lens, np.array([0, 2048]), step.scale,
+                                      spec.num_kv_heads, rows)
+    got = torch.stack([out[t, h] for t, h in rows])
+    assert_close(got, ref, "bf16", "long prefill chunk")
+
+
 SHAPES = [
     # (q_lens, seq_lens): decode lengths at block edges, splits, chunks, a 1-token prompt
     ([1, 1, 1, 1, 1, 1], [1, 15, 16, 17, 300, 1000]),

@@ -67,6 +67,11 @@ def test_config_shapes():
     m5 = W.make_meta(s5)
     assert m5.unique_blocks <= 137329
 
+    s6 = W.spec_long_prefill_chunk()
+    m6 = W.make_meta(s6)
+    assert list(s6.q_lens) == [2048] and list(s6.seq_lens) == [8192]
+    assert list(m6.query_start_loc) == [0, 2048] and m6.unique_blocks == 512
+
 
 def test_tensors_and_nan_pool():
     spec = W.spec_tiny_decode_f32()
