@@ -176,6 +176,7 @@ WsLayout ws_layout(const Capacity& cap, int B, int Hkv, int D, int group) {
   w.tiles_p = take(sizeof(int4) * cap.prefill_tiles);
   w.recs_d = take(sizeof(UnitRec) * cap.decode_items);
   w.recs_s = take(sizeof(UnitRec) * cap.small_items);
+  w.order_d = take(sizeof(int) * cap.decode_items);
   w.cnt_d = take(sizeof(int) * cap.decode_tiles * Hkv);
   w.cnt_s = take(sizeof(int) * cap.small_tiles * Hkv);
   w.part_acc_d = take(sizeof(float) * cap.decode_items * Hkv * rows_d * D);
@@ -360,6 +361,7 @@ int pa_forward(const void* q, const void* k_cache, const void* v_cache,
   ap.next = hdr + kHdrDecodeNext;
   ap.items = reinterpret_cast<const int4*>(ws + lay.items_d);
   ap.recs = reinterpret_cast<const UnitRec*>(ws + lay.recs_d);
+  ap.order = reinterpret_cast<const int*>(ws + lay.order_d);
   ap.tiles = reinterpret_cast<const int4*>(ws + lay.tiles_d);
   ap.merge_cnt = reinterpret_cast<int*>(ws + lay.cnt_d);
   ap.part_acc = reinterpret_cast<float*>(ws + lay.part_acc_d);
@@ -377,6 +379,7 @@ int pa_forward(const void* q, const void* k_cache, const void* v_cache,
     ap.next = hdr + kHdrSmallNext;
     ap.items = reinterpret_cast<const int4*>(ws + lay.items_s);
     ap.recs = reinterpret_cast<const UnitRec*>(ws + lay.recs_s);
+    ap.order = nullptr;
     ap.tiles = reinterpret_cast<const int4*>(ws + lay.tiles_s);
     ap.merge_cnt = reinterpret_cast<int*>(ws + lay.cnt_s);
     ap.part_acc = reinterpret_cast<float*>(ws + lay.part_acc_s);

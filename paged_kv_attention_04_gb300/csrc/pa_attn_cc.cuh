@@ -100,8 +100,9 @@ __global__ void __launch_bounds__(CcCfg<T, D, G, P>::kThreads)
     __syncthreads();
     const int unit = s_unit;
     if (unit >= n_units) break;
-    const int item = unit / Hkv;
-    const int g = unit - item * Hkv;
+    const int k = unit / Hkv;
+    const int item = p.order ? __ldg(p.order + k) : k;
+    const int g = unit - k * Hkv;
     const int4 it = __ldg(p.items + item);
     const int r = it.x, m = it.y, tile = it.w;
     const int4 tinfo = __ldg(p.tiles + tile);

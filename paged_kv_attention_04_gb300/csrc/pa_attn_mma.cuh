@@ -185,13 +185,14 @@ __global__ void __launch_bounds__(MmaCfg<D, G, P, NW, NS, F8>::kThreads,
       if (lane == 0) m.valid = 0;
       return;
     }
-    const int item = u / Hkv;
+    const int k = u / Hkv;
+    const int item = p.order ? __ldg(p.order + k) : k;
     const UnitRec* rec = p.recs + item;
     const int4 ra = __ldg(&rec->a), rb = __ldg(&rec->b), rc = __ldg(&rec->c);
     const int32_t* row = p.block_tables + static_cast<long long>(ra.x) * p.max_blocks_per_seq;
     for (int i = lane; i < ra.w - ra.z; i += 32) m.bt[i] = __ldg(row + ra.z + i);
     if (lane == 0) {
-      m.valid = 1; m.item = item; m.g = u - item * Hkv; m.r = ra.x; m.a = rb.w; m.j0 = ra.y;
+      m.valid = 1; m.item = item; m.g = u - k * Hkv; m.r = ra.x; m.a = rb.w; m.j0 = ra.y;
       m.npos = rc.x; m.pos0 = rc.y; m.kv_hi = rc.z; m.b0 = ra.z; m.b1 = ra.w;
       m.tile = rb.x; m.first = rb.y; m.nsplit = rb.z;
     }

@@ -38,6 +38,7 @@ struct WsLayout {
   size_t hdr;
   size_t items_d, tiles_d, items_s, tiles_s, tiles_p;
   size_t recs_d, recs_s;  // per item: 3 x int4 unit records (see UnitRec)
+  size_t order_d;         // decode items in dispatch order (largest split first)
   size_t cnt_d, cnt_s;
   size_t part_acc_d, part_ml_d, part_acc_s, part_ml_s;
   size_t total;
@@ -88,6 +89,7 @@ struct AttnParams {
   int* next;             // device work counter (zeroed by the plan kernel)
   const int4* items;     // {r, m, first KV block, tile}
   const UnitRec* recs;   // per item, the same fully decoded
+  const int* order;      // dispatch order: the k-th item fetched is order[k] (null: k)
   const int4* tiles;     // {first item, number of splits, KV blocks per split, 0}
   int* merge_cnt;        // [tiles][num_kv_heads]
   float* part_acc;       // [items][num_kv_heads][rows][D]

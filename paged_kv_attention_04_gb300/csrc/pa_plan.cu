@@ -11,7 +11,11 @@
 // and writes the work lists the attention kernels consume, plus zeroed
 // per-tile split counters.  A decode or small tile whose KV is longer than
 // `bps` blocks is split into several items whose partial softmax states are
-// merged by the last item to finish.
+// merged by the last item to finish.  Decode items are handed out in a
+// dispatch order: items of at least half a split first, in request order
+// (short items among them would only add their fixed cost late), then the
+// shorter ones largest first (a counting sort by blocks), so the last units
+// the CTAs pick up are short and the step ends evenly.
 #include <climits>
 
 #include "pa_device.cuh"
@@ -23,7 +27,8 @@ namespace {
 
 constexpr int kPlanThreads = 1024;
 
-constexpr int kLists = 5;  // decode items, decode tiles, small items, small tiles, prefill tiles
+// decode items, decode tiles, small items, small tiles, prefill tiles, long decode items
+constexpr int kLists = 6;
 
 // Exclusive scan of kLists ints per thread across the CTA, all lists at once;
 // `total` receives each list's CTA total.
@@ -86,6 +91,8 @@ __global__ void __launch_bounds__(kPlanThreads, 1) plan_kernel(PlanParams p) {
   __shared__ int warp_sums[32][kLists];
   __shared__ int carry[kLists];
   __shared__ int err;
+  __shared__ int size_hist[kMaxUnitBlocks + 1];  // short decode items per size (blocks)
+  static_assert(kMaxUnitBlocks == 8 * 32, "the dispatch-order scan gives each lane 8 sizes");
   // the attention kernel that follows may become resident now; it waits for
   // this grid to finish before it reads the work lists.  This grid itself may
   // have started early (programmatic launch): wait for the previous kernel in
@@ -104,10 +111,12 @@ __global__ void __launch_bounds__(kPlanThreads, 1) plan_kernel(PlanParams p) {
   int* cnt_d = reinterpret_cast<int*>(ws + p.lay.cnt_d);
   int* cnt_s = reinterpret_cast<int*>(ws + p.lay.cnt_s);
   int4* tiles_p = reinterpret_cast<int4*>(ws + p.lay.tiles_p);
+  int* order_d = reinterpret_cast<int*>(ws + p.lay.order_d);
 
+  for (int i = threadIdx.x; i <= kMaxUnitBlocks; i += kPlanThreads) size_hist[i] = 0;
   if (threadIdx.x == 0) {
     err = 0;
-    for (int i = 0; i < 5; ++i) carry[i] = 0;
+    for (int i = 0; i < kLists; ++i) carry[i] = 0;
     const int q0 = __ldg(p.qsl), qB = __ldg(p.qsl + B);
     if (q0 != 0 || qB != p.num_tokens) err |= PA_DEV_QSL;
   }
@@ -116,11 +125,11 @@ __global__ void __launch_bounds__(kPlanThreads, 1) plan_kernel(PlanParams p) {
   // One pass: classify and count, exclusive-scan the counts across the CTA,
   // and let each request's thread write its own items and tiles at its
   // offsets (every write checked against the list's capacity).
-  int carry_r[kLists] = {0, 0, 0, 0, 0};
+  int carry_r[kLists] = {0, 0, 0, 0, 0, 0};
   for (int base = 0; base < B; base += kPlanThreads) {
     const int r = base + threadIdx.x;
     int c = kClassNone;
-    int cnt[kLists] = {0, 0, 0, 0, 0};
+    int cnt[kLists] = {0, 0, 0, 0, 0, 0};
     int S = 0, a = 0, L = 0;
     if (r < B) {
       S = __ldg(p.seq_lens + r);
@@ -137,7 +146,10 @@ __global__ void __launch_bounds__(kPlanThreads, 1) plan_kernel(PlanParams p) {
       } else if (L == 1) {
         c = kClassDecode;
         cnt[1] = 1;
-        cnt[0] = splits_for(S - 1, request_bps(ceil_div(S, kBlockSize), p.bps));
+        const int nb = ceil_div(S, kBlockSize), rb = request_bps(nb, p.bps);
+        cnt[0] = splits_for(S - 1, rb);
+        // long items: every full split, and the last one if it is at least half a split
+        cnt[5] = cnt[0] - 1 + (2 * (nb - (cnt[0] - 1) * rb) >= p.bps ? 1 : 0);
       } else if (L >= p.prefill_min_qlen) {
         c = kClassPrefill;
         cnt[4] = ceil_div(L, p.prefill_rows / p.group);
@@ -169,6 +181,10 @@ __global__ void __launch_bounds__(kPlanThreads, 1) plan_kernel(PlanParams p) {
         if (i >= p.cap.decode_items) break;
         items_d[i] = make_int4(r, 0, s * rb, tile);
         const int b0 = s * rb, b1 = min(b0 + rb, nb);
+        // long items take dispatch slots in request order (they are a prefix
+        // of the request's splits, and off[5] + s <= i); short ones are counted
+        if (s < cnt[5]) order_d[off[5] + s] = i;
+        else atomicAdd(&size_hist[b1 - b0], 1);
         recs_d[i].a = make_int4(r, 0, b0, b1);
         recs_d[i].b = make_int4(tile, off[0], ns, a);
         recs_d[i].c = make_int4(1, S - 1, min(b1 * kBlockSize, S), 0);
@@ -224,6 +240,38 @@ __global__ void __launch_bounds__(kPlanThreads, 1) plan_kernel(PlanParams p) {
     return;
   }
   const int n_di = carry[0], n_dt = carry[1], n_si = carry[2], n_st = carry[3], n_pt = carry[4];
+  // dispatch order (it does not change results: partial states are stored
+  // and merged by item, in split order).  The long items took the first
+  // n_long slots above; short items: exclusive scan of the size histogram
+  // from the largest size down (each bucket's first slot), then every short
+  // item takes the next slot of its bucket
+  const int n_long = carry[5];
+  if (threadIdx.x < 32) {
+    const int lane = threadIdx.x;
+    int tot = 0;
+#pragma unroll
+    for (int j = 0; j < 8; ++j) tot += size_hist[kMaxUnitBlocks - (8 * lane + j)];
+    int incl = tot;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int y = __shfl_up_sync(0xffffffffu, incl, o);
+      if (lane >= o) incl += y;
+    }
+    int run = n_long + incl - tot;
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      const int sz = kMaxUnitBlocks - (8 * lane + j);
+      const int c = size_hist[sz];
+      size_hist[sz] = run;
+      run += c;
+    }
+  }
+  __syncthreads();
+  for (int i = threadIdx.x; i < n_di; i += kPlanThreads) {
+    // short = under half a split (full splits hold at least bps blocks)
+    const int4 a = recs_d[i].a;  // written above by this CTA
+    if (2 * (a.w - a.z) < p.bps) order_d[atomicAdd(&size_hist[a.w - a.z], 1)] = i;
+  }
   for (int i = threadIdx.x; i < n_dt * p.num_kv_heads; i += kPlanThreads) cnt_d[i] = 0;
   for (int i = threadIdx.x; i < n_st * p.num_kv_heads; i += kPlanThreads) cnt_s[i] = 0;
   if (threadIdx.x == 0) {
