@@ -18,15 +18,18 @@
 //     unit's keys read out of bounds, which fills zeros.  Each unit starts at
 //     a different KV tile (rotated by its query tile), so the CTAs that share
 //     a kv head do not read the same lines at the same time;
-//   * warp 9 (MMA): one thread issues S = Q K^T and O += P V as
-//     tcgen05.mma.kind::f16 (bf16 in, fp32 accumulate in tensor memory);
-//   * warps 0-3 and 4-7: two softmax warpgroups.  Warpgroup w takes the KV
-//     tiles t = w, w + 2, ... of the unit, with its own K, V and P buffers and
-//     its own S and O in tensor memory, so one group's softmax runs while the
-//     tensor cores serve the other.  Thread i owns query row i = TMEM lane i;
-//     the running maximum moves only when a row's maximum grows by more than
-//     2^8 (base-2 logits), so O is rescaled rarely.  At the end of the unit
-//     the two partial states (m, l, O) are merged (log-sum-exp) and written.
+//   * warp 9 (MMA): one thread issues S = Q K^T (both operands in shared
+//     memory) and O += P V (P in tensor memory) as tcgen05.mma.kind::f16
+//     (bf16 in, fp32 accumulate in tensor memory); S is double-buffered, so
+//     S of tile t + 1 is computed while the softmax works on tile t;
+//   * warps 0-3 and 4-7: two softmax warpgroups that share every tile:
+//     warpgroup w takes its keys 64w .. 64w + 63, thread i owns query row i
+//     = TMEM lane i.  The two threads of a row trade their half maxima, so
+//     both scale by one running maximum, which moves only when the row's
+//     maximum grows by more than 2^8 (base-2 logits): O is rescaled rarely.
+//     Each writes its half of P (bf16) over the first half of the tile's S,
+//     which both have read by then.  At the end of the unit the two halves'
+//     row sums are added and each warpgroup writes half of O's columns.
 // Hand-offs are mbarriers; every wait is bounded and a timeout makes the whole
 // CTA stop (status PA_DEV_TIMEOUT), drain its copies and MMAs, and free TMEM.
 #include <cuda.h>
@@ -57,7 +60,6 @@ template <int D>
 struct PfCfg {
   static constexpr int kRegionBytes = kTileM * 128;     // 128 rows x 64 bf16
   static constexpr int kTileBytes = kTileM * D * 2;     // Q, K or V tile
-  static constexpr int kPBytes = kTileM * kTileN * 2;   // P tile
   static constexpr int kQOff = 0;
   static constexpr int kKOff = kQOff + kTileBytes;      // K0, K1
   static constexpr int kVOff = kKOff + 2 * kTileBytes;  // V0, V1
@@ -68,34 +70,36 @@ struct PfCfg {
   //   V [block][64-column half][16 rows][128 B] (MN-major operand of P V).
   static constexpr int kVBlockBytes = kBlockSize * 128 * (D / 64);
   static constexpr int kKGroupBytes = 8 * 128 * (D / 64);
-  static constexpr int kPOff = kVOff + 2 * kTileBytes;  // P0, P1
-  static constexpr int kSmemBytes = kPOff + 2 * kPBytes + 1024;  // + alignment slack
-  static constexpr int kTmemCols = 512;  // S0, S1 at 0 / 128; O0, O1 at 256 / 384
+  static constexpr int kSmemBytes = kVOff + 2 * kTileBytes + 1024;  // + alignment slack
+  // S0, S1 (consecutive tiles) at 0 / 128, each tile's P (bf16 pairs) over the
+  // first 64 columns of its S once read; O at 256
+  static constexpr int kTmemCols = 512;
   static_assert(D == 64 || D == 128, "head size 64 or 128");
   static_assert(kTileN == kTileM, "K and V tiles share the Q tile geometry");
   static_assert(kSmemBytes <= 227 * 1024, "shared memory per CTA exceeds 227 KB");
 };
 
-// mbarriers.  [2] = one per softmax warpgroup (or ring slot).  The MMA warp
-// waits once per KV tile t: kGo gathers everything O += P V over t and
-// S = Q K^T over t + 2 (same group, same buffers) need, so the tensor cores
-// are not left idle between hand-offs.
+// mbarriers.  [2] = one per buffer parity (tile t uses buffers t & 1 of S,
+// K, V and P) or per unit slot.  The MMA warp waits once per KV tile t:
+// kGo gathers everything O += P V over t and S = Q K^T over t + 2 (same
+// buffers) need, so the tensor cores are not left idle between hand-offs.
 enum Bar : int {
   kUnitFull = 0,    // [2] unit info published (loader)
   kUnitEmpty = 2,   // [2] unit info read (8 softmax warps, MMA warp, V loader)
   kQFull = 4,       // Q tile landed (TMA)
   kQEmpty = 5,      // every S of the unit done (MMA commit)
-  kKFirst = 6,      // [2] the unit's first K tile of the group landed (TMA)
+  kKFirst = 6,      // [2] the unit's first two K tiles landed (TMA)
   kSFull = 8,       // [2] S = Q K^T done (MMA commit); also frees the K buffer
-  kGo = 10,         // [2] tile t: P written and S read (4 softmax warps), V of t landed
+  kGo = 10,         // [2] tile t: P written and S read (8 softmax warps), V of t landed
                     //     (V loader), K of t + 2 landed or none due (K loader)
   kVLand = 12,      // [2] V tile landed, for a tile whose last block the V loader trims
-  kPVDone = 14,     // [2] O += P V done (MMA commit); frees V and P, O stable
-  kMlFull = 16,     // row (m, l) of both groups published (8 warps)
-  kMlRead = 17,     // ... and read (8 warps)
-  kOFree = 18,      // O of both groups read by the epilogue (8 warps)
-  kDrain = 19,      // teardown after a timeout
-  kNumBars = 20
+  kPVDone = 14,     // [2] O += P V done (MMA commit); frees V and P
+  kMx = 16,         // [2] both halves of each row published their maximum (8 warps)
+  kMlFull = 18,     // row sums of both halves published (8 warps)
+  kMlRead = 19,     // ... and read (8 warps)
+  kOFree = 20,      // O read by the epilogue (8 warps)
+  kDrain = 21,      // teardown after a timeout
+  kNumBars = 22
 };
 
 struct UnitInfo {
@@ -115,12 +119,6 @@ struct PfMaps {
                   // box (64, 8, D/64, 2, 1) at block x 16 x Hkv + head
   CUtensorMap v;  // v_cache as 5-D (64, 16 rows, D/64 halves, Hkv, NB), box (64, 16, D/64, 1, 1)
 };
-
-// Byte offset of 16-byte chunk c of row r in a 128-byte-swizzled tile whose
-// 64-element column groups are stacked regions of 128 rows x 128 bytes.
-__device__ __forceinline__ uint32_t sw128(int r, int c) {
-  return static_cast<uint32_t>((c >> 3) * (kTileM * 128) + r * 128 + (((c & 7) ^ (r & 7)) << 4));
-}
 
 // max of three floats in one instruction (NaN-free operands here)
 __device__ __forceinline__ float max3(float a, float b, float c) {
@@ -174,8 +172,8 @@ __device__ __forceinline__ bool wait_bar(uint32_t bar, uint32_t parity, volatile
 // Arrivals that complete a phase of each barrier.
 __device__ __forceinline__ uint32_t bar_count(int i) {
   if (i == kUnitEmpty || i == kUnitEmpty + 1) return 10;  // 8 softmax warps, MMA, V loader
-  if (i == kGo || i == kGo + 1) return 6;  // 4 softmax warps, V loader, K loader
-  if (i == kMlFull || i == kMlRead || i == kOFree) return 8;
+  if (i == kGo || i == kGo + 1) return 10;  // 8 softmax warps, V loader, K loader
+  if (i == kMx || i == kMx + 1 || i == kMlFull || i == kMlRead || i == kOFree) return 8;
   return 1;  // TMA (arrive + bytes) or tcgen05.commit
 }
 
@@ -212,6 +210,8 @@ __global__ void __launch_bounds__(kPfThreads, 1)
   __shared__ __align__(8) uint64_t bars[kNumBars];
   __shared__ UnitInfo s_units[2];
   __shared__ uint32_t s_tmem;
+  __shared__ float s_mx[2][2][kTileM];  // [buffer][column half][row]: half-row maxima
+  __shared__ float s_ml[2][kTileM];     // [column half][row]: row sums at the unit's end
   __shared__ int s_abort;
 
   unsigned char* smem = reinterpret_cast<unsigned char*>(
@@ -423,7 +423,6 @@ __global__ void __launch_bounds__(kPfThreads, 1)
     constexpr uint32_t kIdPV = idesc_bf16(kTileM, D, 1);
     const uint64_t dq = smem_desc_sw128(sbase + C::kQOff, 16, 1024);
     const uint64_t dk = smem_desc_sw128(sbase + C::kKOff, 16, C::kKGroupBytes);
-    const uint64_t dp = smem_desc_sw128(sbase + C::kPOff, 16, 1024);
     const uint64_t dv = smem_desc_sw128(sbase + C::kVOff, kBlockSize * 128, 1024);
     // byte offset -> descriptor start-address field (16-byte units; no carry:
     // shared addresses stay below 2^18)
@@ -440,16 +439,17 @@ __global__ void __launch_bounds__(kPfThreads, 1)
       }
       tc_commit(bar(kSFull + w));
     };
-    // O += P V of group w's tile (P and V buffers w); first: O is overwritten
+    // O += P V of a tile: P (bf16 pairs, 8 columns per 16 keys) in the first
+    // 64 columns of S buffer w, V in buffer w; first: O is overwritten
     auto mma_pv = [&](int w, bool first) {
-      const uint64_t pb = adv(dp, w * C::kPBytes), vb = adv(dv, w * C::kTileBytes);
+      const uint64_t vb = adv(dv, w * C::kTileBytes);
 #pragma unroll
       for (int kk = 0; kk < kTileN / 16; ++kk)
-        tc_mma_f16(tmem + 256 + w * 128, adv(pb, (kk >> 2) * C::kRegionBytes + (kk & 3) * 32),
-                   adv(vb, kk * C::kVBlockBytes), kIdPV, (first && kk == 0) ? 0u : 1u);
+        tc_mma_f16_ts(tmem + 256, tmem + w * kTileN + kk * 8, adv(vb, kk * C::kVBlockBytes), kIdPV,
+                      (first && kk == 0) ? 0u : 1u);
       tc_commit(bar(kPVDone + w));
     };
-    uint32_t g0 = 0, g1 = 0;    // tiles per group so far (kGo phases)
+    uint32_t g0 = 0, g1 = 0;    // tiles per buffer parity so far (kGo phases)
     uint32_t nf0 = 0, nf1 = 0;  // first-K copies per group so far
     bool ok = true;
     for (int uc = 0; ok; ++uc) {
@@ -479,9 +479,9 @@ __global__ void __launch_bounds__(kPfThreads, 1)
         if (lane == 0) tc_commit(bar(kQEmpty));
         __syncwarp();
       }
-      // PV(t) goes before S(t + 2): when a group's next S is done, so is its
-      // previous PV (a commit covers every earlier MMA), so its softmax never
-      // waits for P or O to be free; the other group keeps the tensor cores busy
+      // PV(t) goes before S(t + 2), which overwrites the P that PV(t) reads
+      // (the tensor cores run one thread's MMAs in order); S(t + 1) is
+      // computed while the softmax works on t
       for (int t = 0; t < nkv; ++t) {
         const int w = t & 1;
         const uint32_t g = w ? g1 : g0;
@@ -493,7 +493,7 @@ __global__ void __launch_bounds__(kPfThreads, 1)
         }
         tc_fence_after();
         if (lane == 0) {
-          mma_pv(w, t < 2);
+          mma_pv(w, t == 0);
           if (t + 2 < nkv) {
             mma_s(w);
             if (t + 2 == nkv - 1) tc_commit(bar(kQEmpty));
@@ -511,16 +511,19 @@ __global__ void __launch_bounds__(kPfThreads, 1)
     __syncwarp();
   } else {
     // ------------------------------------------------------------ softmax
-    const int w = warp >> 2;       // warpgroup
+    // Warpgroup w takes keys 64w .. 64w + 63 of every tile; thread i owns
+    // query row i = TMEM lane i.  The two threads of a row trade their half
+    // maxima through shared memory (kMx), so both use one running maximum
+    // and their P halves, O and the row sums share one scale.
+    const int w = warp >> 2;       // warpgroup = column half
     const int i = tid & 127;       // query row = TMEM lane
     const uint32_t lane_off = static_cast<uint32_t>((warp & 3) * 32) << 16;
-    const uint32_t tmem_s = tmem + w * kTileN + lane_off;
-    const uint32_t tmem_o0 = tmem + 256 + lane_off, tmem_o1 = tmem + 384 + lane_off;
+    const uint32_t tmem_o = tmem + 256 + lane_off;
+    constexpr int kOCols = D / 2;  // O columns this group rescales and writes
     const float sl2 = p.scale_log2;
     const int Hq = p.num_q_heads;
     __nv_bfloat16* out = static_cast<__nv_bfloat16*>(p.out);
-    const uint32_t pbuf = sbase + C::kPOff + w * C::kPBytes;
-    uint32_t n = 0;  // this group's tiles so far (all units)
+    uint32_t nb0 = 0, nb1 = 0;  // tiles per buffer parity so far (all units)
     for (int uc = 0;; ++uc) {
       const int slot = uc & 1;
       if (!wait_bar(bar(kUnitFull + slot), (uc >> 1) & 1, abort, p.status)) break;
@@ -530,141 +533,128 @@ __global__ void __launch_bounds__(kPfThreads, 1)
       const int jj = i / G;
       const bool row_ok = jj < u.npos;
       const int my_pos = u.pos0 + jj;
-      float m_used = -CUDART_INF_F, l_sum = 0.f;
+      float m_used = -CUDART_INF_F, l_part = 0.f;
       bool ok = true;
-      for (int t = w; t < u.n_kv; t += 2, ++n) {  // t: place in the unit's order
+      for (int t = 0; t < u.n_kv; ++t) {  // t: place in the unit's order
+        const int b = t & 1;
+        const uint32_t nb = b ? nb1 : nb0;  // uses of buffer b so far
         const int kt = tile_of(u, t);
-        const int tok0 = kt * kTileN;
-        // S of this tile was issued after the group's previous PV, and a
-        // commit covers every earlier MMA: P and O are free as well
-        if (!wait_bar(bar(kSFull + w), n & 1, abort, p.status)) { ok = false; break; }
+        const int key0 = kt * kTileN + w * 64;  // first key of this half
+        const uint32_t tmem_s = tmem + b * kTileN + lane_off;
+        if (!wait_bar(bar(kSFull + b), nb & 1, abort, p.status)) { ok = false; break; }
         tc_fence_after();
 
-        // causal edge (or a padding row): keys c > lim are masked
-        const bool masked = tok0 + kTileN - 1 > u.pos0 || !row_ok;
-        const int lim = row_ok ? my_pos - tok0 : -1;
-        const float mul = masked ? 1.f : sl2;  // turns what load_half leaves into base-2 logits
-        // 64 keys of the S row -> registers; returns their maximum base-2 logit
-        auto load_half = [&](int h, uint32_t* sr) {
-          PA_TMEM_LD32(tmem_s + h * 64, sr);
-          PA_TMEM_LD32(tmem_s + h * 64 + 32, (sr + 32));
-          tmem_wait_ld();
+        // 64 keys of the S row -> registers, masked (causal edge or padding
+        // row: keys past lim) and turned into base-2 logits there
+        const bool masked = key0 + 63 > u.pos0 || !row_ok;
+        const int lim = row_ok ? my_pos - key0 : -1;
+        const float mul = masked ? 1.f : sl2;
+        uint32_t sr[64];
+        PA_TMEM_LD32(tmem_s + w * 64, sr);
+        PA_TMEM_LD32(tmem_s + w * 64 + 32, (sr + 32));
+        tmem_wait_ld();
+        float mx;
+        {
           float m4[4];
           if (masked) {
 #pragma unroll
             for (int e = 0; e < 4; ++e) m4[e] = -CUDART_INF_F;
 #pragma unroll
             for (int c = 0; c < 64; ++c) {
-              const float x = h * 64 + c <= lim ? __uint_as_float(sr[c]) * sl2 : -CUDART_INF_F;
+              const float x = c <= lim ? __uint_as_float(sr[c]) * sl2 : -CUDART_INF_F;
               sr[c] = __float_as_uint(x);
               m4[c & 3] = fmaxf(m4[c & 3], x);
             }
-            return fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3]));
-          }
+            mx = fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3]));
+          } else {
 #pragma unroll
-          for (int e = 0; e < 4; ++e) m4[e] = __uint_as_float(sr[e]);
-          if (sl2 >= 0.f) {
+            for (int e = 0; e < 4; ++e) m4[e] = __uint_as_float(sr[e]);
+            if (sl2 >= 0.f) {
 #pragma unroll
-            for (int c = 4; c < 64; c += 2)
-              m4[(c >> 1) & 3] = max3(m4[(c >> 1) & 3], __uint_as_float(sr[c]), __uint_as_float(sr[c + 1]));
-            return fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3])) * sl2;
-          }
+              for (int c = 4; c < 64; c += 2)
+                m4[(c >> 1) & 3] = max3(m4[(c >> 1) & 3], __uint_as_float(sr[c]), __uint_as_float(sr[c + 1]));
+              mx = fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3])) * sl2;
+            } else {
 #pragma unroll
-          for (int c = 4; c < 64; c += 2)
-            m4[(c >> 1) & 3] = min3(m4[(c >> 1) & 3], __uint_as_float(sr[c]), __uint_as_float(sr[c + 1]));
-          return fminf(fminf(m4[0], m4[1]), fminf(m4[2], m4[3])) * sl2;
-        };
-        // P = exp2(logit - m) as bf16 for 64 keys, stored 8 keys (16 bytes) at a time
-        auto emit_half = [&](int h, const uint32_t* sr, float m_sub) {
-          float ps4[4] = {0.f, 0.f, 0.f, 0.f};  // two packed pair sums
-#pragma unroll
-          for (int c = 0; c < 8; ++c) {
-            uint32_t pw[4];
-#pragma unroll
-            for (int e = 0; e < 4; ++e) {
-              float x0, x1;
-              fma2(x0, x1, __uint_as_float(sr[8 * c + 2 * e]), __uint_as_float(sr[8 * c + 2 * e + 1]),
-                   mul, -m_sub);
-              const float p0 = ex2(x0), p1 = ex2(x1);
-              add2(ps4[2 * (e & 1)], ps4[2 * (e & 1) + 1], p0, p1);
-              pw[e] = pack_bf16(p0, p1);
+              for (int c = 4; c < 64; c += 2)
+                m4[(c >> 1) & 3] = min3(m4[(c >> 1) & 3], __uint_as_float(sr[c]), __uint_as_float(sr[c + 1]));
+              mx = fminf(fminf(m4[0], m4[1]), fminf(m4[2], m4[3])) * sl2;
             }
-            asm volatile("st.shared.v4.b32 [%0], {%1,%2,%3,%4};\n" ::"r"(pbuf + sw128(i, h * 8 + c)),
-                         "r"(pw[0]), "r"(pw[1]), "r"(pw[2]), "r"(pw[3])
-                         : "memory");
           }
-          return (ps4[0] + ps4[1]) + (ps4[2] + ps4[3]);
-        };
-        float factor = 1.f;  // this tile's rescale of the row's earlier state
-        bool moved_late = false;
+        }
+        // the row's maximum over the whole tile: trade halves with the partner
+        // thread (both have read their S by then, so P may overwrite it after)
+        s_mx[b][w][i] = mx;
+        warp_arrive(bar(kMx + b));
+        if (!wait_bar(bar(kMx + b), nb & 1, abort, p.status)) { ok = false; break; }
+        mx = fmaxf(mx, s_mx[b][w ^ 1][i]);
+        float f = 1.f;  // this tile's rescale of the row's earlier state
+        if (mx > m_used + kRescaleThreshold) {
+          f = ex2(m_used - mx);  // 0 while the row had no visible key
+          l_part *= f;
+          m_used = mx;
+        }
+        // P = exp2(logit - m) as bf16 pairs into columns 32w .. 32w + 31 of S
+        // buffer b (keys 64w .. 64w + 63 of the tile)
+        {
+          const float m_sub = m_used == -CUDART_INF_F ? 0.f : m_used;
+          float ps4[4] = {0.f, 0.f, 0.f, 0.f};  // two packed pair sums
+          uint32_t pw[32];
 #pragma unroll
-        for (int h = 0; h < 2; ++h) {
-          uint32_t sr[64];
-          const float mx = load_half(h, sr);
-          if (mx > m_used + kRescaleThreshold) {
-            const float f = ex2(m_used - mx);  // 0 while the row had no visible key
-            l_sum *= f;
-            factor *= f;
-            moved_late = h == 1 && f > 0.f;  // half 0's P used the old maximum
-            m_used = mx;
+          for (int c = 0; c < 32; ++c) {
+            float x0, x1;
+            fma2(x0, x1, __uint_as_float(sr[2 * c]), __uint_as_float(sr[2 * c + 1]), mul, -m_sub);
+            const float p0 = ex2(x0), p1 = ex2(x1);
+            add2(ps4[2 * (c & 1)], ps4[2 * (c & 1) + 1], p0, p1);
+            pw[c] = pack_bf16(p0, p1);
           }
-          l_sum += emit_half(h, sr, m_used == -CUDART_INF_F ? 0.f : m_used);
+          PA_TMEM_ST32(tmem_s + w * 32, pw);
+          l_part += (ps4[0] + ps4[1]) + (ps4[2] + ps4[3]);
         }
-        if (__any_sync(0xffffffffu, moved_late)) {
-          // rare: redo half 0's P with the new maximum (its sum is already rescaled)
-          uint32_t sr[64];
-          load_half(0, sr);
-          emit_half(0, sr, m_used == -CUDART_INF_F ? 0.f : m_used);
-        }
-
-        // rescale O rows whose maximum moved (not on the group's first tile of
-        // the unit: its PV overwrites O)
-        if (t >= 2 && __any_sync(0xffffffffu, factor != 1.f)) {
-          const uint32_t tmem_o = w ? tmem_o1 : tmem_o0;
+        // rescale this group's O columns in rows whose maximum moved, once
+        // PV(t - 1) is done (not on the unit's first tile: PV(0) overwrites O)
+        if (t > 0 && __any_sync(0xffffffffu, f != 1.f)) {
+          const int pb = b ^ 1;
+          const uint32_t npv = (pb ? nb1 : nb0) - 1;  // PV(t - 1) is that buffer's last use
+          if (!wait_bar(bar(kPVDone + pb), npv & 1, abort, p.status)) { ok = false; break; }
+          tc_fence_after();
 #pragma unroll
-          for (int c0 = 0; c0 < D; c0 += 32) {
+          for (int c0 = 0; c0 < kOCols; c0 += 32) {
             uint32_t o[32];
-            PA_TMEM_LD32(tmem_o + c0, o);
+            PA_TMEM_LD32(tmem_o + w * kOCols + c0, o);
             tmem_wait_ld();
 #pragma unroll
-            for (int j = 0; j < 32; ++j) o[j] = __float_as_uint(__uint_as_float(o[j]) * factor);
-            PA_TMEM_ST32(tmem_o + c0, o);
+            for (int j = 0; j < 32; ++j) o[j] = __float_as_uint(__uint_as_float(o[j]) * f);
+            PA_TMEM_ST32(tmem_o + w * kOCols + c0, o);
           }
           tmem_wait_st();
         }
-        fence_proxy_async_smem();
+        tmem_wait_st();  // P (and O) stores complete
         tc_fence_before();
-        warp_arrive(bar(kGo + w));  // S read, P written, O rescaled
+        warp_arrive(bar(kGo + b));  // S read, P written, O rescaled
+        if (b) ++nb1; else ++nb0;
       }
       if (!ok) break;
 
-      // ---- merge the two groups' (m, l, O) and write this group's half of the columns
-      const int n_mine = (u.n_kv + 1 - w) / 2;
-      if (n_mine > 0 && !wait_bar(bar(kPVDone + w), (n - 1) & 1, abort, p.status)) break;
+      // ---- both halves' row sums, then this group's half of the O columns
+      {
+        const int lb = (u.n_kv - 1) & 1;  // buffer of the last tile: its PV covers all
+        const uint32_t npv = (lb ? nb1 : nb0) - 1;
+        if (!wait_bar(bar(kPVDone + lb), npv & 1, abort, p.status)) break;
+      }
       tc_fence_after();
-      float* ml_mine = reinterpret_cast<float*>(smem + C::kPOff + w * C::kPBytes);
-      const float* ml_other = reinterpret_cast<const float*>(smem + C::kPOff + (w ^ 1) * C::kPBytes);
-      ml_mine[2 * i] = m_used;
-      ml_mine[2 * i + 1] = l_sum;
+      s_ml[w][i] = l_part;
       warp_arrive(bar(kMlFull));
       if (!wait_bar(bar(kMlFull), uc & 1, abort, p.status)) break;
-      const float m_o = ml_other[2 * i], l_o = ml_other[2 * i + 1];
+      const float l_sum = l_part + s_ml[w ^ 1][i];
       warp_arrive(bar(kMlRead));
-      const float m0 = w ? m_o : m_used, l0 = w ? l_o : l_sum;
-      const float m1 = w ? m_used : m_o, l1 = w ? l_sum : l_o;
-      const float m = fmaxf(m0, m1);
-      const float f0 = m0 == -CUDART_INF_F ? 0.f : ex2(m0 - m);
-      const float f1 = m1 == -CUDART_INF_F ? 0.f : ex2(m1 - m);
-      const float inv = p.out_scale / (l0 * f0 + l1 * f1);
-      const bool has1 = u.n_kv > 1;  // group 1 had a tile: O1 holds this unit's data
-      tc_fence_after();
+      const float inv = p.out_scale / l_sum;
       const long long tok = u.a + u.j0 + jj;
       __nv_bfloat16* orow = out + (tok * Hq + u.g * G + (i - jj * G)) * D;
 #pragma unroll
-      for (int c0 = w * (D / 2); c0 < (w + 1) * (D / 2); c0 += 32) {
-        uint32_t o0[32], o1[32];
-        PA_TMEM_LD32(tmem_o0 + c0, o0);
-        if (has1) PA_TMEM_LD32(tmem_o1 + c0, o1);
+      for (int c0 = w * kOCols; c0 < (w + 1) * kOCols; c0 += 32) {
+        uint32_t o[32];
+        PA_TMEM_LD32(tmem_o + c0, o);
         tmem_wait_ld();
         if (row_ok) {
           uint4* dst = reinterpret_cast<uint4*>(orow + c0);
@@ -672,10 +662,7 @@ __global__ void __launch_bounds__(kPfThreads, 1)
           for (int j = 0; j < 4; ++j) {
             float v[8];
 #pragma unroll
-            for (int e = 0; e < 8; ++e) {
-              const float a0 = __uint_as_float(o0[8 * j + e]) * f0;
-              v[e] = (has1 ? fmaf(__uint_as_float(o1[8 * j + e]), f1, a0) : a0) * inv;
-            }
+            for (int e = 0; e < 8; ++e) v[e] = __uint_as_float(o[8 * j + e]) * inv;
             dst[j] = make_uint4(pack_bf16(v[0], v[1]), pack_bf16(v[2], v[3]),
                                 pack_bf16(v[4], v[5]), pack_bf16(v[6], v[7]));
           }
@@ -683,7 +670,7 @@ __global__ void __launch_bounds__(kPfThreads, 1)
       }
       tc_fence_before();
       warp_arrive(bar(kOFree));
-      // nobody writes P (where the (m, l) pairs sit) before both groups read them
+      // neither group publishes its next unit's row sum before both read these
       if (!wait_bar(bar(kMlRead), uc & 1, abort, p.status)) break;
     }
   }
