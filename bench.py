@@ -443,39 +443,50 @@ class StepRunner:
     def time_device(self, steps: int, warmup: int, world: int, clocks: ClockSampler | None = None,
                     flush: bool = False):
         """Inputs resident in HBM; returns (ms per step, decode-kernel ms per launch).
-        With flush, L2 is flushed before every step, outside the timed events."""
+        The steps are timed in one loop with no events inside a step; the decode
+        kernel is timed in a second loop with events around it (those events sit
+        between the plan and the decode kernel, so they would cost the step its
+        launch overlap).  With flush, L2 is flushed before every step, outside the
+        timed events."""
         torch, P = self.torch, self.P
         for _ in range(warmup):
             self.step()
         torch.cuda.synchronize()
-        evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-               for _ in range(steps)]
-        steps_ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-                    for _ in range(steps if flush else 1)]
-        barrier(world)
-        torch.cuda.synchronize()
+
+        def loop(kernel_events):
+            evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+                   for _ in range(steps)]
+            steps_ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+                        for _ in range(steps if flush else 1)]
+            barrier(world)
+            torch.cuda.synchronize()
+            if not flush:
+                steps_ev[0][0].record()
+            for i in range(steps):
+                if flush:
+                    self.flush_l2()
+                    steps_ev[i][0].record()
+                if kernel_events:
+                    P.pa_set_profile_events(evs[i][0], evs[i][1])
+                self.step()
+                if flush:
+                    steps_ev[i][1].record()
+            if not flush:
+                steps_ev[0][1].record()
+            torch.cuda.synchronize()
+            barrier(world)
+            P.pa_set_profile_events(None, None)
+            if kernel_events:
+                return statistics.mean(a.elapsed_time(b) for a, b in evs)
+            return sum(a.elapsed_time(b) for a, b in steps_ev) / steps
+
         if clocks:
             clocks.mark("timed_start")
-        if not flush:
-            steps_ev[0][0].record()
-        for i in range(steps):
-            if flush:
-                self.flush_l2()
-                steps_ev[i][0].record()
-            P.pa_set_profile_events(evs[i][0], evs[i][1])
-            self.step()
-            if flush:
-                steps_ev[i][1].record()
-        if not flush:
-            steps_ev[0][1].record()
-        torch.cuda.synchronize()
+        step_ms = loop(False)
         if clocks:
             clocks.mark("timed_end")
-        barrier(world)
-        P.pa_set_profile_events(None, None)
-        total_ms = sum(a.elapsed_time(b) for a, b in steps_ev)
-        dec_ms = statistics.mean(a.elapsed_time(b) for a, b in evs)
-        return total_ms / steps, dec_ms
+        dec_ms = loop(True)
+        return step_ms, dec_ms
 
     def time_graph(self, steps: int, warmup: int, world: int, flush: bool = False) -> float:
         """The same step captured once in a CUDA graph and replayed; ms per step

@@ -100,6 +100,27 @@ def test_long_prefill_chunk_sampled_parity():
     assert_close(got, ref, "bf16", "long prefill chunk")
 
 
+def test_prefill_runs_are_bit_identical():
+    """Chunks of 16 to 1000 tokens over contexts up to 3000 keys: ~450 tensor-core
+    units, several per CTA, so every hand-off between the kernel's roles is
+    crossed many times, including at unit boundaries.  Three runs must give the
+    same bits (the kernel has no order-dependent arithmetic), and the first must
+    match the oracle."""
+    spec = W.custom_spec("pf-det", "bf16", 32, 8, 128, [16, 100, 513, 40, 1000, 1],
+                         [16, 700, 513, 3000, 1000, 900], seed=61)
+    step_cpu = W.make_step(spec)
+    step = step_cpu.to("cuda")
+    outs = []
+    for _ in range(3):
+        out, kc, vc, status = run_gpu(step)
+        assert status == 0
+        outs.append(out)
+    for o in outs[1:]:
+        assert torch.equal(o.view(torch.int16), outs[0].view(torch.int16))
+    ref, _, _ = run_oracle(step_cpu)
+    assert_close(outs[0], ref, "bf16", "prefill determinism case")
+
+
 SHAPES = [
     # (q_lens, seq_lens): decode lengths at block edges, splits, chunks, a 1-token prompt
     ([1, 1, 1, 1, 1, 1], [1, 15, 16, 17, 300, 1000]),
