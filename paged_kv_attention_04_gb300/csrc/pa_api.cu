@@ -80,14 +80,17 @@ int check_layout(const pa_layout* L) {
   return PA_OK;
 }
 
-#ifndef PA_SPLIT_KV_BYTES
-#define PA_SPLIT_KV_BYTES (512 * 1024)
+#ifndef PA_SPLIT_BLOCKS
+#define PA_SPLIT_BLOCKS 128
 #endif
 
-// Smallest KV split, in blocks: about PA_SPLIT_KV_BYTES of K+V per work unit.
+// Smallest KV split, in blocks (the plan grows it for steps with much KV per
+// CTA).  A decode unit's cost is set by its blocks (instructions and latency
+// per block), not its bytes: 128 blocks measured best for bf16 at head size
+// 128 and 64 and for FP8 alike.
 int blocks_per_split(const pa_layout* L) {
-  const int block_kv_bytes = 2 * kBlockSize * L->head_size * elem_bytes(L->cache_dtype);
-  int b = PA_SPLIT_KV_BYTES / block_kv_bytes;
+  (void)L;
+  int b = PA_SPLIT_BLOCKS;
   if (b > kMaxUnitBlocks) b = kMaxUnitBlocks;
   return b < 1 ? 1 : b;
 }
@@ -297,6 +300,7 @@ int pa_forward(const void* q, const void* k_cache, const void* v_cache,
   pp.max_seq_len = max_seq_len;
   pp.max_blocks_per_seq = max_blocks_per_seq;
   pp.bps = blocks_per_split(layout);
+  pp.num_sms = num_sms;
   pp.small_positions = small_positions(layout);
   const bool tc_prefill = layout->dtype == PA_BF16 && !fp8_cache(layout);
   pp.prefill_min_qlen = tc_prefill ? kPrefillMinQlen : 0x7fffffff;

@@ -49,6 +49,7 @@ struct PlanParams {
   const int32_t* qsl;
   int num_seqs, num_tokens, max_query_len, max_seq_len, max_blocks_per_seq;
   int bps;              // KV blocks per split (minimum; long requests use larger splits)
+  int num_sms;          // SMs of the device (the plan sizes splits from the step's KV per SM)
   int small_positions;  // query positions per small-q tile
   int prefill_min_qlen; // requests with q_len >= this go to the tensor-core kernel
   int prefill_rows;     // query rows (positions x group) per prefill tile

@@ -92,6 +92,7 @@ __global__ void __launch_bounds__(kPlanThreads, 1) plan_kernel(PlanParams p) {
   __shared__ int carry[kLists];
   __shared__ int err;
   __shared__ int size_hist[kMaxUnitBlocks + 1];  // short decode items per size (blocks)
+  __shared__ unsigned long long s_blocks;        // KV blocks of the requests that split
   static_assert(kMaxUnitBlocks == 8 * 32, "the dispatch-order scan gives each lane 8 sizes");
   // the attention kernel that follows may become resident now; it waits for
   // this grid to finish before it reads the work lists.  This grid itself may
@@ -116,11 +117,35 @@ __global__ void __launch_bounds__(kPlanThreads, 1) plan_kernel(PlanParams p) {
   for (int i = threadIdx.x; i <= kMaxUnitBlocks; i += kPlanThreads) size_hist[i] = 0;
   if (threadIdx.x == 0) {
     err = 0;
+    s_blocks = 0;
     for (int i = 0; i < kLists; ++i) carry[i] = 0;
     const int q0 = __ldg(p.qsl), qB = __ldg(p.qsl + B);
     if (q0 != 0 || qB != p.num_tokens) err |= PA_DEV_QSL;
   }
   __syncthreads();
+
+  // Split size for this step: at least p.bps blocks, and longer when the
+  // CTAs (about two per SM) would otherwise get more than ~8 units each of
+  // the decode and few-token KV (measured: longer units amortise each unit's
+  // fixed cost once there are enough of them), up to kMaxUnitBlocks.
+  // Out-of-range lengths are left out here (they are flagged below).
+  {
+    unsigned long long mine = 0;
+    for (int r = threadIdx.x; r < B; r += kPlanThreads) {
+      const int S = __ldg(p.seq_lens + r);
+      const int L = __ldg(p.qsl + r + 1) - __ldg(p.qsl + r);
+      if (S >= 1 && S <= p.max_seq_len && L >= 1 && L < p.prefill_min_qlen)
+        mine += static_cast<unsigned long long>(ceil_div(S, kBlockSize));
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) mine += __shfl_down_sync(0xffffffffu, mine, o);
+    if ((threadIdx.x & 31) == 0 && mine) atomicAdd(&s_blocks, mine);
+  }
+  __syncthreads();
+  const long long per_cta =
+      static_cast<long long>(s_blocks) * p.num_kv_heads / max(1, 2 * p.num_sms);
+  const int bps = static_cast<int>(
+      min(static_cast<long long>(kMaxUnitBlocks), max(static_cast<long long>(p.bps), (per_cta + 7) / 8)));
 
   // One pass: classify and count, exclusive-scan the counts across the CTA,
   // and let each request's thread write its own items and tiles at its
@@ -146,17 +171,17 @@ __global__ void __launch_bounds__(kPlanThreads, 1) plan_kernel(PlanParams p) {
       } else if (L == 1) {
         c = kClassDecode;
         cnt[1] = 1;
-        const int nb = ceil_div(S, kBlockSize), rb = request_bps(nb, p.bps);
+        const int nb = ceil_div(S, kBlockSize), rb = request_bps(nb, bps);
         cnt[0] = splits_for(S - 1, rb);
         // long items: every full split, and the last one if it is at least half a split
-        cnt[5] = cnt[0] - 1 + (2 * (nb - (cnt[0] - 1) * rb) >= p.bps ? 1 : 0);
+        cnt[5] = cnt[0] - 1 + (2 * (nb - (cnt[0] - 1) * rb) >= bps ? 1 : 0);
       } else if (L >= p.prefill_min_qlen) {
         c = kClassPrefill;
         cnt[4] = ceil_div(L, p.prefill_rows / p.group);
       } else {
         c = kClassSmall;
         cnt[3] = ceil_div(L, p.small_positions);
-        const int rb = request_bps(ceil_div(S, kBlockSize), p.bps);
+        const int rb = request_bps(ceil_div(S, kBlockSize), bps);
         for (int m = 0; m < cnt[3]; ++m) {
           const int last = min(L, (m + 1) * p.small_positions) - 1;
           cnt[2] += splits_for(S - L + last, rb);
@@ -173,7 +198,7 @@ __global__ void __launch_bounds__(kPlanThreads, 1) plan_kernel(PlanParams p) {
       // items off[0] .. off[0] + cnt[0] - 1: one split of the request each
       const int tile = off[1];
       const int nb = ceil_div(S, kBlockSize);
-      const int rb = request_bps(nb, p.bps);
+      const int rb = request_bps(nb, bps);
       const int ns = cnt[0];
       if (tile < p.cap.decode_tiles) tiles_d[tile] = make_int4(off[0], ns, rb, 0);
       for (int s = 0; s < ns; ++s) {
@@ -191,7 +216,7 @@ __global__ void __launch_bounds__(kPlanThreads, 1) plan_kernel(PlanParams p) {
       }
     } else if (c == kClassSmall) {
       // tiles of small_positions positions, each expanded into its splits
-      const int rb = request_bps(ceil_div(S, kBlockSize), p.bps);
+      const int rb = request_bps(ceil_div(S, kBlockSize), bps);
       const int P = p.small_positions;
       int first = off[2];
       for (int m = 0; m < cnt[3]; ++m) {
@@ -270,7 +295,7 @@ __global__ void __launch_bounds__(kPlanThreads, 1) plan_kernel(PlanParams p) {
   for (int i = threadIdx.x; i < n_di; i += kPlanThreads) {
     // short = under half a split (full splits hold at least bps blocks)
     const int4 a = recs_d[i].a;  // written above by this CTA
-    if (2 * (a.w - a.z) < p.bps) order_d[atomicAdd(&size_hist[a.w - a.z], 1)] = i;
+    if (2 * (a.w - a.z) < bps) order_d[atomicAdd(&size_hist[a.w - a.z], 1)] = i;
   }
   for (int i = threadIdx.x; i < n_dt * p.num_kv_heads; i += kPlanThreads) cnt_d[i] = 0;
   for (int i = threadIdx.x; i < n_st * p.num_kv_heads; i += kPlanThreads) cnt_s[i] = 0;

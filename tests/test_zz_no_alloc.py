@@ -39,9 +39,9 @@ def _call_noalloc(lib, st, lay, out, status):
 
 def test_oversized_step_is_rejected_before_any_launch(lib):
     lay = P.make_layout(32, 8, 128, 30000, torch.bfloat16)
-    need = P.pa_forward_workspace_size(lay, 256, 256, 8192)
+    need = P.pa_forward_workspace_size(lay, 1024, 1024, 8192)
     assert need > PA_STATIC_SCRATCH_BYTES
-    rc = lib.pa_forward_noalloc(256, 256, 256, 256, 512, 256, 256, 256, 256, 1, 8192,
+    rc = lib.pa_forward_noalloc(256, 256, 256, 256, 512, 256, 256, 1024, 1024, 1, 8192,
                                 ctypes.c_float(0.1), 256, ctypes.byref(lay), None, None)
     assert rc == P.PA_ERR_INVALID
     assert "scratch" in P.last_error()
