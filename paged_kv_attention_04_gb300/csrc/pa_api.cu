@@ -165,7 +165,7 @@ int set_last_error(int code, const char* msg) {
   return code;
 }
 
-WsLayout ws_layout(const Capacity& cap, int B, int Hkv, int D, int group) {
+WsLayout ws_layout(const Capacity& cap, int Hkv, int D, int group) {
   WsLayout w{};
   size_t off = 0;
   auto take = [&](size_t bytes) { size_t o = off; off = align256(off + bytes); return o; };
@@ -243,7 +243,7 @@ size_t pa_forward_workspace_size(const pa_layout* layout, int num_seqs, int num_
     return 0;
   }
   const Capacity cap = capacity(layout, num_seqs, num_tokens, max_seq_len);
-  return ws_layout(cap, num_seqs, layout->num_kv_heads, layout->head_size,
+  return ws_layout(cap, layout->num_kv_heads, layout->head_size,
                    layout->num_q_heads / layout->num_kv_heads)
       .total;
 }
@@ -281,7 +281,7 @@ int pa_forward(const void* q, const void* k_cache, const void* v_cache,
   const Capacity cap = capacity(layout, num_seqs, num_tokens, max_seq_len);
   if (cap.decode_items > (1LL << 30) || cap.small_items > (1LL << 30))
     return fail(PA_ERR_INVALID, "step too large for one call");
-  const WsLayout lay = ws_layout(cap, num_seqs, layout->num_kv_heads, layout->head_size, group);
+  const WsLayout lay = ws_layout(cap, layout->num_kv_heads, layout->head_size, group);
   if (workspace_bytes < lay.total)
     return fail(PA_ERR_INVALID, "workspace of %zu bytes < %zu needed", workspace_bytes, lay.total);
   int num_sms = 0;

@@ -101,8 +101,8 @@ struct AttnParams {
 // Sets the message pa_last_error() returns on this thread; returns code.
 int set_last_error(int code, const char* msg);
 
-WsLayout ws_layout(const Capacity& cap, int num_seqs, int num_kv_heads, int head_size,
-                   int group);
+// Workspace regions for a step with capacity cap (see pa_forward_workspace_size).
+WsLayout ws_layout(const Capacity& cap, int num_kv_heads, int head_size, int group);
 
 // Kernel launchers (return cudaError_t of the launch).
 cudaError_t launch_cache_write(const void* k, const void* v, const int64_t* slot_mapping,
