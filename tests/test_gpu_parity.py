@@ -122,10 +122,13 @@ def test_prefill_runs_are_bit_identical():
 
 
 SHAPES = [
-    # (q_lens, seq_lens): decode lengths at block edges, splits, chunks, a 1-token prompt
+    # (q_lens, seq_lens): decode lengths at block edges, chunks, a 1-token prompt
     ([1, 1, 1, 1, 1, 1], [1, 15, 16, 17, 300, 1000]),
     ([3, 1, 16, 40, 1], [17, 33, 40, 300, 2]),
     ([7, 1, 25], [500, 257, 25]),
+    # KV splits (at least 128 blocks = 2048 keys each) and their merge: a decode one
+    # block past a split, few-token queries (2-15 rows) over long contexts
+    ([1, 4, 15, 2, 1], [2049, 5000, 3000, 6100, 4096]),
 ]
 
 
