@@ -27,6 +27,10 @@ namespace {
 
 constexpr int kPlanThreads = 1024;
 
+#ifndef PA_UNITS_PER_CTA
+#define PA_UNITS_PER_CTA 8  // split-size target: decode units per CTA (see plan_kernel)
+#endif
+
 // decode items, decode tiles, small items, small tiles, prefill tiles, long decode items
 constexpr int kLists = 6;
 
@@ -145,7 +149,8 @@ __global__ void __launch_bounds__(kPlanThreads, 1) plan_kernel(PlanParams p) {
   const long long per_cta =
       static_cast<long long>(s_blocks) * p.num_kv_heads / max(1, 2 * p.num_sms);
   const int bps = static_cast<int>(
-      min(static_cast<long long>(kMaxUnitBlocks), max(static_cast<long long>(p.bps), (per_cta + 7) / 8)));
+      min(static_cast<long long>(kMaxUnitBlocks),
+          max(static_cast<long long>(p.bps), (per_cta + PA_UNITS_PER_CTA - 1) / PA_UNITS_PER_CTA)));
 
   // One pass: classify and count, exclusive-scan the counts across the CTA,
   // and let each request's thread write its own items and tiles at its
