@@ -166,7 +166,10 @@ int pa_forward(const void* q, const void* k_cache, const void* v_cache,
  * caller-owned cudaEvent_t handles, every later pa_forward call on this
  * thread records `start` on its stream just before the decode-attention
  * kernel and `stop` just after it, so the caller can time that kernel alone.
- * pa_set_profile_events(NULL, NULL) turns this off.  Always returns PA_OK.
+ * The events sit between the planning kernel and the decode kernel, so while
+ * they are set the decode kernel cannot start before the plan has finished
+ * (its launch no longer overlaps the plan's tail): time whole steps with them
+ * off.  pa_set_profile_events(NULL, NULL) turns this off.  Always returns PA_OK.
  */
 int pa_set_profile_events(void* start, void* stop);
 
