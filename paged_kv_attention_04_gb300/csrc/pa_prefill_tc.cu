@@ -93,7 +93,7 @@ enum Bar : int {
   kGo = 10,         // [2] tile t: P written and S read (8 softmax warps), V of t landed
                     //     (V loader), K of t + 2 landed or none due (K loader)
   kVLand = 12,      // [2] V tile landed, for a tile whose last block the V loader trims
-  kPVDone = 14,     // [2] O += P V done (MMA commit); frees V and P
+  kPVDone = 14,     // [2] O += P V done (MMA commit); frees the V buffer
   kMx = 16,         // [2] both halves of each row published their maximum (8 warps)
   kMlFull = 18,     // row sums of both halves published (8 warps)
   kMlRead = 19,     // ... and read (8 warps)
@@ -267,9 +267,9 @@ __global__ void __launch_bounds__(kPfThreads, 1)
     // ------------------------------------------------------------ units, Q, K
     const int Hkv = p.num_kv_heads;
     const int n_units = __ldg(p.n_items) * Hkv;
-    // nf: first-K copies per group; sw: S phases waited per group; ga: kGo
-    // arrivals per group (one per tile of the group), gk: the last one that
-    // carried a copy, plus one
+    // per buffer parity w: nf: first-K copies; sw: S phases waited; ga: kGo
+    // arrivals (one per tile of that parity), gk: the last one that carried
+    // a copy, plus one
     uint32_t nf[2] = {0, 0}, sw[2] = {0, 0}, ga[2] = {0, 0}, gk[2] = {0, 0}, nq = 0;
     for (int uc = 0;; ++uc) {
       int unit = 0;
@@ -316,7 +316,7 @@ __global__ void __launch_bounds__(kPfThreads, 1)
       ++nq;
       bool ok = true;
       // K of tile sq goes into buffer w = sq & 1.  The first two were freed
-      // by the previous unit (its last S of each group was waited below);
+      // by the previous unit (its last S of each parity was waited below);
       // later ones wait for S of tile sq - 2 and then count as that tile's
       // kGo arrival (bytes included)
       for (int sq = 0; sq < u.n_kv; ++sq) {
@@ -353,8 +353,8 @@ __global__ void __launch_bounds__(kPfThreads, 1)
     __syncwarp();
   } else if (warp == kVLoadWarp) {
     // ------------------------------------------------------------ V
-    // nv: V tiles per group (= kGo arrivals); gv: the last kGo phase that
-    // carried a copy, plus one; nl: kVLand copies per group
+    // per buffer parity: nv: V tiles (= kGo arrivals); gv: the last kGo phase
+    // that carried a copy, plus one; nl: kVLand copies
     uint32_t nv[2] = {0, 0}, gv[2] = {0, 0}, nl[2] = {0, 0};
     bool landing = false;  // a kVLand copy not yet waited for
     int land_w = 0;
@@ -369,7 +369,7 @@ __global__ void __launch_bounds__(kPfThreads, 1)
       for (int sq = 0; sq < u.n_kv; ++sq) {
         const int w = sq & 1;
         const int kt = tile_of(u, sq);
-        // V buffer w is free once PV of the group's previous tile is done
+        // V buffer w is free once PV of the previous tile of that parity is done
         if (nv[w] > 0 && !wait_bar(bar(kPVDone + w), (nv[w] - 1) & 1, abort, p.status)) {
           ok = false;
           break;
@@ -450,7 +450,7 @@ __global__ void __launch_bounds__(kPfThreads, 1)
       tc_commit(bar(kPVDone + w));
     };
     uint32_t g0 = 0, g1 = 0;    // tiles per buffer parity so far (kGo phases)
-    uint32_t nf0 = 0, nf1 = 0;  // first-K copies per group so far
+    uint32_t nf0 = 0, nf1 = 0;  // first-K copies per buffer parity so far
     bool ok = true;
     for (int uc = 0; ok; ++uc) {
       const int slot = uc & 1;
