@@ -36,6 +36,10 @@ HEADLINE = "llama3_8b_decode"
 MIXED = "mixed_step"
 FALLBACK_HBM_GBS = 6800.0
 FALLBACK_BF16_TFLOPS = 1900.0
+# nominal GB300 figures (context beside the measured peaks): HBM3e 7.9 TB/s,
+# dense bf16 tensor 2.25 PFLOP/s
+NOMINAL_HBM_GBS = 7900.0
+NOMINAL_BF16_TFLOPS = 2250.0
 WORKLOAD_TEXT = {
     "llama3_8b_decode": "Llama-3-8B single-layer decode: batch 256, 32 q / 8 kv heads, head_size 128, "
                         "bf16, context lognormal(median 1024, sigma 0.8, cap 8192), block_size 16, "
@@ -643,6 +647,7 @@ def run_gpu_arm(args):
         "ms_per_step": pms,
         "tflops": pf_tflops,
         "frac_of_bf16_peak": pf_tflops / bf16_peak[0] if bf16_peak[0] else None,
+        "frac_of_nominal_bf16": pf_tflops / NOMINAL_BF16_TFLOPS,
         "peak_tflops": bf16_peak[0], "peak_source": bf16_peak[1],
         "flops": pf.work["chunk_flops"],
         "timed": "pa_cache_write + pa_forward (plan, tensor-core prefill kernel); L2 flushed "
@@ -665,6 +670,7 @@ def run_gpu_arm(args):
         "ms_per_step": lms,
         "tflops": pl_tflops,
         "frac_of_bf16_peak": pl_tflops / bf16_peak[0] if bf16_peak[0] else None,
+        "frac_of_nominal_bf16": pl_tflops / NOMINAL_BF16_TFLOPS,
         "peak_tflops": bf16_peak[0], "peak_source": bf16_peak[1],
         "flops": pl.work["chunk_flops"],
         "timed": "as prefill_chunks",
@@ -719,6 +725,7 @@ def run_gpu_arm(args):
         "roofline": {"bound": "hbm", "kernel": "attn_mma_kernel<128,4,1,4,2> (decode)",
                      "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
                      "peak_source": peak_src, "traffic": traffic,
+                     "nominal_peak": NOMINAL_HBM_GBS, "frac_of_nominal": achieved / NOMINAL_HBM_GBS,
                      "algorithmic_bytes_per_launch": w["decode_bytes"], "kernel_ms": dec_max},
         "e2e": {"value": e2e_value, "unit": "GB/s", "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms},
