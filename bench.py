@@ -446,9 +446,10 @@ class StepRunner:
 
     def time_device(self, steps: int, warmup: int, world: int, clocks: ClockSampler | None = None,
                     flush: bool = False):
-        """Inputs resident in HBM; returns (ms per step, decode-kernel ms per launch).
-        The steps are timed in one loop with no events inside a step; the decode
-        kernel is timed in a second loop with events around it (those events sit
+        """Inputs resident in HBM; returns (ms per step, decode-kernel ms per launch,
+        the median over the launches).  The steps are timed in one loop with no
+        events inside a step; the decode kernel is timed in a second loop with
+        events around it (those events sit
         between the plan and the decode kernel, so they would cost the step its
         launch overlap).  With flush, L2 is flushed before every step, outside the
         timed events."""
@@ -481,7 +482,7 @@ class StepRunner:
             barrier(world)
             P.pa_set_profile_events(None, None)
             if kernel_events:
-                return statistics.mean(a.elapsed_time(b) for a, b in evs)
+                return statistics.median(a.elapsed_time(b) for a, b in evs)
             return sum(a.elapsed_time(b) for a, b in steps_ev) / steps
 
         if clocks:
