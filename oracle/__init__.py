@@ -6,7 +6,8 @@ binding) never imports it.
 """
 from .paged_attention import (blocks_needed, block_bytes, slot_of, widen, validate_step,
                               cache_write, gather_request_kv, paged_attention,
-                              paged_attention_rows, within_tolerance)
+                              paged_attention_rows, within_tolerance, error_report)
 
 __all__ = ["blocks_needed", "block_bytes", "slot_of", "widen", "validate_step", "cache_write",
-           "gather_request_kv", "paged_attention", "paged_attention_rows", "within_tolerance"]
+           "gather_request_kv", "paged_attention", "paged_attention_rows", "within_tolerance",
+           "error_report"]

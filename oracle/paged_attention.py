@@ -27,6 +27,13 @@ What each function follows:
                        the earlier chunks' KV from the cache; a token depends
                        only on the tokens before it).  Softmax attention is
                        written out from its definition.
+  within_tolerance,
+  error_report      -- the comparison the parity tests apply: the combined
+                       elementwise bound |got - ref| <= atol + rtol |ref|, and
+                       the absolute and relative errors measured separately
+                       (the relative one above a stated |ref| floor).  The pages
+                       state no accuracy; the bounds come with the inputs'
+                       precision (bf16 in, fp32 accumulate; or fp32).
 
 Readings where the pages are silent (each is stated once more where used):
   * seq_lens[r] counts the KV tokens of request r including this step's new
@@ -210,12 +217,45 @@ def paged_attention_rows(q, k_cache, v_cache, block_tables, seq_lens, query_star
 
 
 def within_tolerance(got, ref, atol: float, rtol: float):
-    """Elementwise |got - ref| <= atol + rtol * |ref|; returns (ok, max_abs,
+    """Elementwise |got - ref| <= atol + rtol * |ref|, with both sides finite
+    (an infinite ref would otherwise admit any got); returns (ok, max_abs,
     max_rel over |ref| > 1e-2)."""
     got = np.asarray(got, dtype=np.float64)
     ref = np.asarray(ref, dtype=np.float64)
     err = np.abs(got - ref)
-    ok = bool(np.all(err <= atol + rtol * np.abs(ref)))
+    ok = bool(np.all(np.isfinite(got) & np.isfinite(ref) & (err <= atol + rtol * np.abs(ref))))
     big = np.abs(ref) > 1e-2
     max_rel = float((err[big] / np.abs(ref[big])).max()) if big.any() else 0.0
     return ok, float(err.max()) if err.size else 0.0, max_rel
+
+
+def error_report(got, ref, rel_floor: float) -> dict:
+    """The two error measures of the stated accuracy target, each on its own.
+
+      nonfinite  number of elements of `got` that are NaN or infinite
+      max_abs    max |got - ref| over every element (inf when any element of
+                 got or ref is not finite, so a NaN can never pass a bound)
+      max_rel    max |got - ref| / |ref| over the elements with
+                 |ref| >= rel_floor (0 when there are none)
+      rel_count  how many elements max_rel was taken over
+
+    A relative error has no meaning where ref is 0, so it is measured only
+    above a stated floor; below it the absolute bound alone applies."""
+    got = np.asarray(got, dtype=np.float64)
+    ref = np.asarray(ref, dtype=np.float64)
+    if got.shape != ref.shape:
+        raise ValueError(f"shapes differ: {got.shape} vs {ref.shape}")
+    finite = np.isfinite(got) & np.isfinite(ref)
+    err = np.abs(got - ref)
+    if not finite.all():
+        max_abs = float("inf")
+    else:
+        max_abs = float(err.max()) if err.size else 0.0
+    big = np.abs(ref) >= rel_floor
+    if big.any():
+        rel = np.where(finite[big], err[big] / np.abs(ref[big]), np.inf)
+        max_rel = float(rel.max())
+    else:
+        max_rel = 0.0
+    return {"nonfinite": int((~np.isfinite(got)).sum()), "max_abs": max_abs,
+            "max_rel": max_rel, "rel_count": int(big.sum()), "rel_floor": float(rel_floor)}

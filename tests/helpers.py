@@ -8,7 +8,10 @@ import oracle
 import paged_kv_attention_04_gb300 as P
 from paged_kv_attention_04_gb300 import workloads as W
 
+# (max-abs, max-rel) error bounds: bf16 in with fp32 accumulation, and fp32
 TOL = {"bf16": (1e-2, 2e-2), "f32": (1e-5, 1e-5)}
+# |ref| from which the relative error is gated (below it, max-abs alone)
+REL_FLOOR = {"bf16": 0.1, "f32": 1e-2}
 
 
 def bits(t: torch.Tensor) -> np.ndarray:
@@ -49,12 +52,27 @@ def run_oracle(step: W.Step):
 
 
 def assert_close(got: torch.Tensor, ref: np.ndarray, dtype: str, what: str = ""):
+    """The parity gates, all of which must hold:
+      * every output element is finite;
+      * combined, per element: |got - ref| <= atol + rtol |ref|;
+      * max-abs error <= atol over every element;
+      * max-rel error <= rtol over the elements with |ref| >= REL_FLOOR[dtype].
+    Returns (max_abs, max_rel)."""
     atol, rtol = TOL[dtype]
     g = oracle.widen(bits(got)) if got.dtype == torch.bfloat16 else got.detach().cpu().double().numpy()
-    ok, max_abs, max_rel = oracle.within_tolerance(g, ref, atol, rtol)
+    ok, _, _ = oracle.within_tolerance(g, ref, atol, rtol)
+    rep = oracle.error_report(g, ref, REL_FLOOR[dtype])
+    msg = (f"{what}: max_abs={rep['max_abs']:.3g} (gate {atol:g}), max_rel={rep['max_rel']:.3g} "
+           f"over |ref| >= {REL_FLOOR[dtype]:g} (gate {rtol:g}), nonfinite={rep['nonfinite']}")
+    if rep["nonfinite"]:
+        raise AssertionError(f"non-finite outputs; {msg}")
     if not ok:
         err = np.abs(g - ref)
         bad = np.argwhere(~(err <= atol + rtol * np.abs(ref)))
-        raise AssertionError(f"{what}: {len(bad)} elements outside tolerance; first {bad[:5].tolist()}"
-                             f" max_abs={max_abs:.3g} max_rel={max_rel:.3g}")
-    return max_abs, max_rel
+        raise AssertionError(f"{len(bad)} elements outside atol + rtol|ref|; first "
+                             f"{bad[:5].tolist()}; {msg}")
+    if not rep["max_abs"] <= atol:
+        raise AssertionError(f"max_abs above its gate; {msg}")
+    if not rep["max_rel"] <= rtol:
+        raise AssertionError(f"max_rel above its gate; {msg}")
+    return rep["max_abs"], rep["max_rel"]
