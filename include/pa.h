@@ -145,11 +145,19 @@ size_t pa_forward_workspace_size(const pa_layout* layout, int num_seqs, int num_
  *   out              device, [num_tokens][num_q_heads][head_size]
  * Rows of skipped requests are left unwritten.
  *
+ * The call's first kernel reads seq_lens and query_start_loc as soon as it
+ * starts, which may be while the kernel before it in `stream` still runs, if
+ * that kernel lets dependent launches start early (pa_cache_write does;
+ * ordinary kernels, copies and event waits do not).  Such a kernel must not
+ * write them.  Everything else pa_forward reads is read only after the
+ * previous kernel has finished.
+ *
  * Streams: everything is ordered on `stream`.  When the step can hold bf16
  * chunks of at least 16 tokens (max_query_len >= 16), their tensor-core
  * kernel runs on a library side stream forked from `stream` after the
  * planning kernel and joined back before the call returns, so it overlaps
- * the decode kernel.  The side stream and its two events are created once
+ * the decode kernel (unless pa_set_prefill_overlap(0) asked for one stream).
+ * The side stream and its two events are created once
  * per host thread and device, on the first such call (they hold no device
  * memory); make that first call before capturing `stream` into a CUDA graph.
  * A captured step records the fork and join as parallel graph branches.
@@ -172,6 +180,26 @@ int pa_forward(const void* q, const void* k_cache, const void* v_cache,
  * off.  pa_set_profile_events(NULL, NULL) turns this off.  Always returns PA_OK.
  */
 int pa_set_profile_events(void* start, void* stop);
+
+/*
+ * Profiling aid (no counterpart on the pages): the same for the tensor-core
+ * prefill kernel.  `start` and `stop` are recorded just before and after it
+ * on the stream it is launched on (the side stream, or `stream` when the
+ * overlap is off, see pa_set_prefill_overlap).  NULL, NULL turns this off.
+ * Always returns PA_OK.
+ */
+int pa_set_prefill_profile_events(void* start, void* stop);
+
+/*
+ * Scheduling choice (no counterpart on the pages).  on != 0 (the default):
+ * the tensor-core prefill kernel of a step runs on the library side stream
+ * beside the decode kernel (see pa_forward).  on == 0: it runs on `stream`
+ * between the planning kernel and the decode kernel, and no side stream is
+ * used.  Results are bit-identical either way (the kernels write disjoint
+ * output rows).  Applies to later pa_forward calls on this host thread.
+ * Always returns PA_OK.
+ */
+int pa_set_prefill_overlap(int on);
 
 /*
  * pa_forward without a caller-provided workspace, for callers that cannot

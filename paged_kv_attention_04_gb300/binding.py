@@ -62,6 +62,10 @@ def lib() -> ctypes.CDLL:
         L.pa_forward_noalloc.restype = i32
         L.pa_set_profile_events.argtypes = [vp, vp]
         L.pa_set_profile_events.restype = i32
+        L.pa_set_prefill_profile_events.argtypes = [vp, vp]
+        L.pa_set_prefill_profile_events.restype = i32
+        L.pa_set_prefill_overlap.argtypes = [i32]
+        L.pa_set_prefill_overlap.restype = i32
         L.pa_version.argtypes = []
         L.pa_version.restype = i32
         _lib = L
@@ -181,11 +185,10 @@ def pa_forward_noalloc(q, k_cache, v_cache, block_tables, seq_lens, query_start_
                                     ctypes.byref(layout), _ptr(status), _stream(stream)))
 
 
-def pa_set_profile_events(start: "torch.cuda.Event | None", stop: "torch.cuda.Event | None") -> None:
-    """Record `start`/`stop` around the decode-attention kernel of later
-    pa_forward calls on this thread (None, None turns it off).  torch creates
-    an event's CUDA handle on its first record, so unrecorded events are
-    recorded once here first."""
+def _event_handles(start, stop) -> list:
+    """CUDA handles of two torch events (None stays None).  torch creates an
+    event's handle on its first record, so unrecorded events are recorded once
+    here first."""
     handles = []
     for ev in (start, stop):
         if ev is None:
@@ -194,7 +197,27 @@ def pa_set_profile_events(start: "torch.cuda.Event | None", stop: "torch.cuda.Ev
         if not ev.cuda_event:
             ev.record()
         handles.append(ev.cuda_event)
-    _check(lib().pa_set_profile_events(handles[0], handles[1]))
+    return handles
+
+
+def pa_set_profile_events(start: "torch.cuda.Event | None", stop: "torch.cuda.Event | None") -> None:
+    """Record `start`/`stop` around the decode-attention kernel of later
+    pa_forward calls on this thread (None, None turns it off)."""
+    _check(lib().pa_set_profile_events(*_event_handles(start, stop)))
+
+
+def pa_set_prefill_profile_events(start: "torch.cuda.Event | None",
+                                  stop: "torch.cuda.Event | None") -> None:
+    """Record `start`/`stop` around the tensor-core prefill kernel of later
+    pa_forward calls on this thread, on the stream it runs on (None, None
+    turns it off)."""
+    _check(lib().pa_set_prefill_profile_events(*_event_handles(start, stop)))
+
+
+def pa_set_prefill_overlap(on: bool) -> None:
+    """True (the default): the prefill kernel runs on a side stream beside the
+    decode kernel; False: on the caller's stream before it."""
+    _check(lib().pa_set_prefill_overlap(1 if on else 0))
 
 
 def alloc_workspace(layout: pa_layout, num_seqs: int, num_tokens: int, max_seq_len: int,

@@ -10,14 +10,14 @@
 #include "pa_internal.h"
 
 namespace pa {
-cudaError_t launch_attn_cc_bf16(const AttnParams& p, int head_size, int group, int positions,
-                                int num_sms, cudaStream_t stream);
+cudaError_t launch_attn_mma_bf16(const AttnParams& p, int head_size, int group, int positions,
+                                 int num_sms, cudaStream_t stream);
 cudaError_t launch_attn_cc_f32(const AttnParams& p, int head_size, int group, int positions,
                                int num_sms, cudaStream_t stream);
 
-cudaError_t launch_attn_cuda_core(const AttnParams& p, pa_dtype dtype, int head_size, int group,
-                                  int positions, int num_sms, cudaStream_t stream) {
-  return dtype == PA_BF16 ? launch_attn_cc_bf16(p, head_size, group, positions, num_sms, stream)
+cudaError_t launch_attn_by_dtype(const AttnParams& p, pa_dtype dtype, int head_size, int group,
+                                 int positions, int num_sms, cudaStream_t stream) {
+  return dtype == PA_BF16 ? launch_attn_mma_bf16(p, head_size, group, positions, num_sms, stream)
                           : launch_attn_cc_f32(p, head_size, group, positions, num_sms, stream);
 }
 
@@ -26,6 +26,9 @@ namespace {
 thread_local std::string g_last_error;
 thread_local cudaEvent_t g_prof_start = nullptr;
 thread_local cudaEvent_t g_prof_stop = nullptr;
+thread_local cudaEvent_t g_pf_prof_start = nullptr;
+thread_local cudaEvent_t g_pf_prof_stop = nullptr;
+thread_local bool g_prefill_overlap = true;
 
 int fail(int code, const char* fmt, ...) {
   char buf[512];
@@ -91,6 +94,9 @@ int check_layout(const pa_layout* L) {
 int blocks_per_split(const pa_layout* L) {
   (void)L;
   int b = PA_SPLIT_BLOCKS;
+#if defined(PA_SPLIT_BLOCKS_SMALL) && PA_SPLIT_BLOCKS_SMALL > 0
+  if (PA_SPLIT_BLOCKS_SMALL < b) b = PA_SPLIT_BLOCKS_SMALL;
+#endif
   if (b > kMaxUnitBlocks) b = kMaxUnitBlocks;
   return b < 1 ? 1 : b;
 }
@@ -198,11 +204,22 @@ extern "C" {
 
 const char* pa_last_error(void) { return g_last_error.c_str(); }
 
-int pa_version(void) { return 100; }
+int pa_version(void) { return 200; }
 
 int pa_set_profile_events(void* start, void* stop) {
   g_prof_start = static_cast<cudaEvent_t>(start);
   g_prof_stop = static_cast<cudaEvent_t>(stop);
+  return PA_OK;
+}
+
+int pa_set_prefill_profile_events(void* start, void* stop) {
+  g_pf_prof_start = static_cast<cudaEvent_t>(start);
+  g_pf_prof_stop = static_cast<cudaEvent_t>(stop);
+  return PA_OK;
+}
+
+int pa_set_prefill_overlap(int on) {
+  g_prefill_overlap = on != 0;
   return PA_OK;
 }
 
@@ -316,10 +333,12 @@ int pa_forward(const void* q, const void* k_cache, const void* v_cache,
 
   // Chunked prefill (tensor cores) runs on a side stream, launched before the
   // decode kernel so that decode CTAs fill the SMs the prefill CTAs leave:
-  // the HBM-bound and the tensor-bound work overlap.
+  // the HBM-bound and the tensor-bound work overlap.  With the overlap off it
+  // runs on `st` before the decode kernel.
   const bool run_prefill = tc_prefill && max_query_len >= kPrefillMinQlen;
+  const bool fork = run_prefill && g_prefill_overlap;
   SideStream* side = nullptr;
-  if (run_prefill) {
+  if (fork) {
     if (int rc = side_stream_of_current_device(&side)) return rc;
   }
 
@@ -350,13 +369,21 @@ int pa_forward(const void* q, const void* k_cache, const void* v_cache,
     pf.merge_cnt = nullptr;
     pf.part_acc = nullptr;
     pf.part_ml = nullptr;
-    e = cudaEventRecord(side->fork, st);
-    if (e == cudaSuccess) e = cudaStreamWaitEvent(side->stream, side->fork, 0);
-    if (e != cudaSuccess) return fail_cuda(e, "side stream fork");
-    e = launch_prefill_tc(pf, layout->head_size, group, num_sms, side->stream);
+    cudaStream_t pst = st;
+    if (fork) {
+      e = cudaEventRecord(side->fork, st);
+      if (e == cudaSuccess) e = cudaStreamWaitEvent(side->stream, side->fork, 0);
+      if (e != cudaSuccess) return fail_cuda(e, "side stream fork");
+      pst = side->stream;
+    }
+    if (g_pf_prof_start) cudaEventRecord(g_pf_prof_start, pst);
+    e = launch_prefill_tc(pf, layout->head_size, group, num_sms, pst);
     if (e != cudaSuccess) return fail_cuda(e, "prefill attention launch");
-    e = cudaEventRecord(side->join, side->stream);
-    if (e != cudaSuccess) return fail_cuda(e, "side stream join");
+    if (g_pf_prof_stop) cudaEventRecord(g_pf_prof_stop, pst);
+    if (fork) {
+      e = cudaEventRecord(side->join, side->stream);
+      if (e != cudaSuccess) return fail_cuda(e, "side stream join");
+    }
   }
 
   // decode rows (q_len == 1); the launch may overlap the plan's tail
@@ -373,7 +400,7 @@ int pa_forward(const void* q, const void* k_cache, const void* v_cache,
   if (g_prof_start) cudaEventRecord(g_prof_start, st);
   e = fp8_cache(layout)
           ? launch_attn_fp8(ap, layout->head_size, group, 1, num_sms, st)
-          : launch_attn_cuda_core(ap, layout->dtype, layout->head_size, group, 1, num_sms, st);
+          : launch_attn_by_dtype(ap, layout->dtype, layout->head_size, group, 1, num_sms, st);
   if (e != cudaSuccess) return fail_cuda(e, "decode attention launch");
   if (g_prof_stop) cudaEventRecord(g_prof_stop, st);
 
@@ -390,11 +417,11 @@ int pa_forward(const void* q, const void* k_cache, const void* v_cache,
     ap.part_ml = reinterpret_cast<float*>(ws + lay.part_ml_s);
     e = fp8_cache(layout)
             ? launch_attn_fp8(ap, layout->head_size, group, small_positions(layout), num_sms, st)
-            : launch_attn_cuda_core(ap, layout->dtype, layout->head_size, group,
-                                    small_positions(layout), num_sms, st);
+            : launch_attn_by_dtype(ap, layout->dtype, layout->head_size, group,
+                                   small_positions(layout), num_sms, st);
     if (e != cudaSuccess) return fail_cuda(e, "small-q attention launch");
   }
-  if (run_prefill) {
+  if (fork) {
     e = cudaStreamWaitEvent(st, side->join, 0);
     if (e != cudaSuccess) return fail_cuda(e, "side stream join wait");
   }

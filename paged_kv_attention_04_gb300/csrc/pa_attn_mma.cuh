@@ -39,6 +39,9 @@
 #ifndef PA_CLAIM_AHEAD
 #define PA_CLAIM_AHEAD 0  // 1: the scheduler warp claims a unit one fetch early
 #endif
+#ifndef PA_SPARE_CLAIM
+#define PA_SPARE_CLAIM 1  // 1: claim a second unit at the start only when units are plentiful
+#endif
 #ifndef PA_QK_SPLIT_ACC
 #define PA_QK_SPLIT_ACC 0  // 1: two accumulator sets per score tile (shorter MMA chains)
 #endif
@@ -47,6 +50,9 @@
 // the current one (1) or not (0).
 #ifndef PA_L2_PREFETCH
 #define PA_L2_PREFETCH 1
+#endif
+#ifndef PA_L2_PREFETCH_D64
+#define PA_L2_PREFETCH_D64 0
 #endif
 
 namespace pa {
@@ -260,8 +266,12 @@ __global__ void __launch_bounds__(MmaCfg<D, G, P, NW, NS, F8>::kThreads,
         *reinterpret_cast<uint4*>(smem + C::kQOff + buf * 16 * C::kRowBytes +
                                   swz<C::kRowBytes>(row, c)) = make_uint4(0, 0, 0, 0);
     }
+    // A second unit is claimed up front only if every CTA can still get one:
+    // with fewer units than that (small steps), taking two would leave other
+    // CTAs idle while this one works through both.
     const int u0 = claim();
-    const int u1 = claim();
+    const int u1 = (!PA_SPARE_CLAIM || u0 + static_cast<int>(gridDim.x) < n_units) ? claim()
+                                                                                    : n_units;
     const int u2 = PA_CLAIM_AHEAD ? claim() : 0;
     if (lane == 0) {
       s_next_u = u2;
@@ -332,7 +342,7 @@ __global__ void __launch_bounds__(MmaCfg<D, G, P, NW, NS, F8>::kThreads,
     // lane (lanes 0-15 K, 16-31 V).  With the cp.async ring this keeps two
     // blocks per warp in flight from HBM without more shared memory (measured
     // on head size 128: +5.5 % decode bandwidth; head size 64 lost 8 %).
-    if (PA_L2_PREFETCH && D == 128 && iss_i < share(m)) {
+    if (PA_L2_PREFETCH && (D == 128 || PA_L2_PREFETCH_D64) && iss_i < share(m)) {
       const int nphys = m.bt[warp + iss_i * NW];
       if (nphys >= 0 && nphys < p.num_blocks) {
         const int t = lane & (kBlockSize - 1);
@@ -451,7 +461,9 @@ __global__ void __launch_bounds__(MmaCfg<D, G, P, NW, NS, F8>::kThreads,
       const UnitTail tail = s_tail;
       if (tail.valid) finish_unit(tail, (k - 1) & 1);
       store_q(qv, (k + 1) & 1);
-      const int nu = claim();
+      // the stream ends at the first empty slot: claim nothing past it (a
+      // unit claimed there would never be run)
+      const int nu = meta[(k + 1) % 3].valid ? claim() : n_units;
       fetch_unit(meta[(k + 2) % 3], PA_CLAIM_AHEAD ? s_next_u : nu);
       __syncwarp();
       if (lane == 0) {

@@ -8,6 +8,13 @@
 #ifndef PA_MMA_STAGES
 #define PA_MMA_STAGES 2
 #endif
+// head size 64: a K+V block is 4 KB, half the head-size-128 block
+#ifndef PA_MMA_WARPS_D64
+#define PA_MMA_WARPS_D64 PA_MMA_WARPS
+#endif
+#ifndef PA_MMA_STAGES_D64
+#define PA_MMA_STAGES_D64 PA_MMA_STAGES
+#endif
 
 namespace pa {
 
@@ -15,9 +22,10 @@ namespace {
 template <int D, int G>
 cudaError_t dispatch_positions(const AttnParams& p, int positions, int num_sms,
                                cudaStream_t stream) {
-  if (positions == 1)
-    return launch_mma<D, G, 1, PA_MMA_WARPS, PA_MMA_STAGES>(p, num_sms, stream);
-  return launch_mma<D, G, kSmallRows / G, PA_MMA_WARPS, PA_MMA_STAGES>(p, num_sms, stream);
+  constexpr int NW = D == 64 ? PA_MMA_WARPS_D64 : PA_MMA_WARPS;
+  constexpr int NS = D == 64 ? PA_MMA_STAGES_D64 : PA_MMA_STAGES;
+  if (positions == 1) return launch_mma<D, G, 1, NW, NS>(p, num_sms, stream);
+  return launch_mma<D, G, kSmallRows / G, NW, NS>(p, num_sms, stream);
 }
 
 template <int D>
@@ -33,7 +41,7 @@ cudaError_t dispatch_group(const AttnParams& p, int group, int positions, int nu
 }
 }  // namespace
 
-cudaError_t launch_attn_cc_bf16(const AttnParams& p, int head_size, int group, int positions,
+cudaError_t launch_attn_mma_bf16(const AttnParams& p, int head_size, int group, int positions,
                                 int num_sms, cudaStream_t stream) {
   switch (head_size) {
     case 64: return dispatch_group<64>(p, group, positions, num_sms, stream);

@@ -114,13 +114,15 @@ cudaError_t launch_cache_write_fp8(const void* k, const void* v, const int64_t* 
                                    long long num_slots, float k_scale, float v_scale,
                                    int32_t* status, cudaStream_t stream);
 cudaError_t launch_plan(const PlanParams& p, cudaStream_t stream);
-// CUDA-core split-KV attention.  positions: 1 (decode list) or the small-q
-// tile height.  Returns cudaErrorInvalidValue for an unbuilt combination.
 // Tensor-core (tcgen05) chunked-prefill attention over the prefill list.
 cudaError_t launch_prefill_tc(const AttnParams& p, int head_size, int group, int num_sms,
                               cudaStream_t stream);
-cudaError_t launch_attn_cuda_core(const AttnParams& p, pa_dtype dtype, int head_size, int group,
-                                  int positions, int num_sms, cudaStream_t stream);
+// Split-KV attention over the decode or few-token list, by element type:
+// bf16 runs the warp-level tensor-core (mma.sync) kernel, fp32 the CUDA-core
+// kernel.  positions: 1 (decode list) or the few-token tile height.  Returns
+// cudaErrorInvalidValue for an unbuilt combination.
+cudaError_t launch_attn_by_dtype(const AttnParams& p, pa_dtype dtype, int head_size, int group,
+                                 int positions, int num_sms, cudaStream_t stream);
 // bf16 q/out over an FP8 (E4M3) cache (tensor-core decode and few-token tiles).
 cudaError_t launch_attn_fp8(const AttnParams& p, int head_size, int group, int positions,
                             int num_sms, cudaStream_t stream);

@@ -30,6 +30,12 @@ constexpr int kPlanThreads = 1024;
 #ifndef PA_UNITS_PER_CTA
 #define PA_UNITS_PER_CTA 8  // split-size target: decode units per CTA (see plan_kernel)
 #endif
+#ifndef PA_SPLIT_BLOCKS_SMALL
+#define PA_SPLIT_BLOCKS_SMALL 0  // > 0: smallest split of steps with little KV per CTA
+#endif
+#ifndef PA_SMALL_UNITS
+#define PA_SMALL_UNITS 2
+#endif
 
 // decode items, decode tiles, small items, small tiles, prefill tiles, long decode items
 constexpr int kLists = 6;
@@ -98,12 +104,16 @@ __global__ void __launch_bounds__(kPlanThreads, 1) plan_kernel(PlanParams p) {
   __shared__ int size_hist[kMaxUnitBlocks + 1];  // short decode items per size (blocks)
   __shared__ unsigned long long s_blocks;        // KV blocks of the requests that split
   static_assert(kMaxUnitBlocks == 8 * 32, "the dispatch-order scan gives each lane 8 sizes");
-  // the attention kernel that follows may become resident now; it waits for
+  // The attention kernel that follows may become resident now; it waits for
   // this grid to finish before it reads the work lists.  This grid itself may
-  // have started early (programmatic launch): wait for the previous kernel in
-  // the stream before reading anything it might have written.
+  // have started early (programmatic launch) beside the previous kernel in
+  // the stream, normally the slot write.  It reads only seq_lens and
+  // query_start_loc, which that kernel does not write, and writes only the
+  // workspace, which no kernel still running reads (the slot write starts only
+  // after the previous step's kernels have finished).  So it plans at once and
+  // waits for the previous kernel only before finishing: the attention kernel
+  // then sees the slot write complete as well.
   launch_dependents();
-  wait_prior_grid();
   const int B = p.num_seqs;
   char* ws = p.ws;
   int* hdr = reinterpret_cast<int*>(ws + p.lay.hdr);
@@ -148,9 +158,14 @@ __global__ void __launch_bounds__(kPlanThreads, 1) plan_kernel(PlanParams p) {
   __syncthreads();
   const long long per_cta =
       static_cast<long long>(s_blocks) * p.num_kv_heads / max(1, 2 * p.num_sms);
-  const int bps = static_cast<int>(
+  int bps = static_cast<int>(
       min(static_cast<long long>(kMaxUnitBlocks),
           max(static_cast<long long>(p.bps), (per_cta + PA_UNITS_PER_CTA - 1) / PA_UNITS_PER_CTA)));
+#if PA_SPLIT_BLOCKS_SMALL > 0
+  if (per_cta < p.bps)
+    bps = static_cast<int>(max(static_cast<long long>(PA_SPLIT_BLOCKS_SMALL),
+                               (per_cta + PA_SMALL_UNITS - 1) / PA_SMALL_UNITS));
+#endif
 
   // One pass: classify and count, exclusive-scan the counts across the CTA,
   // and let each request's thread write its own items and tiles at its
@@ -267,6 +282,7 @@ __global__ void __launch_bounds__(kPlanThreads, 1) plan_kernel(PlanParams p) {
       for (int i = 0; i < kHdrWords; ++i) hdr[i] = 0;
       flag_error(p.status, err);
     }
+    wait_prior_grid();
     return;
   }
   const int n_di = carry[0], n_dt = carry[1], n_si = carry[2], n_st = carry[3], n_pt = carry[4];
@@ -315,6 +331,7 @@ __global__ void __launch_bounds__(kPlanThreads, 1) plan_kernel(PlanParams p) {
     hdr[kHdrPrefillNext] = 0;
     if (err) flag_error(p.status, err);
   }
+  wait_prior_grid();
 }
 
 cudaError_t launch_plan(const PlanParams& p, cudaStream_t stream) {
