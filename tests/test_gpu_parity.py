@@ -1,9 +1,11 @@
 """GPU parity: libpa against the fp64 oracle on the same seeded inputs.
 
 Cache writes must match bit for bit (the whole cache, so untouched slots are
-checked too); attention must satisfy |gpu - oracle| <= atol + rtol*|oracle|
-elementwise with (atol, rtol) = (1e-2, 2e-2) for bf16 and (1e-5, 1e-5) for
-fp32.  Every launch goes through the C ABI."""
+checked too).  Attention outputs must be finite and meet, with (atol, rtol) =
+(1e-2, 2e-2) for bf16 and (1e-5, 1e-5) for fp32: |gpu - oracle| <= atol +
+rtol |oracle| per element, max-abs error <= atol, and max-rel error <= rtol
+over the elements with |oracle| at or above a stated floor (helpers.assert_close).
+Every launch goes through the C ABI."""
 import numpy as np
 import pytest
 import torch
@@ -42,7 +44,8 @@ def test_config_full_parity(name):
 
 def test_long_context_sampled_parity():
     """Long-context decode at full size (a ~9 GB pool): the whole cache write
-    is checked, attention on sampled rows the oracle evaluates one by one."""
+    is checked bit for bit; attention on 128 rows the oracle evaluates one by
+    one, one q head of every kv head of every request."""
     spec = W.spec_long_context_decode()
     step = W.make_step(spec, device="cuda")
     out, kc, vc, status = run_gpu(step)
@@ -57,10 +60,13 @@ def test_long_context_sampled_parity():
         restored[slots] = orig.view(NBS, -1).view(torch.int16)[slots]
         assert torch.equal(restored, orig.view(NBS, -1).view(torch.int16))
         del restored
-    # oracle on sampled rows, over a private copy of each request's blocks
+    # oracle on every request and every kv head (one of its q heads, rotating
+    # through the group), over a private copy of each request's blocks
     bt = step.block_tables.cpu().numpy()
     S_all = spec.seq_lens
-    for r, h in ((int(np.argmin(S_all)), 0), (int(np.argmax(S_all)), 31), (5, 13)):
+    G = spec.num_q_heads // spec.num_kv_heads
+    checked = 0
+    for r in range(spec.num_seqs):
         S = int(S_all[r])
         nb = oracle.blocks_needed(S)
         blocks = torch.from_numpy(bt[r, :nb].astype(np.int64)).cuda()
@@ -70,11 +76,15 @@ def test_long_context_sampled_parity():
         slot = (pos // 16) * 16 + pos % 16
         mk, mv = oracle.cache_write(bits(step.k[r:r + 1]), bits(step.v[r:r + 1]),
                                     np.array([slot]), mk, mv)
+        rows = [(0, g * G + (r + g) % G) for g in range(spec.num_kv_heads)]
         ref = oracle.paged_attention_rows(bits(step.q[r:r + 1]), mk, mv, np.arange(nb)[None, :],
                                           np.array([S]), np.array([0, 1]), step.scale,
-                                          spec.num_kv_heads, [(0, h)])
-        assert_close(out[r, h], ref[0], "bf16", f"long-context r={r} h={h}")
+                                          spec.num_kv_heads, rows)
+        got = torch.stack([out[r, h] for _, h in rows])
+        assert_close(got, ref, "bf16", f"long-context r={r} S={S}")
+        checked += len(rows)
         del mk, mv
+    assert checked == spec.num_seqs * spec.num_kv_heads
 
 
 def test_long_prefill_chunk_sampled_parity():

@@ -158,7 +158,7 @@ def test_assert_close_max_rel_gate(dtype):
     the same relative error below the floor is left to the absolute bound."""
     atol, rtol = helpers.TOL[dtype]
     floor = helpers.REL_FLOOR[dtype]
-    x = 1.5 * floor
+    x = 1.2 * floor
     assert 1.5 * rtol * x < atol
     ref = _exact(np.full(256, 0.37), dtype)
     ref[9] = _exact(np.array([x]), dtype)[0]
