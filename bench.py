@@ -118,7 +118,7 @@ def measured_bf16_tflops() -> tuple[float, str]:
 
 def kernel_source_hash() -> str:
     h = hashlib.sha256()
-    for name in ("pa_attn_mma.cuh", "pa_attn_cc_bf16.cu", "pa_device.cuh"):
+    for name in ("pa_attn_mma.cuh", "pa_attn_mma_bf16.cu", "pa_device.cuh"):
         with open(os.path.join(ROOT, "paged_kv_attention_04_gb300", "csrc", name), "rb") as f:
             h.update(f.read())
     return h.hexdigest()[:16]
@@ -438,29 +438,39 @@ class StepRunner:
                      st.max_query_len, st.max_seq_len, st.scale, self.out, self.ws, self.layout,
                      self.status)
 
+    FLUSH_TEXT = ("flushed before every step, outside the timed events: a 256 MiB buffer "
+                  "(twice L2) written, then read back, so the step starts with none of its "
+                  "inputs in L2 and no dirty lines left to write back")
+
     def flush_l2(self):
-        """Write 256 MiB (twice the L2) so the next step starts with a cold L2."""
+        """Write 256 MiB (twice the L2), then read it, so the next step starts
+        with a cold L2: the read evicts the written lines, whose write-back to
+        HBM would otherwise land inside the timed step."""
         if not hasattr(self, "_flush"):
             self._flush = self.torch.empty(256 << 20, dtype=self.torch.uint8, device="cuda")
         self._flush.zero_()
+        self._flush.view(self.torch.int32).sum()
 
     def time_device(self, steps: int, warmup: int, world: int, clocks: ClockSampler | None = None,
                     flush: bool = False):
         """Inputs resident in HBM; returns (ms per step, decode-kernel ms per launch,
-        the median over the launches).  The steps are timed in one loop with no
-        events inside a step; the decode kernel is timed in a second loop with
-        events around it (those events sit
-        between the plan and the decode kernel, so they would cost the step its
-        launch overlap).  With flush, L2 is flushed before every step, outside the
-        timed events."""
+        prefill-kernel ms per launch or None), the kernel times being medians over
+        the launches.  The steps are timed in one loop with no events inside a
+        step; the kernels are timed in a second loop with events around each
+        (events between the plan and the decode kernel would cost the step their
+        launch overlap).  With flush, L2 is flushed before every step, outside
+        the timed events."""
         torch, P = self.torch, self.P
         for _ in range(warmup):
             self.step()
         torch.cuda.synchronize()
+        has_prefill = self.st.max_query_len >= 16 and self.spec.dtype == "bf16"
 
         def loop(kernel_events):
             evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
                    for _ in range(steps)]
+            pevs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+                    for _ in range(steps)]
             steps_ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
                         for _ in range(steps if flush else 1)]
             barrier(world)
@@ -473,6 +483,8 @@ class StepRunner:
                     steps_ev[i][0].record()
                 if kernel_events:
                     P.pa_set_profile_events(evs[i][0], evs[i][1])
+                    if has_prefill:
+                        P.pa_set_prefill_profile_events(pevs[i][0], pevs[i][1])
                 self.step()
                 if flush:
                     steps_ev[i][1].record()
@@ -481,8 +493,11 @@ class StepRunner:
             torch.cuda.synchronize()
             barrier(world)
             P.pa_set_profile_events(None, None)
+            P.pa_set_prefill_profile_events(None, None)
             if kernel_events:
-                return statistics.median(a.elapsed_time(b) for a, b in evs)
+                dec = statistics.median(a.elapsed_time(b) for a, b in evs)
+                pf = statistics.median(a.elapsed_time(b) for a, b in pevs) if has_prefill else None
+                return dec, pf
             return sum(a.elapsed_time(b) for a, b in steps_ev) / steps
 
         if clocks:
@@ -490,8 +505,8 @@ class StepRunner:
         step_ms = loop(False)
         if clocks:
             clocks.mark("timed_end")
-        dec_ms = loop(True)
-        return step_ms, dec_ms
+        dec_ms, pf_ms = loop(True)
+        return step_ms, dec_ms, pf_ms
 
     def time_graph(self, steps: int, warmup: int, world: int, flush: bool = False) -> float:
         """The same step captured once in a CUDA graph and replayed; ms per step
@@ -576,8 +591,15 @@ class StepRunner:
         return e0.elapsed_time(e1) / steps, h2d, d2h
 
 
+def _check_status(runner, what: str) -> None:
+    if int(runner.status.item()) != 0:
+        raise RuntimeError(f"{what}: device status {int(runner.status.item())}")
+
+
 def run_gpu_arm(args):
     import torch
+
+    import paged_kv_attention_04_gb300 as P
     from paged_kv_attention_04_gb300 import build
     build.build()
     world, rank, local = dist_setup()
@@ -589,16 +611,20 @@ def run_gpu_arm(args):
         dev_uuid = u if u.startswith("GPU-") else "GPU-" + u
     except Exception:
         pass
+    seed_off = rank * 1000 if world > 1 else 0
+    peak, peak_src = measured_peaks()
+    bf16_peak = measured_bf16_tflops()
+    half = max(3, args.steps // 2)
 
-    runner = StepRunner(HEADLINE, seed_offset=rank * 1000 if world > 1 else 0)
+    # ---- headline: Llama-3-8B decode step
+    runner = StepRunner(HEADLINE, seed_offset=seed_off)
     clocks = ClockSampler(dev_uuid)
     clocks.start()
     time.sleep(0.3)
     clocks.mark("warm_start")
-    ms, dec_ms = runner.time_device(args.steps, args.warmup, world, clocks)
+    ms, dec_ms, _ = runner.time_device(args.steps, args.warmup, world, clocks)
     clock_info = clocks.stop()
-    if int(runner.status.item()) != 0:
-        raise RuntimeError(f"device status {int(runner.status.item())}")
+    _check_status(runner, "headline")
     ms_max = dist_max(ms, world)
     dec_max = dist_max(dec_ms, world)
     w = runner.work
@@ -607,112 +633,196 @@ def run_gpu_arm(args):
     e2e_ms, h2d, d2h = runner.time_e2e(max(3, args.steps // 4), max(3, args.warmup), world)
     e2e_ms = dist_max(e2e_ms, world)
     e2e_value = replica_value(w["step_bytes"], e2e_ms, world)
-    peak, peak_src = measured_peaks()
     achieved = w["decode_bytes"] / (dec_max * 1e-3) / 1e9
     traffic = recorded_traffic(HEADLINE)
     launches = runner.launches_per_step * args.steps
     del runner
     torch.cuda.empty_cache()
 
-    # mixed continuous-batching step
-    mixed = StepRunner(MIXED, seed_offset=rank * 1000 if world > 1 else 0)
-    mms, mdec = mixed.time_device(max(3, args.steps // 2), args.warmup, world)
-    mms, mdec = dist_max(mms, world), dist_max(mdec, world)
+    # ---- mixed continuous-batching step: prefill overlapped with decode, and serial
+    mixed = StepRunner(MIXED, seed_offset=seed_off)
+    mms, mdec, _ = (dist_max(x, world) if x is not None else None
+                    for x in mixed.time_device(half, args.warmup, world))
+    mgraph = dist_max(mixed.time_graph(half, args.warmup, world), world)
+    P.pa_set_prefill_overlap(False)
+    try:
+        sms_, sdec, spf = (dist_max(x, world) for x in mixed.time_device(half, args.warmup, world))
+    finally:
+        P.pa_set_prefill_overlap(True)
+    _check_status(mixed, "mixed step")
     mw = mixed.work
-    rest_ms = max(mms - mdec, 1e-6)
+    del mixed
+    torch.cuda.empty_cache()
+    # the step's decode requests alone: the decode kernel's standalone rate
+    md = StepRunner(MIXED, seed_offset=seed_off, requests=slice(0, -2))
+    _, adec, _ = md.time_device(half, args.warmup, world)
+    adec = dist_max(adec, world)
+    _check_status(md, "mixed-step decodes alone")
+    del md
+    torch.cuda.empty_cache()
     mixed_info = {
         "workload": WORKLOAD_TEXT[MIXED],
         "tokens_per_s_per_layer": world * mw["tokens"] / (mms * 1e-3),
         "ms_per_step": mms,
+        "serial_ms_per_step": sms_,
+        "overlap_speedup": sms_ / mms,
+        "graph_ms_per_step": mgraph,
         "decode_kernel_ms": mdec,
         "decode_gbs": mw["decode_bytes"] / (mdec * 1e-3) / 1e9,
-        "chunk_and_write_ms": rest_ms,
-        "chunk_tflops_upper": mw["chunk_flops"] / (rest_ms * 1e-3) / 1e12,
+        "serial_decode_kernel_ms": sdec,
+        "serial_prefill_kernel_ms": spf,
+        "serial_prefill_tflops": mw["chunk_flops"] / (spf * 1e-3) / 1e12,
+        "decode_alone_kernel_ms": adec,
+        "decode_alone_gbs": mw["decode_bytes"] / (adec * 1e-3) / 1e9,
+        "decode_in_step_vs_alone": adec / mdec,
+        "timed": "ms_per_step: pa_cache_write + pa_forward back to back with no events inside a "
+                 "step (prefill kernel on the library side stream beside the decode kernel); "
+                 "serial_ms_per_step: the same with pa_set_prefill_overlap(0) (prefill kernel "
+                 "on the caller's stream before the decode kernel); kernel times: medians of "
+                 "events around each kernel in a second loop (overlapped, the prefill kernel's "
+                 "stop event waits for CTAs that only start when decode CTAs leave, so only the "
+                 "serial prefill time is reported); decode_alone: the 192 decode requests as a "
+                 "step of their own",
     }
-    mixed_info["graph_ms_per_step"] = dist_max(mixed.time_graph(max(3, args.steps // 2),
-                                                                 args.warmup, world), world)
-    if int(mixed.status.item()) != 0:
-        raise RuntimeError(f"mixed-step device status {int(mixed.status.item())}")
-    del mixed
-    torch.cuda.empty_cache()
 
-    # the mixed step's two prefill chunks alone: the tensor-core kernel's own rate
-    pf = StepRunner(MIXED, seed_offset=rank * 1000 if world > 1 else 0, requests=slice(-2, None))
-    pms, _ = pf.time_device(max(3, args.steps // 2), args.warmup, world, flush=True)
-    pms = dist_max(pms, world)
-    bf16_peak = measured_bf16_tflops()
-    pf_tflops = pf.work["chunk_flops"] / (pms * 1e-3) / 1e12
+    # ---- the mixed step's two prefill chunks alone: the tensor-core kernel's own rate
+    pf = StepRunner(MIXED, seed_offset=seed_off, requests=slice(-2, None))
+    pms, _, ppf = pf.time_device(half, args.warmup, world, flush=True)
+    pms, ppf = dist_max(pms, world), dist_max(ppf, world)
+    _check_status(pf, "prefill chunks")
+    pf_tflops = pf.work["chunk_flops"] / (ppf * 1e-3) / 1e12
     prefill_info = {
         "workload": "the mixed step's two chunked prefills alone: 512 tokens at prior 0 and "
                     "512 at prior 1536, Llama-3-8B heads, bf16",
         "ms_per_step": pms,
+        "prefill_kernel_ms": ppf,
         "tflops": pf_tflops,
-        "frac_of_bf16_peak": pf_tflops / bf16_peak[0] if bf16_peak[0] else None,
+        "frac_of_bf16_peak": pf_tflops / bf16_peak[0],
         "frac_of_nominal_bf16": pf_tflops / NOMINAL_BF16_TFLOPS,
+        "step_tflops": pf.work["chunk_flops"] / (pms * 1e-3) / 1e12,
         "peak_tflops": bf16_peak[0], "peak_source": bf16_peak[1],
         "flops": pf.work["chunk_flops"],
-        "timed": "pa_cache_write + pa_forward (plan, tensor-core prefill kernel); L2 flushed "
-                 "(256 MiB write) before every step, outside the timed events; flops = 4 x D x "
-                 "Hq x visible (query, key) pairs",
+        "timed": "tflops: flops / median event time of the tensor-core prefill kernel; "
+                 "ms_per_step: pa_cache_write + pa_forward (plan, prefill kernel); L2 "
+                 + StepRunner.FLUSH_TEXT + "; flops = 4 x D x Hq x visible (query, key) pairs",
     }
-    if int(pf.status.item()) != 0:
-        raise RuntimeError(f"prefill step device status {int(pf.status.item())}")
     del pf
     torch.cuda.empty_cache()
 
-    # one long chunk: the tensor-core kernel in its steady state (56 KV tiles a unit)
-    pl = StepRunner("long_prefill_chunk", seed_offset=rank * 1000 if world > 1 else 0)
-    lms, _ = pl.time_device(max(3, args.steps // 2), args.warmup, world, flush=True)
-    lms = dist_max(lms, world)
-    pl_tflops = pl.work["chunk_flops"] / (lms * 1e-3) / 1e12
+    # ---- one long chunk: the tensor-core kernel in its steady state (56 KV tiles a unit)
+    pl = StepRunner("long_prefill_chunk", seed_offset=seed_off)
+    lms, _, lpf = pl.time_device(half, args.warmup, world, flush=True)
+    lms, lpf = dist_max(lms, world), dist_max(lpf, world)
+    _check_status(pl, "long prefill")
+    pl_tflops = pl.work["chunk_flops"] / (lpf * 1e-3) / 1e12
     prefill_long_info = {
         "workload": "one 2048-token prefill chunk at prior context 6144 (rows see up to 8192 "
                     "keys), Llama-3-8B heads, bf16",
         "ms_per_step": lms,
+        "prefill_kernel_ms": lpf,
         "tflops": pl_tflops,
-        "frac_of_bf16_peak": pl_tflops / bf16_peak[0] if bf16_peak[0] else None,
+        "frac_of_bf16_peak": pl_tflops / bf16_peak[0],
         "frac_of_nominal_bf16": pl_tflops / NOMINAL_BF16_TFLOPS,
+        "step_tflops": pl.work["chunk_flops"] / (lms * 1e-3) / 1e12,
         "peak_tflops": bf16_peak[0], "peak_source": bf16_peak[1],
         "flops": pl.work["chunk_flops"],
         "timed": "as prefill_chunks",
     }
-    if int(pl.status.item()) != 0:
-        raise RuntimeError(f"long prefill device status {int(pl.status.item())}")
     del pl
     torch.cuda.empty_cache()
 
-    # the headline shape over an 8-bit (E4M3) KV cache: half the KV bytes per token
-    f8 = StepRunner(HEADLINE, seed_offset=rank * 1000 if world > 1 else 0, fp8_scales=(0.01, 0.01))
-    fms, fdec = f8.time_device(args.steps, args.warmup, world)
+    # ---- short chunks after long prompts: prefill units split over their KV
+    lp = StepRunner("long_prior_chunks", seed_offset=seed_off)
+    pps, _, ppk = lp.time_device(half, args.warmup, world, flush=True)
+    pps, ppk = dist_max(pps, world), dist_max(ppk, world)
+    _check_status(lp, "long-prior chunks")
+    lpw = lp.work
+    long_prior_info = {
+        "workload": "short prefill chunks late in long prompts: 64 tokens after 32768 and 16 "
+                    "after 98304, Llama-3-8B heads, bf16",
+        "ms_per_step": pps,
+        "prefill_kernel_ms": ppk,
+        "kv_gbs": lpw["chunk_bytes"] / (ppk * 1e-3) / 1e9,
+        "frac_of_hbm_peak": lpw["chunk_bytes"] / (ppk * 1e-3) / 1e9 / peak,
+        "tflops": lpw["chunk_flops"] / (ppk * 1e-3) / 1e12,
+        "bound": "hbm: each query tile reads all its prior KV once (bytes = unique KV slots "
+                 "read + q + out + block tables)",
+        "algorithmic_bytes": lpw["chunk_bytes"], "flops": lpw["chunk_flops"],
+        "l2": StepRunner.FLUSH_TEXT,
+    }
+    del lp
+    torch.cuda.empty_cache()
+
+    # ---- long-context decode: 16 requests of 32K-128K tokens, split-KV + merge
+    lc = StepRunner("long_context_decode", seed_offset=seed_off)
+    cms, cdec, _ = lc.time_device(half, args.warmup, world)
+    cms, cdec = dist_max(cms, world), dist_max(cdec, world)
+    _check_status(lc, "long-context decode")
+    lw = lc.work
+    long_info = {
+        "workload": "long-context decode: batch 16, context U[32768,131072], 32 q / 8 kv heads, "
+                    "D=128, bf16, random block tables over a 9 GB pool",
+        "ms_per_step": cms,
+        "decode_kernel_ms": cdec,
+        "decode_gbs": lw["decode_bytes"] / (cdec * 1e-3) / 1e9,
+        "decode_frac_of_peak": lw["decode_bytes"] / (cdec * 1e-3) / 1e9 / peak,
+        "step_gbs": world * lw["step_bytes"] / (cms * 1e-3) / 1e9,
+        "algorithmic_bytes_per_launch": lw["decode_bytes"],
+        "l2": "no flush: KV read per step (5.8 GB) > L2",
+    }
+    del lc
+    torch.cuda.empty_cache()
+
+    # ---- the headline shape over an 8-bit (E4M3) KV cache: half the KV bytes per token
+    f8 = StepRunner(HEADLINE, seed_offset=seed_off, fp8_scales=(0.01, 0.01))
+    fms, fdec, _ = f8.time_device(args.steps, args.warmup, world)
     fms, fdec = dist_max(fms, world), dist_max(fdec, world)
+    _check_status(f8, "fp8 decode")
     fkv = f8.work["decode_bytes"] - f8.work["kv_bytes"] // 2  # KV counted at 1 byte/element
     fp8_info = {
         "workload": WORKLOAD_TEXT[HEADLINE] + ", KV cache FP8 E4M3 (per-tensor scales)",
         "ms_per_step": fms, "decode_kernel_ms": fdec,
         "decode_gbs": fkv / (fdec * 1e-3) / 1e9,
-        "decode_frac_of_peak": fkv / (fdec * 1e-3) / 1e9 / measured_peaks()[0],
+        "decode_frac_of_peak": fkv / (fdec * 1e-3) / 1e9 / peak,
         "tokens_per_s": world * f8.spec.num_tokens / (fms * 1e-3),
     }
-    if int(f8.status.item()) != 0:
-        raise RuntimeError(f"fp8 step device status {int(f8.status.item())}")
     del f8
     torch.cuda.empty_cache()
 
-    # a small decode step (79 MB of KV) where launch overhead is visible
-    small = StepRunner("tinyllama_decode", seed_offset=rank * 1000 if world > 1 else 0)
-    sms, sdec = small.time_device(args.steps, args.warmup, world, flush=True)
+    # ---- a small decode step (79 MB of KV) where launch overhead is visible
+    small = StepRunner("tinyllama_decode", seed_offset=seed_off)
+    sms, sdec, _ = small.time_device(args.steps, args.warmup, world, flush=True)
     sms, sdec = dist_max(sms, world), dist_max(sdec, world)
     sgraph = dist_max(small.time_graph(args.steps, args.warmup, world, flush=True), world)
+    _check_status(small, "tinyllama decode")
     sw = small.work
     small_info = {
         "workload": "TinyLlama-1.1B single-layer decode: batch 64, 32 q / 4 kv heads, D=64, bf16, "
                     "context U[128,2048]",
         "ms_per_step": sms, "graph_ms_per_step": sgraph, "decode_kernel_ms": sdec,
         "decode_gbs": sw["decode_bytes"] / (sdec * 1e-3) / 1e9,
+        "decode_frac_of_peak": sw["decode_bytes"] / (sdec * 1e-3) / 1e9 / peak,
         "graph_step_gbs": world * sw["step_bytes"] / (sgraph * 1e-3) / 1e9,
-        "l2": "flushed (256 MiB write) before every step, outside the timed events",
+        "l2": StepRunner.FLUSH_TEXT,
     }
     del small
+    torch.cuda.empty_cache()
+
+    # ---- the tiny fp32 decode step: 4 requests, latency-bound
+    tiny = StepRunner("tiny_decode_f32", seed_offset=seed_off)
+    tms, tdec, _ = tiny.time_device(args.steps, args.warmup, world, flush=True)
+    tms, tdec = dist_max(tms, world), dist_max(tdec, world)
+    tgraph = dist_max(tiny.time_graph(args.steps, args.warmup, world, flush=True), world)
+    _check_status(tiny, "tiny fp32 decode")
+    tiny_info = {
+        "workload": "tiny fp32 decode: 4 requests, seq_lens {1,17,33,64}, 4 q / 2 kv heads, "
+                    "D=64, 32-block pool",
+        "us_per_step": tms * 1e3, "graph_us_per_step": tgraph * 1e3,
+        "decode_kernel_us": tdec * 1e3,
+        "decode_bytes": tiny.work["decode_bytes"],
+        "l2": StepRunner.FLUSH_TEXT,
+    }
+    del tiny
     torch.cuda.empty_cache()
 
     line = {
@@ -721,7 +831,7 @@ def run_gpu_arm(args):
         "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
         "config": {"workload": WORKLOAD_TEXT[HEADLINE], "step": "pa_cache_write + pa_forward",
                    "l2": "no flush: KV read per step (1.4 GB) > L2 (126 MB)",
-                   "parallelism": "replicas" if world > 1 else "single GPU",
+                   "parallelism": f"{world} replicas" if world > 1 else "single GPU",
                    "algorithmic_bytes_per_step": w["step_bytes"]},
         "roofline": {"bound": "hbm", "kernel": "attn_mma_kernel<128,4,1,4,2> (decode)",
                      "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
@@ -734,10 +844,13 @@ def run_gpu_arm(args):
         "gpu_launches": launches,
         "clocks": clock_info,
         "mixed": mixed_info,
-        "prefill_chunks": prefill_info,
-        "prefill_long": prefill_long_info,
+        "long_context_decode": long_info,
+        "tiny_decode_f32": tiny_info,
         "tinyllama_decode": small_info,
         "fp8_kv": fp8_info,
+        "prefill_chunks": prefill_info,
+        "prefill_long": prefill_long_info,
+        "long_prior_chunks": long_prior_info,
     }
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         o = time_oracle(HEADLINE, min_seconds=args.oracle_seconds, stride=args.oracle_stride)
@@ -823,6 +936,22 @@ def run_ncu_case(spec_arg: str, iters: int = 3, fp8: bool = False) -> None:
     print(json.dumps({"ncu_case": spec_arg, "tokens": spec.num_tokens, "ok": True}))
 
 
+def free_port() -> int:
+    import socket
+    with socket.socket(socket.AF_INET, socket.SOCK_STREAM) as sk:
+        sk.bind(("127.0.0.1", 0))
+        return sk.getsockname()[1]
+
+
+def spawn_replicas(n: int, script: str, argv: list[str], env: dict | None = None) -> int:
+    """Run `script argv` as n ranks on this node under torch.distributed.run
+    (rendezvous on 127.0.0.1, a free port); the ranks' output passes through.
+    Returns the launcher's exit code."""
+    cmd = [sys.executable, "-m", "torch.distributed.run", "--nnodes=1", f"--nproc-per-node={n}",
+           "--master-addr=127.0.0.1", f"--master-port={free_port()}", script, *argv]
+    return subprocess.run(cmd, env=env).returncode
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -852,6 +981,10 @@ def main():
         args.warmup = 3
     if args.impl == "reference":
         run_reference_arm(args)
+    elif args.gpus > 1 and "WORLD_SIZE" not in os.environ:
+        # one process per GPU: start the ranks here (barrier and max-over-ranks
+        # timing happen inside each rank's run)
+        sys.exit(spawn_replicas(args.gpus, os.path.abspath(__file__), sys.argv[1:]))
     else:
         run_gpu_arm(args)
 

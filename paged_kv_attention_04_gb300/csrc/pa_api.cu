@@ -11,14 +11,16 @@
 
 namespace pa {
 cudaError_t launch_attn_mma_bf16(const AttnParams& p, int head_size, int group, int positions,
-                                 int num_sms, cudaStream_t stream);
+                                 int num_sms, cudaStream_t stream, int* grid_only);
 cudaError_t launch_attn_cc_f32(const AttnParams& p, int head_size, int group, int positions,
-                               int num_sms, cudaStream_t stream);
+                               int num_sms, cudaStream_t stream, int* grid_only);
 
 cudaError_t launch_attn_by_dtype(const AttnParams& p, pa_dtype dtype, int head_size, int group,
-                                 int positions, int num_sms, cudaStream_t stream) {
-  return dtype == PA_BF16 ? launch_attn_mma_bf16(p, head_size, group, positions, num_sms, stream)
-                          : launch_attn_cc_f32(p, head_size, group, positions, num_sms, stream);
+                                 int positions, int num_sms, cudaStream_t stream,
+                                 int* grid_only) {
+  return dtype == PA_BF16
+             ? launch_attn_mma_bf16(p, head_size, group, positions, num_sms, stream, grid_only)
+             : launch_attn_cc_f32(p, head_size, group, positions, num_sms, stream, grid_only);
 }
 
 namespace {
@@ -94,9 +96,6 @@ int check_layout(const pa_layout* L) {
 int blocks_per_split(const pa_layout* L) {
   (void)L;
   int b = PA_SPLIT_BLOCKS;
-#if defined(PA_SPLIT_BLOCKS_SMALL) && PA_SPLIT_BLOCKS_SMALL > 0
-  if (PA_SPLIT_BLOCKS_SMALL < b) b = PA_SPLIT_BLOCKS_SMALL;
-#endif
   if (b > kMaxUnitBlocks) b = kMaxUnitBlocks;
   return b < 1 ? 1 : b;
 }
@@ -112,12 +111,20 @@ Capacity capacity(const pa_layout* L, int B, int T, int max_seq_len) {
   if (cdiv(max_nb, kMaxUnitBlocks) > splits) splits = cdiv(max_nb, kMaxUnitBlocks);
   const long long multi = T > B ? (T - B < B ? T - B : B) : 0;  // requests with q_len >= 2
   c.decode_tiles = B;
-  c.decode_items = static_cast<long long>(B) * splits;
+  // plus room for the finer splits of small steps: the plan keeps a small
+  // step's decode items within requests + blocks / split, and raises its
+  // split size until they fit this capacity
+  c.decode_items = static_cast<long long>(B) * splits + cdiv(kSmallStepUnits, L->num_kv_heads);
   c.small_tiles = (T > B ? cdiv(T - B, small_positions(L)) : 0) + multi;
   c.small_items = c.small_tiles * splits;
   const long long group = L->num_q_heads / L->num_kv_heads;
   c.prefill_tiles = (L->dtype == PA_BF16 && !fp8_cache(L))
                         ? cdiv(static_cast<long long>(T) * group, kPrefillRows) + multi : 0;
+  // a step that can hold a chunk of kPrefillMinQlen tokens may split its
+  // prefill query tiles' KV
+  c.prefill_slots = (c.prefill_tiles > 0 && T - B >= kPrefillMinQlen - 1)
+                        ? cdiv(kPrefillSplitUnits, L->num_kv_heads) : 0;
+  c.prefill_items = c.prefill_tiles + c.prefill_slots;
   return c;
 }
 
@@ -182,7 +189,8 @@ WsLayout ws_layout(const Capacity& cap, int Hkv, int D, int group) {
   w.tiles_d = take(sizeof(int4) * cap.decode_tiles);
   w.items_s = take(sizeof(int4) * cap.small_items);
   w.tiles_s = take(sizeof(int4) * cap.small_tiles);
-  w.tiles_p = take(sizeof(int4) * cap.prefill_tiles);
+  w.items_p = take(sizeof(PfItem) * cap.prefill_items);
+  w.cnt_p = take(sizeof(int) * cap.prefill_tiles * Hkv);
   w.recs_d = take(sizeof(UnitRec) * cap.decode_items);
   w.recs_s = take(sizeof(UnitRec) * cap.small_items);
   w.order_d = take(sizeof(int) * cap.decode_items);
@@ -192,6 +200,8 @@ WsLayout ws_layout(const Capacity& cap, int Hkv, int D, int group) {
   w.part_ml_d = take(sizeof(float) * cap.decode_items * Hkv * rows_d * 2);
   w.part_acc_s = take(sizeof(float) * cap.small_items * Hkv * rows_s * D);
   w.part_ml_s = take(sizeof(float) * cap.small_items * Hkv * rows_s * 2);
+  w.part_acc_p = take(sizeof(float) * cap.prefill_slots * Hkv * kPrefillRows * D);
+  w.part_ml_p = take(sizeof(float) * cap.prefill_slots * Hkv * kPrefillRows * 2);
   w.total = off;
   return w;
 }
@@ -305,6 +315,7 @@ int pa_forward(const void* q, const void* k_cache, const void* v_cache,
   if (int rc = num_sms_of_current_device(&num_sms)) return rc;
 
   cudaStream_t st = static_cast<cudaStream_t>(stream);
+  cudaError_t e = cudaSuccess;
   char* ws = static_cast<char*>(workspace);
   int* hdr = reinterpret_cast<int*>(ws + lay.hdr);
 
@@ -318,6 +329,14 @@ int pa_forward(const void* q, const void* k_cache, const void* v_cache,
   pp.max_blocks_per_seq = max_blocks_per_seq;
   pp.bps = blocks_per_split(layout);
   pp.num_sms = num_sms;
+  {
+    AttnParams none{};
+    e = fp8_cache(layout)
+            ? launch_attn_fp8(none, layout->head_size, group, 1, num_sms, st, &pp.num_ctas)
+            : launch_attn_by_dtype(none, layout->dtype, layout->head_size, group, 1, num_sms, st,
+                                   &pp.num_ctas);
+    if (e != cudaSuccess) return fail_cuda(e, "decode grid size");
+  }
   pp.small_positions = small_positions(layout);
   const bool tc_prefill = layout->dtype == PA_BF16 && !fp8_cache(layout);
   pp.prefill_min_qlen = tc_prefill ? kPrefillMinQlen : 0x7fffffff;
@@ -328,7 +347,7 @@ int pa_forward(const void* q, const void* k_cache, const void* v_cache,
   pp.ws = ws;
   pp.lay = lay;
   pp.status = status;
-  cudaError_t e = launch_plan(pp, st);
+  e = launch_plan(pp, st);
   if (e != cudaSuccess) return fail_cuda(e, "plan launch");
 
   // Chunked prefill (tensor cores) runs on a side stream, launched before the
@@ -361,14 +380,14 @@ int pa_forward(const void* q, const void* k_cache, const void* v_cache,
 
   if (run_prefill) {
     AttnParams pf = ap;
-    pf.n_items = hdr + kHdrPrefillTiles;
+    pf.n_items = hdr + kHdrPrefillItems;
     pf.next = hdr + kHdrPrefillNext;
-    pf.items = reinterpret_cast<const int4*>(ws + lay.tiles_p);
+    pf.items = reinterpret_cast<const int4*>(ws + lay.items_p);  // PfItem pairs
     pf.recs = nullptr;
     pf.tiles = nullptr;
-    pf.merge_cnt = nullptr;
-    pf.part_acc = nullptr;
-    pf.part_ml = nullptr;
+    pf.merge_cnt = reinterpret_cast<int*>(ws + lay.cnt_p);
+    pf.part_acc = reinterpret_cast<float*>(ws + lay.part_acc_p);
+    pf.part_ml = reinterpret_cast<float*>(ws + lay.part_ml_p);
     cudaStream_t pst = st;
     if (fork) {
       e = cudaEventRecord(side->fork, st);

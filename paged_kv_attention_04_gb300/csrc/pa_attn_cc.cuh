@@ -352,7 +352,8 @@ __global__ void __launch_bounds__(CcCfg<T, D, G, P>::kThreads)
 
 // Occupancy and shared-memory opt-in, computed once per device.
 template <typename T, int D, int G, int P>
-cudaError_t launch_cc(const AttnParams& p, int num_sms, cudaStream_t stream) {
+cudaError_t launch_cc(const AttnParams& p, int num_sms, cudaStream_t stream,
+                      int* grid_only = nullptr) {
   using C = CcCfg<T, D, G, P>;
   static int ctas_per_sm[64] = {0};
   int dev = 0;
@@ -370,33 +371,37 @@ cudaError_t launch_cc(const AttnParams& p, int num_sms, cudaStream_t stream) {
     ctas_per_sm[dev] = n > 0 ? n : 1;
   }
   const int grid = num_sms * ctas_per_sm[dev];
+  if (grid_only) {
+    *grid_only = grid;
+    return cudaSuccess;
+  }
   attn_cc_kernel<T, D, G, P><<<grid, C::kThreads, C::kSmemBytes, stream>>>(p);
   return cudaGetLastError();
 }
 
 template <typename T, int D>
 cudaError_t dispatch_cc_group(const AttnParams& p, int group, int positions, int num_sms,
-                              cudaStream_t stream) {
+                              cudaStream_t stream, int* grid_only) {
   const bool dec = positions == 1;
   switch (group) {
-    case 1: return dec ? launch_cc<T, D, 1, 1>(p, num_sms, stream)
-                       : launch_cc<T, D, 1, kSmallRows / 1>(p, num_sms, stream);
-    case 2: return dec ? launch_cc<T, D, 2, 1>(p, num_sms, stream)
-                       : launch_cc<T, D, 2, kSmallRows / 2>(p, num_sms, stream);
-    case 4: return dec ? launch_cc<T, D, 4, 1>(p, num_sms, stream)
-                       : launch_cc<T, D, 4, kSmallRows / 4>(p, num_sms, stream);
-    case 8: return dec ? launch_cc<T, D, 8, 1>(p, num_sms, stream)
-                       : launch_cc<T, D, 8, kSmallRows / 8>(p, num_sms, stream);
+    case 1: return dec ? launch_cc<T, D, 1, 1>(p, num_sms, stream, grid_only)
+                       : launch_cc<T, D, 1, kSmallRows / 1>(p, num_sms, stream, grid_only);
+    case 2: return dec ? launch_cc<T, D, 2, 1>(p, num_sms, stream, grid_only)
+                       : launch_cc<T, D, 2, kSmallRows / 2>(p, num_sms, stream, grid_only);
+    case 4: return dec ? launch_cc<T, D, 4, 1>(p, num_sms, stream, grid_only)
+                       : launch_cc<T, D, 4, kSmallRows / 4>(p, num_sms, stream, grid_only);
+    case 8: return dec ? launch_cc<T, D, 8, 1>(p, num_sms, stream, grid_only)
+                       : launch_cc<T, D, 8, kSmallRows / 8>(p, num_sms, stream, grid_only);
     default: return cudaErrorInvalidValue;
   }
 }
 
 template <typename T>
 cudaError_t dispatch_cc(const AttnParams& p, int head_size, int group, int positions, int num_sms,
-                        cudaStream_t stream) {
+                        cudaStream_t stream, int* grid_only) {
   switch (head_size) {
-    case 64: return dispatch_cc_group<T, 64>(p, group, positions, num_sms, stream);
-    case 128: return dispatch_cc_group<T, 128>(p, group, positions, num_sms, stream);
+    case 64: return dispatch_cc_group<T, 64>(p, group, positions, num_sms, stream, grid_only);
+    case 128: return dispatch_cc_group<T, 128>(p, group, positions, num_sms, stream, grid_only);
     default: return cudaErrorInvalidValue;
   }
 }

@@ -419,26 +419,47 @@ __global__ void __launch_bounds__(MmaCfg<D, G, P, NW, NS, F8>::kThreads,
       last = __shfl_sync(0xffffffffu, last, 0);
       if (last) {
         __threadfence();
+        // The partials sit in L2; each group of kMergeChunk splits is loaded
+        // with independent loads before any is used, so a merge costs one
+        // round trip per group instead of two per split.
+        constexpr int kMergeChunk = 4;
+#pragma unroll 2
         for (int idx = lane; idx < R * D / 4; idx += 32) {
           const int row = (idx * 4) / D, d = idx * 4 - row * D;
           const int jj = row / G, hh = row - jj * G;
           if (jj >= u.npos) continue;
           float M = -CUDART_INF_F, den = 0.f;
           float4 num = make_float4(0.f, 0.f, 0.f, 0.f);
-          for (int sp = 0; sp < u.nsplit; ++sp) {
-            const long long pb = (static_cast<long long>(u.first + sp) * Hkv + u.g) * R + row;
-            const float2 ml = __ldcg(reinterpret_cast<const float2*>(p.part_ml + pb * 2));
-            if (ml.x == -CUDART_INF_F) continue;
-            const float4 a4 = __ldcg(reinterpret_cast<const float4*>(p.part_acc + pb * D + d));
-            if (ml.x > M) {  // online rescale to the new maximum
-              const float sc = exp2f(M - ml.x);
-              num.x *= sc; num.y *= sc; num.z *= sc; num.w *= sc; den *= sc;
-              M = ml.x;
+          for (int sp0 = 0; sp0 < u.nsplit; sp0 += kMergeChunk) {
+            float2 ml[kMergeChunk];
+            float4 a4[kMergeChunk];
+#pragma unroll
+            for (int j = 0; j < kMergeChunk; ++j) {
+              ml[j] = make_float2(-CUDART_INF_F, 0.f);
+              a4[j] = make_float4(0.f, 0.f, 0.f, 0.f);
+              if (sp0 + j < u.nsplit) {
+                const long long pb = (static_cast<long long>(u.first + sp0 + j) * Hkv + u.g) * R + row;
+                ml[j] = __ldcg(reinterpret_cast<const float2*>(p.part_ml + pb * 2));
+                a4[j] = __ldcg(reinterpret_cast<const float4*>(p.part_acc + pb * D + d));
+              }
             }
-            const float f = exp2f(ml.x - M);
-            num.x = fmaf(a4.x, f, num.x); num.y = fmaf(a4.y, f, num.y);
-            num.z = fmaf(a4.z, f, num.z); num.w = fmaf(a4.w, f, num.w);
-            den = fmaf(ml.y, f, den);
+            // a split with no visible key for this row holds (-inf, 0) and zeros
+            float mc = M;
+#pragma unroll
+            for (int j = 0; j < kMergeChunk; ++j) mc = fmaxf(mc, ml[j].x);
+            if (mc == -CUDART_INF_F) continue;
+            if (mc > M) {  // rescale the running sums to the new maximum
+              const float sc = exp2f(M - mc);  // 0 while nothing was visible
+              num.x *= sc; num.y *= sc; num.z *= sc; num.w *= sc; den *= sc;
+              M = mc;
+            }
+#pragma unroll
+            for (int j = 0; j < kMergeChunk; ++j) {
+              const float f = exp2f(ml[j].x - M);  // 0 for an empty split
+              num.x = fmaf(a4[j].x, f, num.x); num.y = fmaf(a4[j].y, f, num.y);
+              num.z = fmaf(a4[j].z, f, num.z); num.w = fmaf(a4[j].w, f, num.w);
+              den = fmaf(ml[j].y, f, den);
+            }
           }
           const long long tok = u.a + u.j0 + jj;
           const float inv = p.out_scale / den;
@@ -748,8 +769,11 @@ __global__ void __launch_bounds__(MmaCfg<D, G, P, NW, NS, F8>::kThreads,
   cp_async_wait<0>();
 }
 
+// Launches the kernel, or with grid_only set only stores the grid size it
+// would use (CTAs per SM by occupancy x SMs).
 template <int D, int G, int P, int NW, int NS, bool F8 = false>
-cudaError_t launch_mma(const AttnParams& p, int num_sms, cudaStream_t stream) {
+cudaError_t launch_mma(const AttnParams& p, int num_sms, cudaStream_t stream,
+                       int* grid_only = nullptr) {
   using C = MmaCfg<D, G, P, NW, NS, F8>;
   static int ctas_per_sm[64] = {0};
   int dev = 0;
@@ -765,6 +789,10 @@ cudaError_t launch_mma(const AttnParams& p, int num_sms, cudaStream_t stream) {
                                                       C::kThreads, C::kSmemBytes);
     if (e != cudaSuccess) return e;
     ctas_per_sm[dev] = n > 0 ? n : 1;
+  }
+  if (grid_only) {
+    *grid_only = num_sms * ctas_per_sm[dev];
+    return cudaSuccess;
   }
   // right after the plan kernel the launch may overlap its tail (the kernel
   // waits for the plan before reading the work lists)

@@ -14,6 +14,12 @@ constexpr int kMaxSplits = 64;        // KV splits per tile are kept at or below
 constexpr int kMaxUnitBlocks = 256;   // ... unless a split would exceed this many blocks
 constexpr int kPrefillRows = 128;     // query rows per tensor-core prefill tile
 constexpr int kPrefillMinQlen = 16;   // bf16 chunks at least this long use the tensor-core kernel
+constexpr int kSmallStepUnits = 2048; // extra decode units (items x kv heads) a workspace holds
+                                      // for the finer splits of small steps
+constexpr int kPrefillKeys = 128;     // keys per KV tile of the tensor-core prefill kernel
+constexpr int kMinPrefillSplitTiles = 4;  // smallest KV piece of a split prefill query tile
+constexpr int kPrefillSplitUnits = 256;   // split prefill units (items x kv heads) a workspace
+                                          // holds partial states for
 
 // Work-list classes written by the plan kernel.
 enum ReqClass : int { kClassNone = 0, kClassDecode = 1, kClassSmall = 2, kClassPrefill = 3 };
@@ -22,7 +28,7 @@ enum ReqClass : int { kClassNone = 0, kClassDecode = 1, kClassSmall = 2, kClassP
 enum Hdr : int {
   kHdrDecodeItems = 0, kHdrDecodeTiles, kHdrDecodeNext,
   kHdrSmallItems, kHdrSmallTiles, kHdrSmallNext,
-  kHdrPrefillTiles, kHdrPrefillNext,
+  kHdrPrefillItems, kHdrPrefillNext,
   kHdrWords = 16
 };
 
@@ -30,13 +36,16 @@ enum Hdr : int {
 struct Capacity {
   long long decode_items, decode_tiles;
   long long small_items, small_tiles;
-  long long prefill_tiles;
+  long long prefill_tiles;  // query tiles of 128 rows
+  long long prefill_items;  // query tiles or pieces of their KV
+  long long prefill_slots;  // pieces with a partial state (query tiles split in several)
 };
 
 // Byte offsets of every workspace region (all 256-byte aligned).
 struct WsLayout {
   size_t hdr;
-  size_t items_d, tiles_d, items_s, tiles_s, tiles_p;
+  size_t items_d, tiles_d, items_s, tiles_s;
+  size_t items_p, cnt_p, part_acc_p, part_ml_p;  // prefill items, merge counters, partials
   size_t recs_d, recs_s;  // per item: 3 x int4 unit records (see UnitRec)
   size_t order_d;         // decode items in dispatch order (largest split first)
   size_t cnt_d, cnt_s;
@@ -49,7 +58,9 @@ struct PlanParams {
   const int32_t* qsl;
   int num_seqs, num_tokens, max_query_len, max_seq_len, max_blocks_per_seq;
   int bps;              // KV blocks per split (minimum; long requests use larger splits)
-  int num_sms;          // SMs of the device (the plan sizes splits from the step's KV per SM)
+  int num_sms;          // SMs of the device
+  int num_ctas;         // CTAs of the decode kernel's grid (the plan sizes splits from the
+                        // step's KV per CTA)
   int small_positions;  // query positions per small-q tile
   int prefill_min_qlen; // requests with q_len >= this go to the tensor-core kernel
   int prefill_rows;     // query rows (positions x group) per prefill tile
@@ -69,6 +80,15 @@ struct PlanParams {
 //        last visible key of this split, 0}
 struct UnitRec {
   int4 a, b, c;
+};
+
+// One unit of tensor-core prefill work (x num_kv_heads):
+//   a = {r, query tile m of the request, first KV tile, one past the last KV tile}
+//   b = {query tile index in the step, piece index sp, pieces of the tile ns,
+//        first partial-state slot of the tile (-1 when ns = 1: the piece
+//        writes the output); piece sp uses slot b.w + sp}
+struct PfItem {
+  int4 a, b;
 };
 
 // One unit of CUDA-core attention work: request r, query tile m, KV split s,
@@ -119,12 +139,15 @@ cudaError_t launch_prefill_tc(const AttnParams& p, int head_size, int group, int
                               cudaStream_t stream);
 // Split-KV attention over the decode or few-token list, by element type:
 // bf16 runs the warp-level tensor-core (mma.sync) kernel, fp32 the CUDA-core
-// kernel.  positions: 1 (decode list) or the few-token tile height.  Returns
-// cudaErrorInvalidValue for an unbuilt combination.
+// kernel.  positions: 1 (decode list) or the few-token tile height.  With
+// grid_only set nothing is launched: the grid size (CTAs) the launch would
+// use is stored there.  Returns cudaErrorInvalidValue for an unbuilt
+// combination.
 cudaError_t launch_attn_by_dtype(const AttnParams& p, pa_dtype dtype, int head_size, int group,
-                                 int positions, int num_sms, cudaStream_t stream);
+                                 int positions, int num_sms, cudaStream_t stream,
+                                 int* grid_only = nullptr);
 // bf16 q/out over an FP8 (E4M3) cache (tensor-core decode and few-token tiles).
 cudaError_t launch_attn_fp8(const AttnParams& p, int head_size, int group, int positions,
-                            int num_sms, cudaStream_t stream);
+                            int num_sms, cudaStream_t stream, int* grid_only = nullptr);
 
 }  // namespace pa

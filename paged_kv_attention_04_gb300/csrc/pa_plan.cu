@@ -30,15 +30,16 @@ constexpr int kPlanThreads = 1024;
 #ifndef PA_UNITS_PER_CTA
 #define PA_UNITS_PER_CTA 8  // split-size target: decode units per CTA (see plan_kernel)
 #endif
-#ifndef PA_SPLIT_BLOCKS_SMALL
-#define PA_SPLIT_BLOCKS_SMALL 0  // > 0: smallest split of steps with little KV per CTA
+#ifndef PA_SMALL_SPLIT_PCT
+#define PA_SMALL_SPLIT_PCT 150  // small-step decode split, % of the even per-CTA share
 #endif
-#ifndef PA_SMALL_UNITS
-#define PA_SMALL_UNITS 2
+#ifndef PA_SPLIT_MIN
+#define PA_SPLIT_MIN 16  // smallest decode split (blocks)
 #endif
 
-// decode items, decode tiles, small items, small tiles, prefill tiles, long decode items
-constexpr int kLists = 6;
+// decode items, decode tiles, small items, small tiles, prefill items, long decode items,
+// prefill query tiles, prefill partial slots
+constexpr int kLists = 8;
 
 // Exclusive scan of kLists ints per thread across the CTA, all lists at once;
 // `total` receives each list's CTA total.
@@ -103,6 +104,9 @@ __global__ void __launch_bounds__(kPlanThreads, 1) plan_kernel(PlanParams p) {
   __shared__ int err;
   __shared__ int size_hist[kMaxUnitBlocks + 1];  // short decode items per size (blocks)
   __shared__ unsigned long long s_blocks;        // KV blocks of the requests that split
+  __shared__ unsigned long long s_blocks_d;      // ... of the decode requests among them
+  __shared__ unsigned long long s_pf_tiles;      // prefill query tiles of the step
+  __shared__ unsigned long long s_pf_kv;         // KV tiles those query tiles see, summed
   static_assert(kMaxUnitBlocks == 8 * 32, "the dispatch-order scan gives each lane 8 sizes");
   // The attention kernel that follows may become resident now; it waits for
   // this grid to finish before it reads the work lists.  This grid itself may
@@ -125,13 +129,17 @@ __global__ void __launch_bounds__(kPlanThreads, 1) plan_kernel(PlanParams p) {
   UnitRec* recs_s = reinterpret_cast<UnitRec*>(ws + p.lay.recs_s);
   int* cnt_d = reinterpret_cast<int*>(ws + p.lay.cnt_d);
   int* cnt_s = reinterpret_cast<int*>(ws + p.lay.cnt_s);
-  int4* tiles_p = reinterpret_cast<int4*>(ws + p.lay.tiles_p);
+  PfItem* items_p = reinterpret_cast<PfItem*>(ws + p.lay.items_p);
+  int* cnt_p = reinterpret_cast<int*>(ws + p.lay.cnt_p);
   int* order_d = reinterpret_cast<int*>(ws + p.lay.order_d);
 
   for (int i = threadIdx.x; i <= kMaxUnitBlocks; i += kPlanThreads) size_hist[i] = 0;
   if (threadIdx.x == 0) {
     err = 0;
     s_blocks = 0;
+    s_blocks_d = 0;
+    s_pf_tiles = 0;
+    s_pf_kv = 0;
     for (int i = 0; i < kLists; ++i) carry[i] = 0;
     const int q0 = __ldg(p.qsl), qB = __ldg(p.qsl + B);
     if (q0 != 0 || qB != p.num_tokens) err |= PA_DEV_QSL;
@@ -139,42 +147,97 @@ __global__ void __launch_bounds__(kPlanThreads, 1) plan_kernel(PlanParams p) {
   __syncthreads();
 
   // Split size for this step: at least p.bps blocks, and longer when the
-  // CTAs (about two per SM) would otherwise get more than ~8 units each of
-  // the decode and few-token KV (measured: longer units amortise each unit's
-  // fixed cost once there are enough of them), up to kMaxUnitBlocks.
+  // CTAs would otherwise get more than ~8 units each of the decode and
+  // few-token KV (measured: longer units amortise each unit's fixed cost once
+  // there are enough of them), up to kMaxUnitBlocks.
   // Out-of-range lengths are left out here (they are flagged below).
   {
-    unsigned long long mine = 0;
+    unsigned long long mine = 0, mine_d = 0, pf_tiles = 0, pf_kv = 0;
+    const int pm = p.prefill_rows / p.group;  // positions per prefill query tile
     for (int r = threadIdx.x; r < B; r += kPlanThreads) {
       const int S = __ldg(p.seq_lens + r);
       const int L = __ldg(p.qsl + r + 1) - __ldg(p.qsl + r);
-      if (S >= 1 && S <= p.max_seq_len && L >= 1 && L < p.prefill_min_qlen)
+      if (S < 1 || S > p.max_seq_len || L < 1 || L > S) continue;
+      if (L < p.prefill_min_qlen) {
         mine += static_cast<unsigned long long>(ceil_div(S, kBlockSize));
+        if (L == 1) mine_d += static_cast<unsigned long long>(ceil_div(S, kBlockSize));
+      } else if (L <= p.max_query_len) {
+        const int nt = ceil_div(L, pm);
+        pf_tiles += nt;
+        for (int m = 0; m < nt; ++m)
+          pf_kv += static_cast<unsigned long long>(ceil_div(S - L + min(L, (m + 1) * pm), kPrefillKeys));
+      }
     }
 #pragma unroll
-    for (int o = 16; o > 0; o >>= 1) mine += __shfl_down_sync(0xffffffffu, mine, o);
+    for (int o = 16; o > 0; o >>= 1) {
+      mine += __shfl_down_sync(0xffffffffu, mine, o);
+      mine_d += __shfl_down_sync(0xffffffffu, mine_d, o);
+      pf_tiles += __shfl_down_sync(0xffffffffu, pf_tiles, o);
+      pf_kv += __shfl_down_sync(0xffffffffu, pf_kv, o);
+    }
     if ((threadIdx.x & 31) == 0 && mine) atomicAdd(&s_blocks, mine);
+    if ((threadIdx.x & 31) == 0 && mine_d) atomicAdd(&s_blocks_d, mine_d);
+    if ((threadIdx.x & 31) == 0 && pf_tiles) atomicAdd(&s_pf_tiles, pf_tiles);
+    if ((threadIdx.x & 31) == 0 && pf_kv) atomicAdd(&s_pf_kv, pf_kv);
   }
   __syncthreads();
-  const long long per_cta =
-      static_cast<long long>(s_blocks) * p.num_kv_heads / max(1, 2 * p.num_sms);
-  int bps = static_cast<int>(
+  const int num_ctas = max(1, p.num_ctas);
+  const long long per_cta = static_cast<long long>(s_blocks) * p.num_kv_heads / num_ctas;
+  const int bps = static_cast<int>(
       min(static_cast<long long>(kMaxUnitBlocks),
           max(static_cast<long long>(p.bps), (per_cta + PA_UNITS_PER_CTA - 1) / PA_UNITS_PER_CTA)));
-#if PA_SPLIT_BLOCKS_SMALL > 0
-  if (per_cta < p.bps)
-    bps = static_cast<int>(max(static_cast<long long>(PA_SPLIT_BLOCKS_SMALL),
-                               (per_cta + PA_SMALL_UNITS - 1) / PA_SMALL_UNITS));
-#endif
+  // Decode splits of a small step (fewer KV blocks x heads than one
+  // p.bps-block split per CTA): with whole-request units most CTAs would sit
+  // idle while a few stream the longest requests, so the split is sized to
+  // give about one unit per CTA (PA_SMALL_SPLIT_PCT % of the even share), at
+  // least PA_SPLIT_MIN blocks, and large enough that the items fit the
+  // workspace: items <= requests + blocks / split.
+  int bps_d = bps;
+  {
+    const long long total_d = static_cast<long long>(s_blocks_d) * p.num_kv_heads;
+    if (total_d < static_cast<long long>(num_ctas) * p.bps) {
+      const long long want = (total_d * PA_SMALL_SPLIT_PCT + 100LL * num_ctas - 1) / (100LL * num_ctas);
+      const long long room = p.cap.decode_items - B;
+      const long long need = room > 0 ? (static_cast<long long>(s_blocks_d) + room - 1) / room
+                                       : static_cast<long long>(p.bps);
+      bps_d = static_cast<int>(min(static_cast<long long>(p.bps),
+                                   max(max(want, need), static_cast<long long>(PA_SPLIT_MIN))));
+    }
+  }
+
+  // KV tiles per prefill unit.  With fewer prefill units (query tiles x kv
+  // heads) than SMs, a unit streams all the KV its rows see and most SMs idle
+  // (a short chunk after a long prompt: every later chunk reads all earlier
+  // ones from the cache), so each query tile's KV is split into pieces sized
+  // for one piece per SM, at least kMinPrefillSplitTiles, whose partial
+  // softmax states the last piece merges.  Pieces with a partial state must
+  // fit the capacity: they number at most query tiles + KV tiles / split (and
+  // the items then fit as well).
+  int tps = INT_MAX;
+  {
+    const long long nt = static_cast<long long>(s_pf_tiles);
+    const long long units = nt * p.num_kv_heads;
+    const long long room = p.cap.prefill_slots - nt;
+    if (units > 0 && units < p.num_sms && room > 0) {
+      // pieces x heads <= units + kv x heads / tps <= num_sms: one round of
+      // pieces, every SM streaming at most one
+      const long long kv = static_cast<long long>(s_pf_kv);
+      const long long spare = p.num_sms - units;
+      const long long want = (kv * p.num_kv_heads + spare - 1) / spare;
+      const long long need = (kv + room - 1) / room;
+      tps = static_cast<int>(min(static_cast<long long>(INT_MAX),
+                                 max(max(want, need), static_cast<long long>(kMinPrefillSplitTiles))));
+    }
+  }
 
   // One pass: classify and count, exclusive-scan the counts across the CTA,
   // and let each request's thread write its own items and tiles at its
   // offsets (every write checked against the list's capacity).
-  int carry_r[kLists] = {0, 0, 0, 0, 0, 0};
+  int carry_r[kLists] = {0, 0, 0, 0, 0, 0, 0, 0};
   for (int base = 0; base < B; base += kPlanThreads) {
     const int r = base + threadIdx.x;
     int c = kClassNone;
-    int cnt[kLists] = {0, 0, 0, 0, 0, 0};
+    int cnt[kLists] = {0, 0, 0, 0, 0, 0, 0, 0};
     int S = 0, a = 0, L = 0;
     if (r < B) {
       S = __ldg(p.seq_lens + r);
@@ -191,13 +254,20 @@ __global__ void __launch_bounds__(kPlanThreads, 1) plan_kernel(PlanParams p) {
       } else if (L == 1) {
         c = kClassDecode;
         cnt[1] = 1;
-        const int nb = ceil_div(S, kBlockSize), rb = request_bps(nb, bps);
+        const int nb = ceil_div(S, kBlockSize), rb = request_bps(nb, bps_d);
         cnt[0] = splits_for(S - 1, rb);
         // long items: every full split, and the last one if it is at least half a split
-        cnt[5] = cnt[0] - 1 + (2 * (nb - (cnt[0] - 1) * rb) >= bps ? 1 : 0);
+        cnt[5] = cnt[0] - 1 + (2 * (nb - (cnt[0] - 1) * rb) >= bps_d ? 1 : 0);
       } else if (L >= p.prefill_min_qlen) {
         c = kClassPrefill;
-        cnt[4] = ceil_div(L, p.prefill_rows / p.group);
+        const int pm = p.prefill_rows / p.group;
+        cnt[6] = ceil_div(L, pm);
+        for (int m = 0; m < cnt[6]; ++m) {
+          const int nkv = ceil_div(S - L + min(L, (m + 1) * pm), kPrefillKeys);
+          const int ns = nkv > tps ? ceil_div(nkv, tps) : 1;
+          cnt[4] += ns;
+          if (ns > 1) cnt[7] += ns;
+        }
       } else {
         c = kClassSmall;
         cnt[3] = ceil_div(L, p.small_positions);
@@ -218,7 +288,7 @@ __global__ void __launch_bounds__(kPlanThreads, 1) plan_kernel(PlanParams p) {
       // items off[0] .. off[0] + cnt[0] - 1: one split of the request each
       const int tile = off[1];
       const int nb = ceil_div(S, kBlockSize);
-      const int rb = request_bps(nb, bps);
+      const int rb = request_bps(nb, bps_d);
       const int ns = cnt[0];
       if (tile < p.cap.decode_tiles) tiles_d[tile] = make_int4(off[0], ns, rb, 0);
       for (int s = 0; s < ns; ++s) {
@@ -257,9 +327,24 @@ __global__ void __launch_bounds__(kPlanThreads, 1) plan_kernel(PlanParams p) {
         first += ns;
       }
     } else if (c == kClassPrefill) {
-      // tensor-core tiles of prefill_rows query rows (positions x grouped heads)
-      for (int m = 0; m < cnt[4] && off[4] + m < p.cap.prefill_tiles; ++m)
-        tiles_p[off[4] + m] = make_int4(r, m, 0, 0);
+      // tensor-core query tiles of prefill_rows rows (positions x grouped
+      // heads), each as one item or as pieces of its KV tiles
+      const int pm = p.prefill_rows / p.group;
+      int item = off[4], slot = off[7];
+      for (int m = 0; m < cnt[6]; ++m) {
+        const int tile = off[6] + m;
+        const int nkv = ceil_div(S - L + min(L, (m + 1) * pm), kPrefillKeys);
+        const int ns = nkv > tps ? ceil_div(nkv, tps) : 1;
+        const int per = ceil_div(nkv, ns);
+        for (int sp = 0; sp < ns; ++sp, ++item) {
+          if (item >= p.cap.prefill_items) break;
+          PfItem it;
+          it.a = make_int4(r, m, sp * per, min(nkv, (sp + 1) * per));
+          it.b = make_int4(tile, sp, ns, ns > 1 ? slot : -1);
+          items_p[item] = it;
+        }
+        if (ns > 1) slot += ns;
+      }
     }
 #pragma unroll
     for (int k = 0; k < kLists; ++k) carry_r[k] += tot[k];
@@ -272,7 +357,8 @@ __global__ void __launch_bounds__(kPlanThreads, 1) plan_kernel(PlanParams p) {
   if (threadIdx.x == 0) {
     if (carry[0] > p.cap.decode_items || carry[1] > p.cap.decode_tiles ||
         carry[2] > p.cap.small_items || carry[3] > p.cap.small_tiles ||
-        carry[4] > p.cap.prefill_tiles)
+        carry[4] > p.cap.prefill_items || carry[6] > p.cap.prefill_tiles ||
+        carry[7] > p.cap.prefill_slots)
       err |= PA_DEV_CAPACITY;
   }
   __syncthreads();
@@ -285,7 +371,8 @@ __global__ void __launch_bounds__(kPlanThreads, 1) plan_kernel(PlanParams p) {
     wait_prior_grid();
     return;
   }
-  const int n_di = carry[0], n_dt = carry[1], n_si = carry[2], n_st = carry[3], n_pt = carry[4];
+  const int n_di = carry[0], n_dt = carry[1], n_si = carry[2], n_st = carry[3];
+  const int n_pi = carry[4], n_pt = carry[6];
   // dispatch order (it does not change results: partial states are stored
   // and merged by item, in split order).  The long items took the first
   // n_long slots above; short items: exclusive scan of the size histogram
@@ -314,12 +401,13 @@ __global__ void __launch_bounds__(kPlanThreads, 1) plan_kernel(PlanParams p) {
   }
   __syncthreads();
   for (int i = threadIdx.x; i < n_di; i += kPlanThreads) {
-    // short = under half a split (full splits hold at least bps blocks)
+    // short = under half a split (full splits hold at least bps_d blocks)
     const int4 a = recs_d[i].a;  // written above by this CTA
-    if (2 * (a.w - a.z) < bps) order_d[atomicAdd(&size_hist[a.w - a.z], 1)] = i;
+    if (2 * (a.w - a.z) < bps_d) order_d[atomicAdd(&size_hist[a.w - a.z], 1)] = i;
   }
   for (int i = threadIdx.x; i < n_dt * p.num_kv_heads; i += kPlanThreads) cnt_d[i] = 0;
   for (int i = threadIdx.x; i < n_st * p.num_kv_heads; i += kPlanThreads) cnt_s[i] = 0;
+  for (int i = threadIdx.x; i < n_pt * p.num_kv_heads; i += kPlanThreads) cnt_p[i] = 0;
   if (threadIdx.x == 0) {
     hdr[kHdrDecodeItems] = n_di;
     hdr[kHdrDecodeTiles] = n_dt;
@@ -327,7 +415,7 @@ __global__ void __launch_bounds__(kPlanThreads, 1) plan_kernel(PlanParams p) {
     hdr[kHdrSmallItems] = n_si;
     hdr[kHdrSmallTiles] = n_st;
     hdr[kHdrSmallNext] = 0;
-    hdr[kHdrPrefillTiles] = n_pt;
+    hdr[kHdrPrefillItems] = n_pi;
     hdr[kHdrPrefillNext] = 0;
     if (err) flag_error(p.status, err);
   }

@@ -99,18 +99,22 @@ enum Bar : int {
   kMlRead = 19,     // ... and read (8 warps)
   kOFree = 20,      // O read by the epilogue (8 warps)
   kDrain = 21,      // teardown after a timeout
-  kNumBars = 22
+  kPieceDone = 22,  // a split piece's partial state stored (8 softmax warps)
+  kPieceLast = 23,  // ... and whether it was the tile's last piece decided (warp 0)
+  kNumBars = 24
 };
 
 struct UnitInfo {
   int r, g, a, j0, npos, pos0, kv_end, n_kv;  // r < 0: no more units
-  int rot;                                    // KV tile processed first
+  int kt0;                                    // first KV tile (n_kv tiles from there)
+  int rot;                                    // KV tile processed first (from kt0)
+  int ptile, piece, nsplit, slot0;            // split pieces of the query tile (PfItem::b)
 };
 
 // KV tile processed s-th in unit u (tiles are visited in rotated order).
 __device__ __forceinline__ int tile_of(const UnitInfo& u, int s) {
   const int t = s + u.rot;
-  return t >= u.n_kv ? t - u.n_kv : t;
+  return u.kt0 + (t >= u.n_kv ? t - u.n_kv : t);
 }
 
 struct PfMaps {
@@ -173,7 +177,9 @@ __device__ __forceinline__ bool wait_bar(uint32_t bar, uint32_t parity, volatile
 __device__ __forceinline__ uint32_t bar_count(int i) {
   if (i == kUnitEmpty || i == kUnitEmpty + 1) return 10;  // 8 softmax warps, MMA, V loader
   if (i == kGo || i == kGo + 1) return 10;  // 8 softmax warps, V loader, K loader
-  if (i == kMx || i == kMx + 1 || i == kMlFull || i == kMlRead || i == kOFree) return 8;
+  if (i == kMx || i == kMx + 1 || i == kMlFull || i == kMlRead || i == kOFree ||
+      i == kPieceDone)
+    return 8;
   return 1;  // TMA (arrive + bytes) or tcgen05.commit
 }
 
@@ -213,6 +219,7 @@ __global__ void __launch_bounds__(kPfThreads, 1)
   __shared__ float s_mx[2][2][kTileM];  // [buffer][column half][row]: half-row maxima
   __shared__ float s_ml[2][kTileM];     // [column half][row]: row sums at the unit's end
   __shared__ int s_abort;
+  __shared__ int s_last;  // this CTA's split piece was its query tile's last
 
   unsigned char* smem = reinterpret_cast<unsigned char*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
@@ -278,22 +285,28 @@ __global__ void __launch_bounds__(kPfThreads, 1)
       UnitInfo u;
       u.r = -1;
       if (unit < n_units) {
-        // last tile first: within a chunk later query tiles see more keys, and
+        // last item first: within a chunk later query tiles see more keys, and
         // later chunks of the step carry more prior context
-        const int tile = __ldg(p.n_items) - 1 - unit / Hkv;
-        const int4 tr = __ldg(p.items + tile);
-        const int S = __ldg(p.seq_lens + tr.x);
-        const int a = __ldg(p.qsl + tr.x);
-        const int L = __ldg(p.qsl + tr.x + 1) - a;
-        u.r = tr.x;
+        const PfItem* it = reinterpret_cast<const PfItem*>(p.items) +
+                           (__ldg(p.n_items) - 1 - unit / Hkv);
+        const int4 ta = __ldg(&it->a), tb = __ldg(&it->b);
+        const int S = __ldg(p.seq_lens + ta.x);
+        const int a = __ldg(p.qsl + ta.x);
+        const int L = __ldg(p.qsl + ta.x + 1) - a;
+        u.r = ta.x;
         u.g = unit % Hkv;
         u.a = a;
-        u.j0 = tr.y * PM;
+        u.j0 = ta.y * PM;
         u.npos = min(PM, L - u.j0);
         u.pos0 = S - L + u.j0;
-        u.kv_end = u.pos0 + u.npos;
-        u.n_kv = (u.kv_end + kTileN - 1) / kTileN;
-        u.rot = tr.y % u.n_kv;
+        u.kt0 = ta.z;
+        u.n_kv = ta.w - ta.z;
+        u.kv_end = min(u.pos0 + u.npos, ta.w * kTileN);  // this piece's keys end here
+        u.rot = ta.y % u.n_kv;
+        u.ptile = tb.x;
+        u.piece = tb.y;
+        u.nsplit = tb.z;
+        u.slot0 = tb.w;
       }
       const int slot = uc & 1;
       if (uc >= 2 && !wait_bar(bar(kUnitEmpty + slot), ((uc >> 1) - 1) & 1, abort, p.status)) break;
@@ -375,7 +388,7 @@ __global__ void __launch_bounds__(kPfThreads, 1)
           break;
         }
         const uint32_t vb = sbase + C::kVOff + w * C::kTileBytes;
-        if (kt != u.n_kv - 1 || (u.kv_end & (kBlockSize - 1)) == 0) {
+        if (kt != u.kt0 + u.n_kv - 1 || (u.kv_end & (kBlockSize - 1)) == 0) {
           copy_kv_tile(u, kt, ph, true, vb, bar(kGo + w));  // this tile's kGo arrival
           gv[w] = nv[w] + 1;
         } else {
@@ -524,6 +537,55 @@ __global__ void __launch_bounds__(kPfThreads, 1)
     const int Hq = p.num_q_heads;
     __nv_bfloat16* out = static_cast<__nv_bfloat16*>(p.out);
     uint32_t nb0 = 0, nb1 = 0;  // tiles per buffer parity so far (all units)
+    uint32_t npieces = 0;       // split pieces finished so far
+    const int Hkv = p.num_kv_heads;
+    // Merge of a split query tile, by its last piece: this thread's row i and
+    // its warpgroup's half of the columns, from every piece's (max, sum) and
+    // unnormalised O (fp32, in L2).
+    auto merge_row = [&](const UnitInfo& u, long long tok, int hh) {
+      const long long rbase = static_cast<long long>(u.slot0) * Hkv + u.g;
+      auto ml_of = [&](int sp) {
+        return __ldcg(reinterpret_cast<const float2*>(p.part_ml) +
+                      ((rbase + static_cast<long long>(sp) * Hkv) * kTileM + i));
+      };
+      float M = -CUDART_INF_F;
+      for (int sp = 0; sp < u.nsplit; ++sp) M = fmaxf(M, ml_of(sp).x);
+      float den = 0.f;
+      for (int sp = 0; sp < u.nsplit; ++sp) {
+        const float2 ml = ml_of(sp);
+        den = fmaf(ml.y, ex2(ml.x - M), den);  // 0 for a piece without visible keys
+      }
+      const float inv = p.out_scale / den;
+      __nv_bfloat16* orow = out + (tok * Hq + u.g * G + hh) * D;
+#pragma unroll 1
+      for (int c0 = w * kOCols; c0 < (w + 1) * kOCols; c0 += 32) {
+        float acc[32];
+#pragma unroll
+        for (int j = 0; j < 32; ++j) acc[j] = 0.f;
+        for (int sp = 0; sp < u.nsplit; ++sp) {
+          const float f = ex2(ml_of(sp).x - M);
+          const float4* src = reinterpret_cast<const float4*>(
+              p.part_acc + ((rbase + static_cast<long long>(sp) * Hkv) * kTileM + i) * D + c0);
+          float4 v[8];
+#pragma unroll
+          for (int j = 0; j < 8; ++j) v[j] = __ldcg(src + j);
+#pragma unroll
+          for (int j = 0; j < 8; ++j) {
+            acc[4 * j] = fmaf(v[j].x, f, acc[4 * j]);
+            acc[4 * j + 1] = fmaf(v[j].y, f, acc[4 * j + 1]);
+            acc[4 * j + 2] = fmaf(v[j].z, f, acc[4 * j + 2]);
+            acc[4 * j + 3] = fmaf(v[j].w, f, acc[4 * j + 3]);
+          }
+        }
+        uint4* dst = reinterpret_cast<uint4*>(orow + c0);
+#pragma unroll
+        for (int j = 0; j < 4; ++j)
+          dst[j] = make_uint4(pack_bf16(acc[8 * j] * inv, acc[8 * j + 1] * inv),
+                              pack_bf16(acc[8 * j + 2] * inv, acc[8 * j + 3] * inv),
+                              pack_bf16(acc[8 * j + 4] * inv, acc[8 * j + 5] * inv),
+                              pack_bf16(acc[8 * j + 6] * inv, acc[8 * j + 7] * inv));
+      }
+    };
     for (int uc = 0;; ++uc) {
       const int slot = uc & 1;
       if (!wait_bar(bar(kUnitFull + slot), (uc >> 1) & 1, abort, p.status)) break;
@@ -651,12 +713,23 @@ __global__ void __launch_bounds__(kPfThreads, 1)
       const float inv = p.out_scale / l_sum;
       const long long tok = u.a + u.j0 + jj;
       __nv_bfloat16* orow = out + (tok * Hq + u.g * G + (i - jj * G)) * D;
+      // a piece of a split query tile keeps its state: unnormalised O and
+      // the row's (maximum used, sum) go to its partial slot
+      const bool split = u.nsplit > 1;
+      const long long prow =
+          (static_cast<long long>(u.slot0 + u.piece) * Hkv + u.g) * kTileM + i;
 #pragma unroll
       for (int c0 = w * kOCols; c0 < (w + 1) * kOCols; c0 += 32) {
         uint32_t o[32];
         PA_TMEM_LD32(tmem_o + c0, o);
         tmem_wait_ld();
-        if (row_ok) {
+        if (row_ok && split) {
+          float4* dst = reinterpret_cast<float4*>(p.part_acc + prow * D + c0);
+#pragma unroll
+          for (int j = 0; j < 8; ++j)
+            dst[j] = make_float4(__uint_as_float(o[4 * j]), __uint_as_float(o[4 * j + 1]),
+                                 __uint_as_float(o[4 * j + 2]), __uint_as_float(o[4 * j + 3]));
+        } else if (row_ok) {
           uint4* dst = reinterpret_cast<uint4*>(orow + c0);
 #pragma unroll
           for (int j = 0; j < 4; ++j) {
@@ -668,10 +741,34 @@ __global__ void __launch_bounds__(kPfThreads, 1)
           }
         }
       }
+      if (split && row_ok && w == 0)
+        reinterpret_cast<float2*>(p.part_ml)[prow] = make_float2(m_used, l_sum);
       tc_fence_before();
       warp_arrive(bar(kOFree));
       // neither group publishes its next unit's row sum before both read these
       if (!wait_bar(bar(kMlRead), uc & 1, abort, p.status)) break;
+      if (split) {
+        // every piece counts itself in once its state is stored; the last one
+        // (of any CTA) merges the tile's pieces
+        __threadfence();
+        warp_arrive(bar(kPieceDone));
+        if (warp == 0) {
+          if (!wait_bar(bar(kPieceDone), npieces & 1, abort, p.status)) break;
+          if (lane == 0) {
+            __threadfence();
+            s_last = atomicAdd(p.merge_cnt + u.ptile * Hkv + u.g, 1) == u.nsplit - 1;
+            mbar_arrive(bar(kPieceLast));
+          }
+          __syncwarp();
+        }
+        if (!wait_bar(bar(kPieceLast), npieces & 1, abort, p.status)) break;
+        const bool last = *reinterpret_cast<volatile int*>(&s_last) != 0;
+        ++npieces;
+        if (last) {
+          __threadfence();
+          if (row_ok) merge_row(u, tok, i - jj * G);
+        }
+      }
     }
   }
 

@@ -158,6 +158,16 @@ def spec_long_prefill_chunk(seed: int = 5) -> StepSpec:
                     np.array([8192], np.int64), seed=seed)
 
 
+def spec_long_prior_chunks(seed: int = 6) -> StepSpec:
+    """Short prefill chunks late in long prompts: a 64-token chunk after 32768
+    tokens and a 16-token chunk after 98304 ("Serving models at scale with
+    vLLM", section Chunked prefill: a long prompt is split under a small token
+    budget and every later chunk reads all earlier ones from the cache);
+    Llama-3-8B heads, bf16."""
+    return StepSpec("long_prior_chunks", "bf16", 32, 8, 128, np.array([64, 16], np.int64),
+                    np.array([32768 + 64, 98304 + 16], np.int64), seed=seed)
+
+
 CONFIGS = {
     "tiny_decode_f32": spec_tiny_decode_f32,
     "tinyllama_decode": spec_tinyllama_decode,
@@ -165,6 +175,7 @@ CONFIGS = {
     "mixed_step": spec_mixed_step,
     "long_context_decode": spec_long_context_decode,
     "long_prefill_chunk": spec_long_prefill_chunk,
+    "long_prior_chunks": spec_long_prior_chunks,
 }
 
 

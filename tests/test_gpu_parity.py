@@ -110,6 +110,34 @@ def test_long_prefill_chunk_sampled_parity():
     assert_close(got, ref, "bf16", "long prefill chunk")
 
 
+def test_long_prior_chunks_sampled_parity():
+    """Short chunks late in long prompts (64 tokens after 32768, 16 after
+    98304), as bench.py times them: the KV of each query tile is split into
+    pieces and merged.  The whole cache write is checked bit for bit,
+    attention on sampled rows of both chunks and every kv head."""
+    spec = W.spec_long_prior_chunks()
+    step = W.make_step(spec, device="cuda")
+    out, kc, vc, status = run_gpu(step)
+    assert status == 0
+    mk, mv = oracle.cache_write(bits(step.k), bits(step.v), step.slot_mapping.cpu().numpy(),
+                                bits(step.k_cache), bits(step.v_cache))
+    assert np.array_equal(bits(kc), mk) and np.array_equal(bits(vc), mv)
+    bt = step.block_tables.cpu().numpy()
+    qsl = step.query_start_loc.cpu().numpy()
+    G = spec.num_q_heads // spec.num_kv_heads
+    for r in range(spec.num_seqs):
+        S, L = int(spec.seq_lens[r]), int(spec.q_lens[r])
+        nb = oracle.blocks_needed(S)
+        rows = [(int(qsl[r]) + j, g * G + (j + g) % G) for g in range(spec.num_kv_heads)
+                for j in (0, L // 2, L - 1)]
+        ref = oracle.paged_attention_rows(bits(step.q), mk[bt[r, :nb]], mv[bt[r, :nb]],
+                                          np.arange(nb)[None, :].repeat(spec.num_seqs, 0),
+                                          spec.seq_lens, qsl, step.scale, spec.num_kv_heads,
+                                          rows)
+        got = torch.stack([out[t, h] for t, h in rows])
+        assert_close(got, ref, "bf16", f"long prior chunk r={r}")
+
+
 def test_prefill_runs_are_bit_identical():
     """Chunks of 16 to 1000 tokens over contexts up to 3000 keys: ~450 tensor-core
     units, several per CTA, so every hand-off between the kernel's roles is
@@ -245,6 +273,13 @@ PREFILL_SHAPES = [
     ("bf16", 128, 1, [200], [260]),
     # fp32 chunk (CUDA-core path) with splits
     ("f32", 128, 2, [100, 1], [700, 300]),
+    # fewer tensor-core units than SMs: each query tile's KV is split into
+    # pieces whose partial states the last piece merges
+    ("bf16", 128, 4, [20, 1], [9000, 3000]),
+    ("bf16", 64, 8, [40, 1], [6000, 17]),
+    # G = 1, 128 positions per tile: a piece boundary (key 4096) falls inside
+    # the first query tile, so its early rows see no key in the last piece
+    ("bf16", 128, 1, [150], [4150]),
 ]
 
 
