@@ -221,7 +221,10 @@ int pa_set_prefill_overlap(int on);
  *
  * The first call on each device looks up the array's device address
  * (cudaGetSymbolAddress, with that device current); make that first call
- * before any stream capture starts on the device.  All calls share the one
+ * before any stream capture starts on the device.  The address is kept for
+ * the life of the process: after cudaDeviceReset on a device the array may
+ * live elsewhere and the kept address is stale, so a process that resets a
+ * device must not call this entry point on it again.  All calls share the one
  * array and each call re-initialises what it needs, but calls whose work
  * overlaps on the GPU (other streams, other threads) race on it: order them.
  */

@@ -2,10 +2,11 @@
 for callers that cannot allocate device memory (for example a serving
 engine that gave nearly all free GPU memory to its KV pool at start-up).
 
-The GPU test calls the entry point through the C ABI twice in a row, on two
-different steps, and checks each result against pa_forward with a caller
-workspace on the same inputs.  The second call shows that what the first
-call left in the shared scratch does not leak into the next result.  This
+The GPU test calls the entry point through the C ABI on three different
+steps in a row, the last with a chunk on the tensor-core prefill path, and
+checks each result against pa_forward with a caller workspace on the same
+inputs.  The later calls show that what an earlier call left in the shared
+scratch does not leak into the next result.  This
 file is collected last so that a run stopping at its first failure has run
 every other test before it."""
 import ctypes
@@ -48,12 +49,16 @@ def test_oversized_step_is_rejected_before_any_launch(lib):
 
 
 @pytest.mark.gpu
-def test_noalloc_matches_pa_forward_on_two_calls_in_a_row(lib):
+def test_noalloc_matches_pa_forward_on_calls_in_a_row(lib):
     specs = [
         # decodes that split over several KV blocks, plus a multi-token chunk
         W.custom_spec("noalloc-a", "bf16", 32, 8, 128, [1, 1, 6, 1], [900, 17, 70, 2500], seed=41),
         # different shape and head layout: the scratch is reused with new contents
         W.custom_spec("noalloc-b", "bf16", 16, 2, 64, [1, 3, 1], [3000, 40, 128], seed=42),
+        # a 40-token chunk on the tensor-core prefill path (its work list, counter
+        # and KV-split partial states in the scratch), after calls that left
+        # other contents there
+        W.custom_spec("noalloc-c", "bf16", 32, 8, 128, [1, 40, 1], [600, 340, 2100], seed=43),
     ]
     for spec in specs:
         st = W.make_step(spec, device="cuda")
