@@ -685,6 +685,23 @@ def run_gpu_arm(args):
                  "step of their own",
     }
 
+    # ---- the mixed step over an 8-bit (E4M3) KV cache
+    mf = StepRunner(MIXED, seed_offset=seed_off, fp8_scales=(0.01, 0.01))
+    fms_, fmdec, _ = mf.time_device(half, args.warmup, world)
+    fms_, fmdec = dist_max(fms_, world), dist_max(fmdec, world)
+    _check_status(mf, "mixed step, fp8")
+    fmw = mf.work
+    mixed_info["fp8_kv"] = {
+        "ms_per_step": fms_,
+        "tokens_per_s_per_layer": world * fmw["tokens"] / (fms_ * 1e-3),
+        "decode_kernel_ms": fmdec,
+        "decode_gbs": (fmw["decode_bytes"] - fmw["kv_bytes"] // 2) / (fmdec * 1e-3) / 1e9,
+        "note": "KV cache E4M3 (scales 0.01): decode reads 8-bit codes, the chunks run on "
+                "the tensor-core prefill kernel over codes widened to f16 in shared memory",
+    }
+    del mf
+    torch.cuda.empty_cache()
+
     # ---- the mixed step's two prefill chunks alone: the tensor-core kernel's own rate
     pf = StepRunner(MIXED, seed_offset=seed_off, requests=slice(-2, None))
     pms, _, ppf = pf.time_device(half, args.warmup, world, flush=True)

@@ -118,7 +118,7 @@ Capacity capacity(const pa_layout* L, int B, int T, int max_seq_len) {
   c.small_tiles = (T > B ? cdiv(T - B, small_positions(L)) : 0) + multi;
   c.small_items = c.small_tiles * splits;
   const long long group = L->num_q_heads / L->num_kv_heads;
-  c.prefill_tiles = (L->dtype == PA_BF16 && !fp8_cache(L))
+  c.prefill_tiles = L->dtype == PA_BF16
                         ? cdiv(static_cast<long long>(T) * group, kPrefillRows) + multi : 0;
   // a step that can hold a chunk of kPrefillMinQlen tokens may split its
   // prefill query tiles' KV
@@ -338,7 +338,7 @@ int pa_forward(const void* q, const void* k_cache, const void* v_cache,
     if (e != cudaSuccess) return fail_cuda(e, "decode grid size");
   }
   pp.small_positions = small_positions(layout);
-  const bool tc_prefill = layout->dtype == PA_BF16 && !fp8_cache(layout);
+  const bool tc_prefill = layout->dtype == PA_BF16;  // bf16 or FP8 cache
   pp.prefill_min_qlen = tc_prefill ? kPrefillMinQlen : 0x7fffffff;
   pp.prefill_rows = kPrefillRows;
   pp.group = group;
@@ -396,7 +396,7 @@ int pa_forward(const void* q, const void* k_cache, const void* v_cache,
       pst = side->stream;
     }
     if (g_pf_prof_start) cudaEventRecord(g_pf_prof_start, pst);
-    e = launch_prefill_tc(pf, layout->head_size, group, num_sms, pst);
+    e = launch_prefill_tc(pf, layout->head_size, group, num_sms, fp8_cache(layout), pst);
     if (e != cudaSuccess) return fail_cuda(e, "prefill attention launch");
     if (g_pf_prof_stop) cudaEventRecord(g_pf_prof_stop, pst);
     if (fork) {

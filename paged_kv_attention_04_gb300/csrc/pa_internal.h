@@ -134,9 +134,10 @@ cudaError_t launch_cache_write_fp8(const void* k, const void* v, const int64_t* 
                                    long long num_slots, float k_scale, float v_scale,
                                    int32_t* status, cudaStream_t stream);
 cudaError_t launch_plan(const PlanParams& p, cudaStream_t stream);
-// Tensor-core (tcgen05) chunked-prefill attention over the prefill list.
+// Tensor-core (tcgen05) chunked-prefill attention over the prefill list
+// (bf16 q/out; a bf16 or an FP8 (E4M3) cache).
 cudaError_t launch_prefill_tc(const AttnParams& p, int head_size, int group, int num_sms,
-                              cudaStream_t stream);
+                              bool fp8_cache, cudaStream_t stream);
 // Split-KV attention over the decode or few-token list, by element type:
 // bf16 runs the warp-level tensor-core (mma.sync) kernel, fp32 the CUDA-core
 // kernel.  positions: 1 (decode list) or the few-token tile height.  With

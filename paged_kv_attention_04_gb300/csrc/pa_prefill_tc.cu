@@ -101,7 +101,9 @@ enum Bar : int {
   kDrain = 21,      // teardown after a timeout
   kPieceDone = 22,  // a split piece's partial state stored (8 softmax warps)
   kPieceLast = 23,  // ... and whether it was the tile's last piece decided (warp 0)
-  kNumBars = 24
+  kQLand = 24,      // FP8 cache: the bf16 Q tile landed (TMA), before its f16 conversion
+  kKLand = 25,      // [2] FP8 cache: a K tile's codes landed (TMA), before widening
+  kNumBars = 27
 };
 
 struct UnitInfo {
@@ -119,9 +121,12 @@ __device__ __forceinline__ int tile_of(const UnitInfo& u, int s) {
 
 struct PfMaps {
   CUtensorMap q;  // q [T][Hq][D] as 3-D (D, Hq, T), box (64, G, 128/G)
+  // bf16 cache:
   CUtensorMap k;  // k_cache as 5-D (64, 8 rows, D/64 halves, 2 row groups, NB x 16 x Hkv),
                   // box (64, 8, D/64, 2, 1) at block x 16 x Hkv + head
   CUtensorMap v;  // v_cache as 5-D (64, 16 rows, D/64 halves, Hkv, NB), box (64, 16, D/64, 1, 1)
+  // FP8 cache: k and v as 3-D byte maps (D, 16 rows, NB x 16 x Hkv), box (D, 16, 1) at
+  // block x 16 x Hkv + head: one block's codes, [16 rows][D bytes]
 };
 
 // max of three floats in one instruction (NaN-free operands here)
@@ -180,6 +185,8 @@ __device__ __forceinline__ uint32_t bar_count(int i) {
   if (i == kMx || i == kMx + 1 || i == kMlFull || i == kMlRead || i == kOFree ||
       i == kPieceDone)
     return 8;
+  // kQLand, kKLand: TMA (arrive + bytes); kQFull, kKFirst also take the
+  // loader's plain arrival after an FP8 conversion: one arrival either way
   return 1;  // TMA (arrive + bytes) or tcgen05.commit
 }
 
@@ -204,10 +211,27 @@ __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
   asm("cvt.rn.bf16x2.f32 %0, %1, %2;\n" : "=r"(w) : "f"(hi), "f"(lo));
   return w;
 }
+__device__ __forceinline__ uint32_t pack_f16(float lo, float hi) {
+  uint32_t w;
+  asm("cvt.rn.f16x2.f32 %0, %1, %2;\n" : "=r"(w) : "f"(hi), "f"(lo));
+  return w;
+}
+// Two E4M3 codes (low byte first) -> two f16 values, exactly.
+__device__ __forceinline__ uint32_t e4m3x2_f16x2(uint32_t codes16) {
+  uint32_t r;
+  const uint16_t c = static_cast<uint16_t>(codes16);
+  asm("cvt.rn.f16x2.e4m3x2 %0, %1;\n" : "=r"(r) : "h"(c));
+  return r;
+}
 
 }  // namespace
 
-template <int D, int G>
+// F8: the cache holds E4M3 codes.  They are copied by TMA into the upper half
+// of each K / V tile buffer and widened there to f16 (exactly) by the loader
+// warp, Q is converted from bf16 to f16 in place once per unit, and the two
+// products run as kind::f16 with f16 operands (P in f16).  The K scale is
+// folded into the softmax scale and the V scale into the normalisation.
+template <int D, int G, bool F8>
 __global__ void __launch_bounds__(kPfThreads, 1)
     prefill_tc_kernel(const AttnParams p, const __grid_constant__ PfMaps maps) {
   using C = PfCfg<D>;
@@ -258,6 +282,17 @@ __global__ void __launch_bounds__(kPfThreads, 1)
       flag_error(p.status, PA_DEV_BLOCK_RANGE);
       ph = -1;
     }
+    if constexpr (F8) {
+      // the codes, [block][16 rows][D bytes], into the buffer's upper half
+      if (lane == 0) mbar_arrive_expect_tx(full, C::kTileBytes / 2);
+      __syncwarp();
+      if (lane < kTileN / kBlockSize) {
+        const int coord = ph < 0 ? p.num_blocks : ph;
+        tma_load_3d(dst + C::kTileBytes / 2 + lane * kBlockSize * D, is_v ? &maps.v : &maps.k, 0,
+                    0, coord * kBlockSize * p.num_kv_heads + u.g, full);
+      }
+      return;
+    }
     if (lane == 0) mbar_arrive_expect_tx(full, C::kTileBytes);
     __syncwarp();
     if (lane < kTileN / kBlockSize) {
@@ -269,6 +304,79 @@ __global__ void __launch_bounds__(kPfThreads, 1)
                     coord * kBlockSize * p.num_kv_heads + u.g, full);
     }
   };
+  // FP8: widen the codes of a landed tile to f16 in the layout the bf16 TMA
+  // copy would have produced (K: [block][8-row group][64-column half][8 rows]
+  // [128 B]; V: [block][64-column half][16 rows][128 B]; 16-byte chunks
+  // XOR-swizzled by row), in place, block by block.  Block b's f16 rows cover
+  // the codes of blocks 2b - 8 and 2b - 7 only, each read at an earlier block
+  // except block 7's own codes, which the warp reads into registers before it
+  // writes.  Rows from tile row zero_from on are written as zeros.
+  auto widen_tile = [&](uint32_t buf, bool is_v, int zero_from) {
+    constexpr int kRowChunks = D / 16;                        // 16-code chunks per row
+    constexpr int kPerLane = kBlockSize * kRowChunks / 32;    // chunks per lane per block
+    const uint32_t codes = buf + C::kTileBytes / 2;
+#pragma unroll 1
+    for (int b = 0; b < kTileN / kBlockSize; ++b) {
+      uint4 cv[kPerLane];
+#pragma unroll
+      for (int j = 0; j < kPerLane; ++j)
+        asm volatile("ld.shared.v4.b32 {%0,%1,%2,%3}, [%4];\n"
+                     : "=r"(cv[j].x), "=r"(cv[j].y), "=r"(cv[j].z), "=r"(cv[j].w)
+                     : "r"(codes + b * kBlockSize * D + (lane + 32 * j) * 16)
+                     : "memory");
+      __syncwarp();
+#pragma unroll
+      for (int j = 0; j < kPerLane; ++j) {
+        const int q = lane + 32 * j;
+        const int t = q / kRowChunks, c0 = (q % kRowChunks) * 16;
+        const bool zero = b * kBlockSize + t >= zero_from;
+        const uint32_t wd[4] = {cv[j].x, cv[j].y, cv[j].z, cv[j].w};
+        uint32_t h[8];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          h[2 * e] = zero ? 0u : e4m3x2_f16x2(wd[e] & 0xffffu);
+          h[2 * e + 1] = zero ? 0u : e4m3x2_f16x2(wd[e] >> 16);
+        }
+#pragma unroll
+        for (int o = 0; o < 2; ++o) {
+          const int col = c0 + 8 * o, half = col >> 6, ch = (col & 63) >> 3;
+          const uint32_t sw = static_cast<uint32_t>((ch ^ (t & 7)) << 4);
+          const uint32_t addr =
+              is_v ? buf + b * C::kVBlockBytes + half * (kBlockSize * 128) + t * 128 + sw
+                   : buf + b * C::kVBlockBytes + (t >> 3) * C::kKGroupBytes + half * 1024 +
+                         (t & 7) * 128 + sw;
+          asm volatile("st.shared.v4.b32 [%0], {%1,%2,%3,%4};\n" ::"r"(addr), "r"(h[4 * o]),
+                       "r"(h[4 * o + 1]), "r"(h[4 * o + 2]), "r"(h[4 * o + 3])
+                       : "memory");
+        }
+      }
+      __syncwarp();
+    }
+    fence_proxy_async_smem();  // the generic-proxy writes, before the tensor cores read them
+    __syncwarp();
+  };
+  // FP8: the landed bf16 Q tile to f16, in place (an element keeps its slot)
+  auto q_to_f16 = [&]() {
+#pragma unroll 4
+    for (int i = lane; i < C::kTileBytes / 16; i += 32) {
+      const uint32_t addr = sbase + C::kQOff + i * 16;
+      uint4 v;
+      asm volatile("ld.shared.v4.b32 {%0,%1,%2,%3}, [%4];\n"
+                   : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+                   : "r"(addr)
+                   : "memory");
+      const uint32_t wd[4] = {v.x, v.y, v.z, v.w};
+      uint32_t h[4];
+#pragma unroll
+      for (int e = 0; e < 4; ++e)
+        h[e] = pack_f16(__uint_as_float(wd[e] << 16), __uint_as_float(wd[e] & 0xffff0000u));
+      asm volatile("st.shared.v4.b32 [%0], {%1,%2,%3,%4};\n" ::"r"(addr), "r"(h[0]), "r"(h[1]),
+                   "r"(h[2]), "r"(h[3])
+                   : "memory");
+    }
+    fence_proxy_async_smem();
+    __syncwarp();
+  };
 
   if (warp == kKLoadWarp) {
     // ------------------------------------------------------------ units, Q, K
@@ -278,6 +386,8 @@ __global__ void __launch_bounds__(kPfThreads, 1)
     // arrivals (one per tile of that parity), gk: the last one that carried
     // a copy, plus one
     uint32_t nf[2] = {0, 0}, sw[2] = {0, 0}, ga[2] = {0, 0}, gk[2] = {0, 0}, nq = 0;
+    uint32_t nkl[2] = {0, 0};     // FP8: K code copies per buffer parity
+    bool kl_wait[2] = {false, false}, q_wait = false;  // FP8: copies not yet waited for
     for (int uc = 0;; ++uc) {
       int unit = 0;
       if (lane == 0) unit = atomicAdd(p.next, 1);
@@ -319,14 +429,16 @@ __global__ void __launch_bounds__(kPfThreads, 1)
       int ph = tile_phys(u, tile_of(u, 0));
       // Q tile: rows (position, head) of 128/G tokens x G heads, one box per 64 columns
       if (uc > 0 && !wait_bar(bar(kQEmpty), (uc - 1) & 1, abort, p.status)) break;
+      const uint32_t q_bar = F8 ? bar(kQLand) : bar(kQFull);
       if (lane == 0) {
-        mbar_arrive_expect_tx(bar(kQFull), C::kTileBytes);
+        mbar_arrive_expect_tx(q_bar, C::kTileBytes);
 #pragma unroll
         for (int h = 0; h < D / 64; ++h)
           tma_load_3d(sbase + C::kQOff + h * C::kRegionBytes, &maps.q, h * 64, u.g * G,
-                      u.a + u.j0, bar(kQFull));
+                      u.a + u.j0, q_bar);
       }
       ++nq;
+      q_wait = F8;
       bool ok = true;
       // K of tile sq goes into buffer w = sq & 1.  The first two were freed
       // by the previous unit (its last S of each parity was waited below);
@@ -343,7 +455,25 @@ __global__ void __launch_bounds__(kPfThreads, 1)
         } else {
           ++nf[w];
         }
-        copy_kv_tile(u, tile_of(u, sq), ph, false, sbase + C::kKOff + w * C::kTileBytes, full);
+        const uint32_t kbuf = sbase + C::kKOff + w * C::kTileBytes;
+        if constexpr (F8) {
+          copy_kv_tile(u, tile_of(u, sq), ph, false, kbuf, bar(kKLand + w));
+          ++nkl[w];
+          kl_wait[w] = true;
+          if (sq + 1 < u.n_kv) ph = tile_phys(u, tile_of(u, sq + 1));
+          if (q_wait) {  // Q to f16 while K(0)'s codes are on their way
+            if (!wait_bar(bar(kQLand), (nq - 1) & 1, abort, p.status)) { ok = false; break; }
+            q_wait = false;
+            q_to_f16();
+            if (lane == 0) mbar_arrive(bar(kQFull));
+          }
+          if (!wait_bar(bar(kKLand + w), (nkl[w] - 1) & 1, abort, p.status)) { ok = false; break; }
+          kl_wait[w] = false;
+          widen_tile(kbuf, false, 0x7fffffff);
+          if (lane == 0) mbar_arrive(full);
+          continue;
+        }
+        copy_kv_tile(u, tile_of(u, sq), ph, false, kbuf, full);
         if (sq + 1 < u.n_kv) ph = tile_phys(u, tile_of(u, sq + 1));
       }
       // tiles with no K two places on: a plain kGo arrival once their S is done
@@ -357,10 +487,16 @@ __global__ void __launch_bounds__(kPfThreads, 1)
       if (!ok) break;
     }
     if (*abort) {  // let every copy issued land before the CTA ends
-      if (nq > 0) drain_wait(bar(kQFull), (nq - 1) & 1);
-      for (int w = 0; w < 2; ++w) {
-        if (nf[w] > 0) drain_wait(bar(kKFirst + w), (nf[w] - 1) & 1);
-        if (gk[w] > 0) drain_wait(bar(kGo + w), (gk[w] - 1) & 1, kGoDrainLimit);
+      if constexpr (F8) {
+        if (q_wait) drain_wait(bar(kQLand), (nq - 1) & 1);
+        for (int w = 0; w < 2; ++w)
+          if (kl_wait[w]) drain_wait(bar(kKLand + w), (nkl[w] - 1) & 1);
+      } else {
+        if (nq > 0) drain_wait(bar(kQFull), (nq - 1) & 1);
+        for (int w = 0; w < 2; ++w) {
+          if (nf[w] > 0) drain_wait(bar(kKFirst + w), (nf[w] - 1) & 1);
+          if (gk[w] > 0) drain_wait(bar(kGo + w), (gk[w] - 1) & 1, kGoDrainLimit);
+        }
       }
     }
     __syncwarp();
@@ -388,7 +524,18 @@ __global__ void __launch_bounds__(kPfThreads, 1)
           break;
         }
         const uint32_t vb = sbase + C::kVOff + w * C::kTileBytes;
-        if (kt != u.kt0 + u.n_kv - 1 || (u.kv_end & (kBlockSize - 1)) == 0) {
+        if constexpr (F8) {
+          // codes -> kVLand, widened to f16 here; rows past the unit's last
+          // key (unwritten slots) become zeros, so p = 0 never meets a NaN
+          copy_kv_tile(u, kt, ph, true, vb, bar(kVLand + w));
+          landing = true;
+          land_w = w;
+          if (!wait_bar(bar(kVLand + w), nl[w] & 1, abort, p.status)) { ok = false; break; }
+          landing = false;
+          ++nl[w];
+          widen_tile(vb, true, u.kv_end - kt * kTileN);
+          warp_arrive(bar(kGo + w));
+        } else if (kt != u.kt0 + u.n_kv - 1 || (u.kv_end & (kBlockSize - 1)) == 0) {
           copy_kv_tile(u, kt, ph, true, vb, bar(kGo + w));  // this tile's kGo arrival
           gv[w] = nv[w] + 1;
         } else {
@@ -432,8 +579,8 @@ __global__ void __launch_bounds__(kPfThreads, 1)
     // Kept lean: every cycle this warp spends between products is tensor-core
     // idle time (the issue queue is shallow).  Counters live in registers,
     // descriptors are built once and advanced by their address field.
-    constexpr uint32_t kIdS = idesc_bf16(kTileM, kTileN, 0);
-    constexpr uint32_t kIdPV = idesc_bf16(kTileM, D, 1);
+    constexpr uint32_t kIdS = idesc_kind_f16(kTileM, kTileN, 0, F8);
+    constexpr uint32_t kIdPV = idesc_kind_f16(kTileM, D, 1, F8);
     const uint64_t dq = smem_desc_sw128(sbase + C::kQOff, 16, 1024);
     const uint64_t dk = smem_desc_sw128(sbase + C::kKOff, 16, C::kKGroupBytes);
     const uint64_t dv = smem_desc_sw128(sbase + C::kVOff, kBlockSize * 128, 1024);
@@ -668,7 +815,7 @@ __global__ void __launch_bounds__(kPfThreads, 1)
             fma2(x0, x1, __uint_as_float(sr[2 * c]), __uint_as_float(sr[2 * c + 1]), mul, -m_sub);
             const float p0 = ex2(x0), p1 = ex2(x1);
             add2(ps4[2 * (c & 1)], ps4[2 * (c & 1) + 1], p0, p1);
-            pw[c] = pack_bf16(p0, p1);
+            pw[c] = F8 ? pack_f16(p0, p1) : pack_bf16(p0, p1);
           }
           PA_TMEM_ST32(tmem_s + w * 32, pw);
           l_part += (ps4[0] + ps4[1]) + (ps4[2] + ps4[3]);
@@ -807,7 +954,20 @@ bool encode_map(CUtensorMap* m, const void* base, int rank, const cuuint64_t* di
          CUDA_SUCCESS;
 }
 
-template <int D, int G>
+// Byte (uint8) tensor map with no swizzle and zero fill out of bounds (FP8 codes).
+bool encode_map_u8(CUtensorMap* m, const void* base, int rank, const cuuint64_t* dims,
+                   const cuuint64_t* strides_bytes, const cuuint32_t* box) {
+  const auto enc = tensor_map_encoder();
+  if (!enc) return false;
+  const cuuint32_t estride[5] = {1, 1, 1, 1, 1};
+  return enc(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, static_cast<cuuint32_t>(rank),
+             const_cast<void*>(base), dims, strides_bytes, box, estride,
+             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) ==
+         CUDA_SUCCESS;
+}
+
+template <int D, int G, bool F8>
 cudaError_t launch_pf(const AttnParams& p, int num_sms, cudaStream_t stream) {
   using C = PfCfg<D>;
   static bool configured[64] = {false};
@@ -816,7 +976,7 @@ cudaError_t launch_pf(const AttnParams& p, int num_sms, cudaStream_t stream) {
   if (e != cudaSuccess) return e;
   if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
   if (!configured[dev]) {
-    e = cudaFuncSetAttribute(prefill_tc_kernel<D, G>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    e = cudaFuncSetAttribute(prefill_tc_kernel<D, G, F8>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              C::kSmemBytes);
     if (e != cudaSuccess) return e;
     configured[dev] = true;
@@ -830,7 +990,18 @@ cudaError_t launch_pf(const AttnParams& p, int num_sms, cudaStream_t stream) {
     const cuuint32_t box[3] = {64, static_cast<cuuint32_t>(G), static_cast<cuuint32_t>(kTileM / G)};
     if (!encode_map(&maps.q, p.q, 3, dims, strides, box)) return cudaErrorInvalidValue;
   }
-  {
+  if constexpr (F8) {
+    // codes of one (block, head): 16 rows of D bytes at a stride of Hkv x D;
+    // the last index steps one head (D bytes), as in the bf16 K map
+    const cuuint64_t hkv = static_cast<cuuint64_t>(p.num_kv_heads);
+    const cuuint64_t dims[3] = {static_cast<cuuint64_t>(D), static_cast<cuuint64_t>(kBlockSize),
+                                static_cast<cuuint64_t>(p.num_blocks) * kBlockSize * hkv};
+    if (dims[2] + hkv > 0x7fffffffull) return cudaErrorInvalidValue;
+    const cuuint64_t strides[2] = {hkv * D, static_cast<cuuint64_t>(D)};
+    const cuuint32_t box[3] = {static_cast<cuuint32_t>(D), static_cast<cuuint32_t>(kBlockSize), 1};
+    if (!encode_map_u8(&maps.k, p.k_cache, 3, dims, strides, box)) return cudaErrorInvalidValue;
+    if (!encode_map_u8(&maps.v, p.v_cache, 3, dims, strides, box)) return cudaErrorInvalidValue;
+  } else {
     const cuuint64_t hkv = static_cast<cuuint64_t>(p.num_kv_heads);
     const cuuint64_t row = hkv * D * e2;  // bytes between a block's rows
     // K: (64 columns, 8 rows, D/64 halves, 2 row groups, block x 16 x Hkv + head);
@@ -853,30 +1024,39 @@ cudaError_t launch_pf(const AttnParams& p, int num_sms, cudaStream_t stream) {
                                 static_cast<cuuint32_t>(D / 64), 1, 1};
     if (!encode_map(&maps.v, p.v_cache, 5, vdims, vstrides, vbox)) return cudaErrorInvalidValue;
   }
-  prefill_tc_kernel<D, G><<<num_sms, kPfThreads, C::kSmemBytes, stream>>>(p, maps);
+  prefill_tc_kernel<D, G, F8><<<num_sms, kPfThreads, C::kSmemBytes, stream>>>(p, maps);
   return cudaGetLastError();
 }
 
 }  // namespace
 
-cudaError_t launch_prefill_tc(const AttnParams& p, int head_size, int group, int num_sms,
-                              cudaStream_t stream) {
+namespace {
+template <bool F8>
+cudaError_t launch_pf_dtype(const AttnParams& p, int head_size, int group, int num_sms,
+                            cudaStream_t stream) {
   if (head_size == 128) {
     switch (group) {
-      case 1: return launch_pf<128, 1>(p, num_sms, stream);
-      case 2: return launch_pf<128, 2>(p, num_sms, stream);
-      case 4: return launch_pf<128, 4>(p, num_sms, stream);
-      case 8: return launch_pf<128, 8>(p, num_sms, stream);
+      case 1: return launch_pf<128, 1, F8>(p, num_sms, stream);
+      case 2: return launch_pf<128, 2, F8>(p, num_sms, stream);
+      case 4: return launch_pf<128, 4, F8>(p, num_sms, stream);
+      case 8: return launch_pf<128, 8, F8>(p, num_sms, stream);
     }
   } else if (head_size == 64) {
     switch (group) {
-      case 1: return launch_pf<64, 1>(p, num_sms, stream);
-      case 2: return launch_pf<64, 2>(p, num_sms, stream);
-      case 4: return launch_pf<64, 4>(p, num_sms, stream);
-      case 8: return launch_pf<64, 8>(p, num_sms, stream);
+      case 1: return launch_pf<64, 1, F8>(p, num_sms, stream);
+      case 2: return launch_pf<64, 2, F8>(p, num_sms, stream);
+      case 4: return launch_pf<64, 4, F8>(p, num_sms, stream);
+      case 8: return launch_pf<64, 8, F8>(p, num_sms, stream);
     }
   }
   return cudaErrorInvalidValue;
+}
+}  // namespace
+
+cudaError_t launch_prefill_tc(const AttnParams& p, int head_size, int group, int num_sms,
+                              bool fp8_cache, cudaStream_t stream) {
+  return fp8_cache ? launch_pf_dtype<true>(p, head_size, group, num_sms, stream)
+                   : launch_pf_dtype<false>(p, head_size, group, num_sms, stream);
 }
 
 }  // namespace pa

@@ -163,15 +163,19 @@ __device__ __forceinline__ uint64_t smem_desc_sw128(uint32_t saddr, uint32_t lbo
   d |= static_cast<uint64_t>(2) << 61;  // 128-byte swizzle
   return d;
 }
-// Instruction descriptor, kind::f16: fp32 accumulator, bf16 A and B,
-// A K-major, B K-major (b_mn_major = 0) or MN-major (1), shape M x N.
-__host__ __device__ constexpr uint32_t idesc_bf16(int M, int N, int b_mn_major) {
+// Instruction descriptor, kind::f16: fp32 accumulator, A and B both bf16
+// (f16 = false) or both f16 (f16 = true), A K-major, B K-major
+// (b_mn_major = 0) or MN-major (1), shape M x N.
+__host__ __device__ constexpr uint32_t idesc_kind_f16(int M, int N, int b_mn_major, bool f16) {
   return (1u << 4)                                   // D format: f32
-         | (1u << 7)                                 // A format: bf16
-         | (1u << 10)                                // B format: bf16
+         | ((f16 ? 0u : 1u) << 7)                    // A format: f16 0, bf16 1
+         | ((f16 ? 0u : 1u) << 10)                   // B format: f16 0, bf16 1
          | (static_cast<uint32_t>(b_mn_major) << 16) // B major
          | (static_cast<uint32_t>(N >> 3) << 17)     // N / 8
          | (static_cast<uint32_t>(M >> 4) << 24);    // M / 16
+}
+__host__ __device__ constexpr uint32_t idesc_bf16(int M, int N, int b_mn_major) {
+  return idesc_kind_f16(M, N, b_mn_major, false);
 }
 
 }  // namespace pa

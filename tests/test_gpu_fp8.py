@@ -75,3 +75,20 @@ def test_fp8_layout_checks():
         P.pa_forward_workspace_size(P.layout_of(kc, 4, dtype=torch.float32), 1, 1, 16)
     with pytest.raises(P.PaError):
         P.pa_forward_workspace_size(P.layout_of(kc, 4, k_scale=0.0), 1, 1, 16)
+
+
+def test_fp8_chunks_on_tensor_cores():
+    """Chunks of 17-300 tokens over an 8-bit cache take the tensor-core prefill
+    kernel (codes widened to f16 in shared memory); with fewer units than SMs
+    their KV is split into pieces that are merged.  Checked against the oracle
+    over the dequantised cache."""
+    spec = W.custom_spec("fp8-chunks", "bf16", 8, 2, 128, [1, 300, 1, 64, 17],
+                         [700, 2300, 40, 64, 900], seed=77)
+    _run(spec, 0.01, 0.02)
+
+
+def test_fp8_mixed_step():
+    """The mixed continuous-batching step (192 decodes, two 512-token chunks)
+    over an 8-bit cache: decode and few-token kernels read codes, the chunks
+    run on the tensor cores."""
+    _run(W.spec_mixed_step(), 0.01, 0.01)
