@@ -208,6 +208,43 @@ __global__ void __launch_bounds__(MmaCfg<D, G, P, NW, NS, F8>::kThreads,
     if (lane == 0) u = atomicAdd(p.next, 1);
     return __shfl_sync(0xffffffffu, u, 0);
   };
+  // The CTA's first two units, decoded together so that their dependent
+  // loads (dispatch slot, record, block-table slice) overlap.
+  auto fetch_first_two = [&](int u0, int u1) {  // whole scheduler warp
+    const bool v0 = u0 < n_units, v1 = u1 < n_units;
+    const int k0 = u0 / Hkv, k1 = u1 / Hkv;
+    int item0 = k0, item1 = k1;
+    if (p.order) {
+      if (v0) item0 = __ldg(p.order + k0);
+      if (v1) item1 = __ldg(p.order + k1);
+    }
+    const int4 z = make_int4(0, 0, 0, 0);
+    const int4 a0 = v0 ? __ldg(&p.recs[item0].a) : z, a1 = v1 ? __ldg(&p.recs[item1].a) : z;
+    const int4 b0 = v0 ? __ldg(&p.recs[item0].b) : z, b1 = v1 ? __ldg(&p.recs[item1].b) : z;
+    const int4 c0 = v0 ? __ldg(&p.recs[item0].c) : z, c1 = v1 ? __ldg(&p.recs[item1].c) : z;
+    const int32_t* row0 = p.block_tables + static_cast<long long>(a0.x) * p.max_blocks_per_seq;
+    const int32_t* row1 = p.block_tables + static_cast<long long>(a1.x) * p.max_blocks_per_seq;
+    const int n0 = a0.w - a0.z, n1 = a1.w - a1.z;
+    for (int i = lane; i < max(n0, n1); i += 32) {
+      if (i < n0) meta[0].bt[i] = __ldg(row0 + a0.z + i);
+      if (i < n1) meta[1].bt[i] = __ldg(row1 + a1.z + i);
+    }
+    if (lane == 0) {
+      UnitMeta* m[2] = {&meta[0], &meta[1]};
+      const int4 ra[2] = {a0, a1}, rb[2] = {b0, b1}, rc[2] = {c0, c1};
+      const int us[2] = {u0, u1}, ks[2] = {k0, k1}, it[2] = {item0, item1};
+      const bool vs[2] = {v0, v1};
+#pragma unroll
+      for (int j = 0; j < 2; ++j) {
+        m[j]->valid = vs[j] ? 1 : 0;
+        if (!vs[j]) continue;
+        m[j]->item = it[j]; m[j]->g = us[j] - ks[j] * Hkv; m[j]->r = ra[j].x; m[j]->a = rb[j].w;
+        m[j]->j0 = ra[j].y; m[j]->npos = rc[j].x; m[j]->pos0 = rc[j].y; m[j]->kv_hi = rc[j].z;
+        m[j]->b0 = ra[j].z; m[j]->b1 = ra[j].w;
+        m[j]->tile = rb[j].x; m[j]->first = rb[j].y; m[j]->nsplit = rb[j].z;
+      }
+    }
+  };
   // q rows of unit m (row = position row/G, head row%G), loaded into registers
   // first and stored later, so the loads overlap other scheduler work.
   constexpr int kQPerLane = (R * C::kChunks + 31) / 32;
@@ -269,16 +306,22 @@ __global__ void __launch_bounds__(MmaCfg<D, G, P, NW, NS, F8>::kThreads,
     // A second unit is claimed up front only if every CTA can still get one:
     // with fewer units than that (small steps), taking two would leave other
     // CTAs idle while this one works through both.
-    const int u0 = claim();
-    const int u1 = (!PA_SPARE_CLAIM || u0 + static_cast<int>(gridDim.x) < n_units) ? claim()
-                                                                                    : n_units;
+    int u0, u1;
+    if (n_units >= 2 * static_cast<int>(gridDim.x)) {  // two units for every CTA: one claim
+      int base = 0;
+      if (lane == 0) base = atomicAdd(p.next, 2);
+      u0 = __shfl_sync(0xffffffffu, base, 0);
+      u1 = u0 + 1;
+    } else {
+      u0 = claim();
+      u1 = (!PA_SPARE_CLAIM || u0 + static_cast<int>(gridDim.x) < n_units) ? claim() : n_units;
+    }
     const int u2 = PA_CLAIM_AHEAD ? claim() : 0;
     if (lane == 0) {
       s_next_u = u2;
       s_tail.valid = 0;
     }
-    fetch_unit(meta[0], u0);
-    fetch_unit(meta[1], u1);
+    fetch_first_two(u0, u1);
     __syncwarp();
     uint4 qv[kQPerLane];
     load_q(meta[0], qv);

@@ -26,6 +26,7 @@ namespace pa {
 namespace {
 
 constexpr int kPlanThreads = 1024;
+constexpr int kShortItems = 2048;  // short decode items listed in shared memory (else re-read)
 
 #ifndef PA_UNITS_PER_CTA
 #define PA_UNITS_PER_CTA 8  // split-size target: decode units per CTA (see plan_kernel)
@@ -107,6 +108,8 @@ __global__ void __launch_bounds__(kPlanThreads, 1) plan_kernel(PlanParams p) {
   __shared__ unsigned long long s_blocks_d;      // ... of the decode requests among them
   __shared__ unsigned long long s_pf_tiles;      // prefill query tiles of the step
   __shared__ unsigned long long s_pf_kv;         // KV tiles those query tiles see, summed
+  __shared__ int2 s_short[kShortItems];          // short decode items: (item, blocks)
+  __shared__ int s_nshort;
   static_assert(kMaxUnitBlocks == 8 * 32, "the dispatch-order scan gives each lane 8 sizes");
   // The attention kernel that follows may become resident now; it waits for
   // this grid to finish before it reads the work lists.  This grid itself may
@@ -140,9 +143,8 @@ __global__ void __launch_bounds__(kPlanThreads, 1) plan_kernel(PlanParams p) {
     s_blocks_d = 0;
     s_pf_tiles = 0;
     s_pf_kv = 0;
+    s_nshort = 0;
     for (int i = 0; i < kLists; ++i) carry[i] = 0;
-    const int q0 = __ldg(p.qsl), qB = __ldg(p.qsl + B);
-    if (q0 != 0 || qB != p.num_tokens) err |= PA_DEV_QSL;
   }
   __syncthreads();
 
@@ -156,7 +158,10 @@ __global__ void __launch_bounds__(kPlanThreads, 1) plan_kernel(PlanParams p) {
     const int pm = p.prefill_rows / p.group;  // positions per prefill query tile
     for (int r = threadIdx.x; r < B; r += kPlanThreads) {
       const int S = __ldg(p.seq_lens + r);
-      const int L = __ldg(p.qsl + r + 1) - __ldg(p.qsl + r);
+      const int qa = __ldg(p.qsl + r), qb = __ldg(p.qsl + r + 1);
+      // the ends of query_start_loc, checked by the threads that load them
+      if ((r == 0 && qa != 0) || (r == B - 1 && qb != p.num_tokens)) atomicOr(&err, PA_DEV_QSL);
+      const int L = qb - qa;
       if (S < 1 || S > p.max_seq_len || L < 1 || L > S) continue;
       if (L < p.prefill_min_qlen) {
         mine += static_cast<unsigned long long>(ceil_div(S, kBlockSize));
@@ -299,7 +304,11 @@ __global__ void __launch_bounds__(kPlanThreads, 1) plan_kernel(PlanParams p) {
         // long items take dispatch slots in request order (they are a prefix
         // of the request's splits, and off[5] + s <= i); short ones are counted
         if (s < cnt[5]) order_d[off[5] + s] = i;
-        else atomicAdd(&size_hist[b1 - b0], 1);
+        else {
+          atomicAdd(&size_hist[b1 - b0], 1);
+          const int j = atomicAdd(&s_nshort, 1);
+          if (j < kShortItems) s_short[j] = make_int2(i, b1 - b0);
+        }
         recs_d[i].a = make_int4(r, 0, b0, b1);
         recs_d[i].b = make_int4(tile, off[0], ns, a);
         recs_d[i].c = make_int4(1, S - 1, min(b1 * kBlockSize, S), 0);
@@ -400,10 +409,17 @@ __global__ void __launch_bounds__(kPlanThreads, 1) plan_kernel(PlanParams p) {
     }
   }
   __syncthreads();
-  for (int i = threadIdx.x; i < n_di; i += kPlanThreads) {
-    // short = under half a split (full splits hold at least bps_d blocks)
-    const int4 a = recs_d[i].a;  // written above by this CTA
-    if (2 * (a.w - a.z) < bps_d) order_d[atomicAdd(&size_hist[a.w - a.z], 1)] = i;
+  if (s_nshort <= kShortItems) {
+    for (int j = threadIdx.x; j < s_nshort; j += kPlanThreads) {
+      const int2 e = s_short[j];
+      order_d[atomicAdd(&size_hist[e.y], 1)] = e.x;
+    }
+  } else {
+    for (int i = threadIdx.x; i < n_di; i += kPlanThreads) {
+      // short = under half a split (full splits hold at least bps_d blocks)
+      const int4 a = recs_d[i].a;  // written above by this CTA
+      if (2 * (a.w - a.z) < bps_d) order_d[atomicAdd(&size_hist[a.w - a.z], 1)] = i;
+    }
   }
   for (int i = threadIdx.x; i < n_dt * p.num_kv_heads; i += kPlanThreads) cnt_d[i] = 0;
   for (int i = threadIdx.x; i < n_st * p.num_kv_heads; i += kPlanThreads) cnt_s[i] = 0;
