@@ -850,7 +850,8 @@ def run_gpu_arm(args):
                    "l2": "no flush: KV read per step (1.4 GB) > L2 (126 MB)",
                    "parallelism": f"{world} replicas" if world > 1 else "single GPU",
                    "algorithmic_bytes_per_step": w["step_bytes"]},
-        "roofline": {"bound": "hbm", "kernel": "attn_mma_kernel<128,4,1,4,2> (decode)",
+        "roofline": {"bound": "hbm",
+                     "kernel": "attn_mma_kernel<128,4,1,4,2,0,0> (decode, query rows as M)",
                      "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
                      "peak_source": peak_src, "traffic": traffic,
                      "nominal_peak": NOMINAL_HBM_GBS, "frac_of_nominal": achieved / NOMINAL_HBM_GBS,

@@ -11,16 +11,18 @@
 
 namespace pa {
 cudaError_t launch_attn_mma_bf16(const AttnParams& p, int head_size, int group, int positions,
-                                 int num_sms, cudaStream_t stream, int* grid_only);
+                                 bool keys_as_m, int num_sms, cudaStream_t stream,
+                                 int* grid_only);
 cudaError_t launch_attn_cc_f32(const AttnParams& p, int head_size, int group, int positions,
                                int num_sms, cudaStream_t stream, int* grid_only);
 
 cudaError_t launch_attn_by_dtype(const AttnParams& p, pa_dtype dtype, int head_size, int group,
-                                 int positions, int num_sms, cudaStream_t stream,
+                                 int positions, bool keys_as_m, int num_sms, cudaStream_t stream,
                                  int* grid_only) {
-  return dtype == PA_BF16
-             ? launch_attn_mma_bf16(p, head_size, group, positions, num_sms, stream, grid_only)
-             : launch_attn_cc_f32(p, head_size, group, positions, num_sms, stream, grid_only);
+  return dtype == PA_BF16 ? launch_attn_mma_bf16(p, head_size, group, positions, keys_as_m,
+                                                 num_sms, stream, grid_only)
+                          : launch_attn_cc_f32(p, head_size, group, positions, num_sms, stream,
+                                               grid_only);
 }
 
 namespace {
@@ -329,16 +331,22 @@ int pa_forward(const void* q, const void* k_cache, const void* v_cache,
   pp.max_blocks_per_seq = max_blocks_per_seq;
   pp.bps = blocks_per_split(layout);
   pp.num_sms = num_sms;
+  const bool tc_prefill = layout->dtype == PA_BF16;  // bf16 or FP8 cache
+  const bool run_prefill = tc_prefill && max_query_len >= kPrefillMinQlen;
+  // bf16 decode tiles: keys as the MMA's M dimension when the step also runs
+  // the tensor-core prefill kernel (the decode kernel then shares the GPU and
+  // is not purely HBM-bound: the mixed step's decode 258 -> 229 us), query
+  // rows as M otherwise (alone, HBM-bound: 225 vs 231 us on Llama-3-8B)
+  const bool keys_as_m = run_prefill;
   {
     AttnParams none{};
     e = fp8_cache(layout)
             ? launch_attn_fp8(none, layout->head_size, group, 1, num_sms, st, &pp.num_ctas)
-            : launch_attn_by_dtype(none, layout->dtype, layout->head_size, group, 1, num_sms, st,
-                                   &pp.num_ctas);
+            : launch_attn_by_dtype(none, layout->dtype, layout->head_size, group, 1, keys_as_m,
+                                   num_sms, st, &pp.num_ctas);
     if (e != cudaSuccess) return fail_cuda(e, "decode grid size");
   }
   pp.small_positions = small_positions(layout);
-  const bool tc_prefill = layout->dtype == PA_BF16;  // bf16 or FP8 cache
   pp.prefill_min_qlen = tc_prefill ? kPrefillMinQlen : 0x7fffffff;
   pp.prefill_rows = kPrefillRows;
   pp.group = group;
@@ -354,7 +362,6 @@ int pa_forward(const void* q, const void* k_cache, const void* v_cache,
   // decode kernel so that decode CTAs fill the SMs the prefill CTAs leave:
   // the HBM-bound and the tensor-bound work overlap.  With the overlap off it
   // runs on `st` before the decode kernel.
-  const bool run_prefill = tc_prefill && max_query_len >= kPrefillMinQlen;
   const bool fork = run_prefill && g_prefill_overlap;
   SideStream* side = nullptr;
   if (fork) {
@@ -419,7 +426,8 @@ int pa_forward(const void* q, const void* k_cache, const void* v_cache,
   if (g_prof_start) cudaEventRecord(g_prof_start, st);
   e = fp8_cache(layout)
           ? launch_attn_fp8(ap, layout->head_size, group, 1, num_sms, st)
-          : launch_attn_by_dtype(ap, layout->dtype, layout->head_size, group, 1, num_sms, st);
+          : launch_attn_by_dtype(ap, layout->dtype, layout->head_size, group, 1, keys_as_m, num_sms,
+                                 st);
   if (e != cudaSuccess) return fail_cuda(e, "decode attention launch");
   if (g_prof_stop) cudaEventRecord(g_prof_stop, st);
 
@@ -437,7 +445,7 @@ int pa_forward(const void* q, const void* k_cache, const void* v_cache,
     e = fp8_cache(layout)
             ? launch_attn_fp8(ap, layout->head_size, group, small_positions(layout), num_sms, st)
             : launch_attn_by_dtype(ap, layout->dtype, layout->head_size, group,
-                                   small_positions(layout), num_sms, st);
+                                   small_positions(layout), false, num_sms, st);
     if (e != cudaSuccess) return fail_cuda(e, "small-q attention launch");
   }
   if (fork) {

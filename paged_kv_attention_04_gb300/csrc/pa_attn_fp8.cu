@@ -17,9 +17,11 @@ namespace {
 template <int D, int G>
 cudaError_t dispatch_positions_fp8(const AttnParams& p, int positions, int num_sms,
                                    cudaStream_t stream, int* grid_only) {
+  // decode tiles with the keys as M (three CTAs per SM): measured faster than
+  // query rows as M for every FP8 workload
   if (positions == 1)
-    return launch_mma<D, G, 1, PA_MMA_FP8_WARPS, PA_MMA_FP8_STAGES, true>(p, num_sms, stream,
-                                                                          grid_only);
+    return launch_mma<D, G, 1, PA_MMA_FP8_WARPS, PA_MMA_FP8_STAGES, true, true>(p, num_sms,
+                                                                                stream, grid_only);
   return launch_mma<D, G, kSmallRows / G, PA_MMA_FP8_WARPS, PA_MMA_FP8_STAGES, true>(
       p, num_sms, stream, grid_only);
 }

@@ -108,6 +108,13 @@ __device__ __forceinline__ uint32_t pack_f16(float lo, float hi) {
   asm("cvt.rn.f16x2.f32 %0, %1, %2;\n" : "=r"(r) : "f"(hi), "f"(lo));
   return r;
 }
+// Transpose of an 8 x 8 matrix of 16-bit elements held one row pair per
+// lane (lane l: row l / 4, columns 2 (l % 4), 2 (l % 4) + 1).
+__device__ __forceinline__ uint32_t movm_trans(uint32_t x) {
+  uint32_t r;
+  asm volatile("movmatrix.sync.aligned.m8n8.trans.b16 %0, %1;\n" : "=r"(r) : "r"(x));
+  return r;
+}
 // Two E4M3 codes (low byte first) -> two f16 values, exactly.
 __device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint32_t codes16) {
   uint32_t r;
@@ -116,7 +123,9 @@ __device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint32_t codes16) {
   return r;
 }
 
-template <int D, int G, int P, int NW, int NS, bool F8>
+// SW (decode tiles only, P = 1): the keys are the MMA's M dimension and the
+// G <= 8 query rows its N; otherwise the query rows are M, padded to 16.
+template <int D, int G, int P, int NW, int NS, bool F8, bool SW>
 struct MmaCfg {
   static constexpr int kR = P * G;                 // real query rows (<= 16)
   static constexpr int kRowBytes = D * 2;          // a 16-bit tile row (bf16, or f16 from FP8)
@@ -143,8 +152,11 @@ struct MmaCfg {
   static constexpr int kMlBytes = 2 * NW * kR * 2 * 4;
   static constexpr int kMetaOff = (kMlOff + kMlBytes + 15) / 16 * 16;
   static constexpr int kSmemBytes = kMetaOff + 3 * static_cast<int>(sizeof(UnitMeta));
-  // two CTAs per SM when their shared memory fits (228 KB per SM, 1 KB reserved per CTA)
-  static constexpr int kMinCtas = 2 * (kSmemBytes + 1024 + 64) <= 228 * 1024 ? 2 : 1;
+  // CTAs per SM that shared memory allows (228 KB per SM, 1 KB reserved per CTA):
+  // two when they fit, three for FP8 keys-as-M tiles (their registers allow it)
+  static constexpr int kFit = (228 * 1024) / (kSmemBytes + 1024 + 64);
+  static constexpr int kMinCtas = (F8 && SW && kFit >= 3) ? 3 : (kFit >= 2 ? 2 : 1);
+  static_assert(!SW || P == 1, "keys-as-M tiles are for decode (one position)");
   static_assert(kSmemBytes <= 227 * 1024, "shared memory per CTA exceeds 227 KB");
   static_assert(kR <= 16, "at most 16 query rows per tile");
   static_assert(NS >= 2 && NS <= 8, "2 to 8 pipeline stages");
@@ -158,11 +170,11 @@ __device__ __forceinline__ uint32_t swz(int t, int c) {
   return static_cast<uint32_t>(t * RowBytes + ((c ^ (t & 7)) << 4));
 }
 
-template <int D, int G, int P, int NW, int NS, bool F8>
-__global__ void __launch_bounds__(MmaCfg<D, G, P, NW, NS, F8>::kThreads,
-                                  MmaCfg<D, G, P, NW, NS, F8>::kMinCtas)
+template <int D, int G, int P, int NW, int NS, bool F8, bool SW>
+__global__ void __launch_bounds__(MmaCfg<D, G, P, NW, NS, F8, SW>::kThreads,
+                                  MmaCfg<D, G, P, NW, NS, F8, SW>::kMinCtas)
     attn_mma_kernel(const AttnParams p) {
-  using C = MmaCfg<D, G, P, NW, NS, F8>;
+  using C = MmaCfg<D, G, P, NW, NS, F8, SW>;
   constexpr int R = C::kR;
   extern __shared__ __align__(128) unsigned char smem[];
 
@@ -545,6 +557,197 @@ __global__ void __launch_bounds__(MmaCfg<D, G, P, NW, NS, F8>::kThreads,
         iss_unit = k;
         iss_i = 0;
       }
+      if constexpr (SW) {
+        // Decode tile, keys as M: S^T = K Q^T (16 keys x 8 query rows) and
+        // O^T += V^T P^T (16 head dims x 8 rows per m-tile): half the MMAs and
+        // accumulators of a tile with the R <= 8 query rows padded to 16 as M.
+        // Lane (g, c) = (lane / 4, lane % 4) holds S^T at keys g, g + 8 and
+        // query rows 2c, 2c + 1, and O^T of m-tile mt at head dims
+        // dim_of_m(mt, g), dim_of_m(mt, g + 8), rows 2c, 2c + 1.
+        const int g = lane >> 2, c4 = lane & 3;
+        const int r0 = 2 * c4, r1 = r0 + 1;  // this lane's query rows
+        // q^T (B operand): b0 / b1 = dims 0-7 / 8-15 of k-step kk, q rows 0-7
+        uint32_t qb[C::kKSteps][2];
+        {
+          const uint32_t qbuf = q_u32 + (k & 1) * 16 * C::kRowBytes;
+#pragma unroll
+          for (int kk = 0; kk < C::kKSteps; kk += 2)
+            ldsm_x4(qbuf + swz<C::kRowBytes>(lane & 7, 2 * kk + (lane >> 3)), qb[kk][0], qb[kk][1],
+                    qb[kk + 1][0], qb[kk + 1][1]);
+        }
+        float o[C::kKSteps][4];
+#pragma unroll
+        for (int j = 0; j < C::kKSteps; ++j) o[j][0] = o[j][1] = o[j][2] = o[j][3] = 0.f;
+        float m0 = -CUDART_INF_F, m1 = -CUDART_INF_F, l0 = 0.f, l1 = 0.f;
+        const int nb = share(cur);
+        for (int i = 0; i < nb; ++i) {
+          issue_one(k + 1);
+          wait_for(computed);
+          const uint32_t st = ring_u32 + (computed % NS) * C::kStageBytes;
+          const int tok0 = (cur.b0 + warp + i * NW) * kBlockSize;
+          // S^T in two accumulators (even / odd k-steps): two shorter MMA chains
+          float sa[4] = {0.f, 0.f, 0.f, 0.f}, sb[4] = {0.f, 0.f, 0.f, 0.f};
+          if constexpr (F8) {
+            // K codes as A fragments: with the head dims permuted as on the q rows,
+            // pi(kk, k) = (D/4)*((k%8)/2) + 4*kk + (k%2) + 2*(k/8), lane (g, c) needs
+            // for k-step kk the 4 codes at (D/4)*c + 4*kk of keys g and g + 8
+            uint32_t kw[2][D / 16];
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+              const int t = g + 8 * h;
+#pragma unroll
+              for (int j = 0; j < D / 64; ++j) {
+                const int cc = (D / 64) * c4 + j;
+                uint4 v;
+                asm volatile("ld.shared.v4.b32 {%0,%1,%2,%3}, [%4];\n"
+                             : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+                             : "r"(st + t * C::kCacheRowBytes + ((cc ^ (t & (C::kCacheChunks - 1))) << 4)));
+                kw[h][4 * j] = v.x; kw[h][4 * j + 1] = v.y; kw[h][4 * j + 2] = v.z; kw[h][4 * j + 3] = v.w;
+              }
+            }
+#pragma unroll
+            for (int kk = 0; kk < C::kKSteps; ++kk) {
+              const uint32_t a[4] = {e4m3x2_to_f16x2(kw[0][kk]), e4m3x2_to_f16x2(kw[1][kk]),
+                                     e4m3x2_to_f16x2(kw[0][kk] >> 16), e4m3x2_to_f16x2(kw[1][kk] >> 16)};
+              mma_f16((kk & 1) ? sb : sa, a, qb[kk][0], qb[kk][1]);
+            }
+          } else {
+            // K rows as A fragments: matrices (keys 0-7 | 8-15) x (dims 0-7 | 8-15)
+#pragma unroll
+            for (int kk = 0; kk < C::kKSteps; ++kk) {
+              uint32_t a[4];
+              ldsm_x4(st + swz<C::kRowBytes>((lane & 7) + ((lane >> 3) & 1) * 8, 2 * kk + (lane >> 4)),
+                      a[0], a[1], a[2], a[3]);
+              mma_bf16((kk & 1) ? sb : sa, a, qb[kk][0], qb[kk][1]);
+            }
+          }
+          // mask and online softmax (base 2): s[0] (key g, row r0), s[1] (key g, r1),
+          // s[2] (key g + 8, r0), s[3] (key g + 8, r1); rows >= R are padding
+          float s[4];
+          {
+            const int ka = tok0 + g, kb = ka + 8;
+            const bool va = ka < cur.kv_hi && ka <= cur.pos0, vb = kb < cur.kv_hi && kb <= cur.pos0;
+            const bool ra = r0 < R, rb = r1 < R;
+            s[0] = (va && ra) ? (sa[0] + sb[0]) * p.scale_log2 : -CUDART_INF_F;
+            s[1] = (va && rb) ? (sa[1] + sb[1]) * p.scale_log2 : -CUDART_INF_F;
+            s[2] = (vb && ra) ? (sa[2] + sb[2]) * p.scale_log2 : -CUDART_INF_F;
+            s[3] = (vb && rb) ? (sa[3] + sb[3]) * p.scale_log2 : -CUDART_INF_F;
+          }
+          float mx0 = fmaxf(s[0], s[2]), mx1 = fmaxf(s[1], s[3]);
+#pragma unroll
+          for (int o8 = 4; o8 < 32; o8 <<= 1) {
+            mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, o8));
+            mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, o8));
+          }
+          const float mn0 = fmaxf(m0, mx0), mn1 = fmaxf(m1, mx1);
+          float corr0 = 1.f, corr1 = 1.f, pr[4];
+          if (mn0 != -CUDART_INF_F) {
+            corr0 = exp2f(m0 - mn0);
+            pr[0] = exp2f(s[0] - mn0);
+            pr[2] = exp2f(s[2] - mn0);
+          } else {
+            pr[0] = pr[2] = 0.f;
+          }
+          if (mn1 != -CUDART_INF_F) {
+            corr1 = exp2f(m1 - mn1);
+            pr[1] = exp2f(s[1] - mn1);
+            pr[3] = exp2f(s[3] - mn1);
+          } else {
+            pr[1] = pr[3] = 0.f;
+          }
+          l0 = l0 * corr0 + (pr[0] + pr[2]);
+          l1 = l1 * corr1 + (pr[1] + pr[3]);
+          m0 = mn0;
+          m1 = mn1;
+          if (__any_sync(0xffffffffu, corr0 != 1.f || corr1 != 1.f)) {
+#pragma unroll
+            for (int mt = 0; mt < C::kKSteps; ++mt) {
+              o[mt][0] *= corr0; o[mt][1] *= corr1;
+              o[mt][2] *= corr0; o[mt][3] *= corr1;
+            }
+          }
+          // P^T as the B operand: an 8 x 8 transpose per half of the block's keys
+          // takes (key g, rows 2c, 2c + 1) to (keys 2c, 2c + 1, row g)
+          const uint32_t pb0 = movm_trans(F8 ? pack_f16(pr[0], pr[1]) : pack_bf16(pr[0], pr[1]));
+          const uint32_t pb1 = movm_trans(F8 ? pack_f16(pr[2], pr[3]) : pack_bf16(pr[2], pr[3]));
+          if constexpr (F8) {
+            // V codes as A fragments of V^T: with the head dims of m-tile mt
+            // permuted as dim_of_m(mt, m) = (D/8)*(m%8) + 2*mt + m/8, lane (g, c)
+            // reads the D/8 codes at (D/8)*g of keys 2c, 2c+1, 2c+8, 2c+9 and
+            // pairs two keys' codes per conversion
+            const uint32_t vt = st + C::kRawTileBytes;
+            uint32_t vw[4][D / 32];
+#pragma unroll
+            for (int i4 = 0; i4 < 4; ++i4) {
+              const int t = 2 * c4 + (i4 & 1) + 8 * (i4 >> 1);
+              if constexpr (D == 128) {
+                uint4 v;
+                asm volatile("ld.shared.v4.b32 {%0,%1,%2,%3}, [%4];\n"
+                             : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+                             : "r"(vt + t * C::kCacheRowBytes + ((g ^ (t & 7)) << 4)));
+                vw[i4][0] = v.x; vw[i4][1] = v.y; vw[i4][2] = v.z; vw[i4][3] = v.w;
+              } else {
+                uint2 v;
+                asm volatile("ld.shared.v2.b32 {%0,%1}, [%2];\n"
+                             : "=r"(v.x), "=r"(v.y)
+                             : "r"(vt + t * C::kCacheRowBytes + (((g >> 1) ^ (t & 3)) << 4) +
+                                   ((g & 1) << 3)));
+                vw[i4][0] = v.x; vw[i4][1] = v.y;
+              }
+            }
+#pragma unroll
+            for (int mt = 0; mt < C::kKSteps; ++mt) {
+              const int w = mt >> 1;
+              const uint32_t sel0 = (mt & 1) ? 0x62u : 0x40u;  // byte of dim 2mt, two keys
+              const uint32_t sel1 = (mt & 1) ? 0x73u : 0x51u;  // byte of dim 2mt + 1
+              const uint32_t a[4] = {e4m3x2_to_f16x2(__byte_perm(vw[0][w], vw[1][w], sel0)),
+                                     e4m3x2_to_f16x2(__byte_perm(vw[0][w], vw[1][w], sel1)),
+                                     e4m3x2_to_f16x2(__byte_perm(vw[2][w], vw[3][w], sel0)),
+                                     e4m3x2_to_f16x2(__byte_perm(vw[2][w], vw[3][w], sel1))};
+              mma_f16(o[mt], a, pb0, pb1);
+            }
+          } else {
+            // V^T fragments by transposed ldmatrix: (keys 0-7 | 8-15) x (dims 0-7 | 8-15)
+            const uint32_t vt = st + C::kTileBytes;
+#pragma unroll
+            for (int mt = 0; mt < C::kKSteps; ++mt) {
+              uint32_t a[4];
+              ldsm_x4_t(vt + swz<C::kRowBytes>((lane & 7) + (lane >> 4) * 8, 2 * mt + ((lane >> 3) & 1)),
+                        a[0], a[1], a[2], a[3]);
+              mma_bf16(o[mt], a, pb0, pb1);
+            }
+          }
+          __syncwarp();
+          ++computed;
+        }
+        // the warp's state for this unit -> shared memory (real rows only); row
+        // sums over the 8 lanes (g) that share rows r0, r1
+#pragma unroll
+        for (int o8 = 4; o8 < 32; o8 <<= 1) {
+          l0 += __shfl_xor_sync(0xffffffffu, l0, o8);
+          l1 += __shfl_xor_sync(0xffffffffu, l1, o8);
+        }
+        float* cb = comb + (k & 1) * NW * R * D;
+        float* cm = comb_ml + (k & 1) * NW * R * 2;
+#pragma unroll
+        for (int mt = 0; mt < C::kKSteps; ++mt)
+#pragma unroll
+          for (int hv = 0; hv < 2; ++hv) {
+            const int dim = F8 ? (D / 8) * g + 2 * mt + hv : 16 * mt + g + 8 * hv;
+            if (r0 < R) cb[(warp * R + r0) * D + dim] = o[mt][2 * hv];
+            if (r1 < R) cb[(warp * R + r1) * D + dim] = o[mt][2 * hv + 1];
+          }
+        if (g == 0) {
+          if (r0 < R) {
+            cm[(warp * R + r0) * 2] = m0;
+            cm[(warp * R + r0) * 2 + 1] = l0;
+          }
+          if (r1 < R) {
+            cm[(warp * R + r1) * 2] = m1;
+            cm[(warp * R + r1) * 2 + 1] = l1;
+          }
+        }
+      } else {
       // q fragments (A operand, rows x D) for this unit
       uint32_t qa[C::kKSteps][4];
       {
@@ -802,6 +1005,7 @@ __global__ void __launch_bounds__(MmaCfg<D, G, P, NW, NS, F8>::kThreads,
           }
         }
       }
+      }  // rows-as-M tile
     }
     __syncthreads();
   }
@@ -814,21 +1018,21 @@ __global__ void __launch_bounds__(MmaCfg<D, G, P, NW, NS, F8>::kThreads,
 
 // Launches the kernel, or with grid_only set only stores the grid size it
 // would use (CTAs per SM by occupancy x SMs).
-template <int D, int G, int P, int NW, int NS, bool F8 = false>
+template <int D, int G, int P, int NW, int NS, bool F8 = false, bool SW = false>
 cudaError_t launch_mma(const AttnParams& p, int num_sms, cudaStream_t stream,
                        int* grid_only = nullptr) {
-  using C = MmaCfg<D, G, P, NW, NS, F8>;
+  using C = MmaCfg<D, G, P, NW, NS, F8, SW>;
   static int ctas_per_sm[64] = {0};
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
   if (ctas_per_sm[dev] == 0) {
-    e = cudaFuncSetAttribute(attn_mma_kernel<D, G, P, NW, NS, F8>,
+    e = cudaFuncSetAttribute(attn_mma_kernel<D, G, P, NW, NS, F8, SW>,
                              cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
     if (e != cudaSuccess) return e;
     int n = 0;
-    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, attn_mma_kernel<D, G, P, NW, NS, F8>,
+    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, attn_mma_kernel<D, G, P, NW, NS, F8, SW>,
                                                       C::kThreads, C::kSmemBytes);
     if (e != cudaSuccess) return e;
     ctas_per_sm[dev] = n > 0 ? n : 1;
@@ -849,7 +1053,7 @@ cudaError_t launch_mma(const AttnParams& p, int num_sms, cudaStream_t stream,
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = p.after_plan ? 1 : 0;
-  return cudaLaunchKernelEx(&cfg, attn_mma_kernel<D, G, P, NW, NS, F8>, p);
+  return cudaLaunchKernelEx(&cfg, attn_mma_kernel<D, G, P, NW, NS, F8, SW>, p);
 }
 
 }  // namespace pa

@@ -140,12 +140,14 @@ cudaError_t launch_prefill_tc(const AttnParams& p, int head_size, int group, int
                               bool fp8_cache, cudaStream_t stream);
 // Split-KV attention over the decode or few-token list, by element type:
 // bf16 runs the warp-level tensor-core (mma.sync) kernel, fp32 the CUDA-core
-// kernel.  positions: 1 (decode list) or the few-token tile height.  With
+// kernel.  positions: 1 (decode list) or the few-token tile height.
+// keys_as_m (bf16 decode tiles): the keys are the MMA's M dimension and the
+// query rows its N, instead of the query rows padded to 16 as M.  With
 // grid_only set nothing is launched: the grid size (CTAs) the launch would
 // use is stored there.  Returns cudaErrorInvalidValue for an unbuilt
 // combination.
 cudaError_t launch_attn_by_dtype(const AttnParams& p, pa_dtype dtype, int head_size, int group,
-                                 int positions, int num_sms, cudaStream_t stream,
+                                 int positions, bool keys_as_m, int num_sms, cudaStream_t stream,
                                  int* grid_only = nullptr);
 // bf16 q/out over an FP8 (E4M3) cache (tensor-core decode and few-token tiles).
 cudaError_t launch_attn_fp8(const AttnParams& p, int head_size, int group, int positions,
