@@ -122,11 +122,20 @@ Capacity capacity(const pa_layout* L, int B, int T, int max_seq_len) {
   const long long group = L->num_q_heads / L->num_kv_heads;
   c.prefill_tiles = L->dtype == PA_BF16
                         ? cdiv(static_cast<long long>(T) * group, kPrefillRows) + multi : 0;
-  // a step that can hold a chunk of kPrefillMinQlen tokens may split its
-  // prefill query tiles' KV
-  c.prefill_slots = (c.prefill_tiles > 0 && T - B >= kPrefillMinQlen - 1)
-                        ? cdiv(kPrefillSplitUnits, L->num_kv_heads) : 0;
-  c.prefill_items = c.prefill_tiles + c.prefill_slots;
+  // a step that can hold a chunk of kPrefillMinQlen tokens may cut prefill
+  // units: at chunk boundaries (a unit with k cuts has k + 1 <= 2k pieces, and
+  // a step has fewer chunks than kPrefillMaxChunks and than its longest
+  // possible unit line over the shortest chunk, unit cost + two min pieces),
+  // or, when units are scarce, into pieces the plan keeps within these slots
+  c.prefill_pieces = c.prefill_tiles * L->num_kv_heads;
+  if (c.prefill_tiles > 0 && T - B >= kPrefillMinQlen - 1) {
+    const long long line = c.prefill_tiles * L->num_kv_heads *
+                           (cdiv(max_seq_len, kPrefillKeys) + kPrefillUnitCost);
+    long long chunks = cdiv(line, kPrefillUnitCost + 2 * kMinPrefillSplitTiles);
+    if (chunks > kPrefillMaxChunks) chunks = kPrefillMaxChunks;
+    c.prefill_slots = 2 * chunks;
+    c.prefill_pieces += c.prefill_slots;
+  }
   return c;
 }
 
@@ -191,7 +200,9 @@ WsLayout ws_layout(const Capacity& cap, int Hkv, int D, int group) {
   w.tiles_d = take(sizeof(int4) * cap.decode_tiles);
   w.items_s = take(sizeof(int4) * cap.small_items);
   w.tiles_s = take(sizeof(int4) * cap.small_tiles);
-  w.items_p = take(sizeof(PfItem) * cap.prefill_items);
+  w.tiles_p = take(sizeof(PfTile) * cap.prefill_tiles);
+  w.items_p = take(sizeof(PfItem) * cap.prefill_pieces);
+  w.starts_p = take(cap.prefill_tiles > 0 ? sizeof(int) * (kPrefillMaxChunks + 1) : 0);
   w.cnt_p = take(sizeof(int) * cap.prefill_tiles * Hkv);
   w.recs_d = take(sizeof(UnitRec) * cap.decode_items);
   w.recs_s = take(sizeof(UnitRec) * cap.small_items);
@@ -202,8 +213,8 @@ WsLayout ws_layout(const Capacity& cap, int Hkv, int D, int group) {
   w.part_ml_d = take(sizeof(float) * cap.decode_items * Hkv * rows_d * 2);
   w.part_acc_s = take(sizeof(float) * cap.small_items * Hkv * rows_s * D);
   w.part_ml_s = take(sizeof(float) * cap.small_items * Hkv * rows_s * 2);
-  w.part_acc_p = take(sizeof(float) * cap.prefill_slots * Hkv * kPrefillRows * D);
-  w.part_ml_p = take(sizeof(float) * cap.prefill_slots * Hkv * kPrefillRows * 2);
+  w.part_acc_p = take(sizeof(float) * cap.prefill_slots * kPrefillRows * D);
+  w.part_ml_p = take(sizeof(float) * cap.prefill_slots * kPrefillRows * 2);
   w.total = off;
   return w;
 }
@@ -391,7 +402,8 @@ int pa_forward(const void* q, const void* k_cache, const void* v_cache,
     pf.next = hdr + kHdrPrefillNext;
     pf.items = reinterpret_cast<const int4*>(ws + lay.items_p);  // PfItem pairs
     pf.recs = nullptr;
-    pf.tiles = nullptr;
+    pf.tiles = reinterpret_cast<const int4*>(ws + lay.tiles_p);  // PfTile
+    pf.order = reinterpret_cast<const int*>(ws + lay.starts_p);  // chunk starts
     pf.merge_cnt = reinterpret_cast<int*>(ws + lay.cnt_p);
     pf.part_acc = reinterpret_cast<float*>(ws + lay.part_acc_p);
     pf.part_ml = reinterpret_cast<float*>(ws + lay.part_ml_p);

@@ -17,9 +17,18 @@ constexpr int kPrefillMinQlen = 16;   // bf16 chunks at least this long use the 
 constexpr int kSmallStepUnits = 2048; // extra decode units (items x kv heads) a workspace holds
                                       // for the finer splits of small steps
 constexpr int kPrefillKeys = 128;     // keys per KV tile of the tensor-core prefill kernel
-constexpr int kMinPrefillSplitTiles = 4;  // smallest KV piece of a split prefill query tile
-constexpr int kPrefillSplitUnits = 256;   // split prefill units (items x kv heads) a workspace
-                                          // holds partial states for
+// Tensor-core prefill scheduling (see the plan kernel).  A unit is (query tile,
+// kv head); its KV tiles may be cut into pieces, each at least
+// kMinPrefillSplitTiles tiles, whose partial softmax states the last piece
+// merges.  Steps with long units and a few of them per SM are cut by a line
+// of units into at most kPrefillMaxChunks equal chunks, a unit taking its KV
+// tiles plus kPrefillUnitCost (its fixed cost: Q load, first copies,
+// epilogue) on the line.
+constexpr int kMinPrefillSplitTiles = 4;
+constexpr int kPrefillUnitCost = 4;
+constexpr int kPrefillMaxChunks = 320;
+constexpr int kPrefillChunkMinTiles = 24;  // chunked when units average at least this many tiles
+constexpr int kPrefillChunkMaxWaves = 6;   // ... and number at most this many per SM
 
 // Work-list classes written by the plan kernel.
 enum ReqClass : int { kClassNone = 0, kClassDecode = 1, kClassSmall = 2, kClassPrefill = 3 };
@@ -28,7 +37,8 @@ enum ReqClass : int { kClassNone = 0, kClassDecode = 1, kClassSmall = 2, kClassP
 enum Hdr : int {
   kHdrDecodeItems = 0, kHdrDecodeTiles, kHdrDecodeNext,
   kHdrSmallItems, kHdrSmallTiles, kHdrSmallNext,
-  kHdrPrefillItems, kHdrPrefillNext,
+  kHdrPrefillItems, kHdrPrefillNext,       // prefill query tiles; chunk counter
+  kHdrPrefillChunks, kHdrPrefillChunked,   // chunks; 1: chunk starts listed, 0: a piece each
   kHdrWords = 16
 };
 
@@ -36,16 +46,17 @@ enum Hdr : int {
 struct Capacity {
   long long decode_items, decode_tiles;
   long long small_items, small_tiles;
-  long long prefill_tiles;  // query tiles of 128 rows
-  long long prefill_items;  // query tiles or pieces of their KV
-  long long prefill_slots;  // pieces with a partial state (query tiles split in several)
+  long long prefill_tiles;   // query tiles of 128 rows
+  long long prefill_pieces;  // units or pieces of their KV
+  long long prefill_slots;   // pieces with a partial state (of units cut in several)
 };
 
 // Byte offsets of every workspace region (all 256-byte aligned).
 struct WsLayout {
   size_t hdr;
   size_t items_d, tiles_d, items_s, tiles_s;
-  size_t items_p, cnt_p, part_acc_p, part_ml_p;  // prefill items, merge counters, partials
+  size_t tiles_p, items_p, starts_p;  // prefill query tiles, pieces, chunk starts
+  size_t cnt_p, part_acc_p, part_ml_p;  // prefill merge counters, partial states
   size_t recs_d, recs_s;  // per item: 3 x int4 unit records (see UnitRec)
   size_t order_d;         // decode items in dispatch order (largest split first)
   size_t cnt_d, cnt_s;
@@ -82,11 +93,18 @@ struct UnitRec {
   int4 a, b, c;
 };
 
-// One unit of tensor-core prefill work (x num_kv_heads):
-//   a = {r, query tile m of the request, first KV tile, one past the last KV tile}
-//   b = {query tile index in the step, piece index sp, pieces of the tile ns,
-//        first partial-state slot of the tile (-1 when ns = 1: the piece
-//        writes the output); piece sp uses slot b.w + sp}
+// A tensor-core prefill query tile of the step, in request order then query
+// tile m: {r, m, KV tiles its rows see (nkv), line position of its kv-head-0
+// unit}.  Its unit for kv head g spans line positions [x + g * len,
+// x + (g + 1) * len), len = nkv + kPrefillUnitCost.
+struct PfTile {
+  int r, m, nkv, x;
+};
+
+// One piece of tensor-core prefill work: a = {query tile q, kv head g, first
+// KV tile, one past the last KV tile}; b = {piece index, pieces of the unit,
+// partial-state slot of piece 0 (-1 for a whole unit: it writes the output),
+// 0}.  Piece k uses slot b.z + k.
 struct PfItem {
   int4 a, b;
 };
@@ -112,6 +130,7 @@ struct AttnParams {
   const UnitRec* recs;   // per item, the same fully decoded
   const int* order;      // dispatch order: the k-th item fetched is order[k] (null: k)
   const int4* tiles;     // {first item, number of splits, KV blocks per split, 0}
+                         // (prefill: the query tiles, PfTile)
   int* merge_cnt;        // [tiles][num_kv_heads]
   float* part_acc;       // [items][num_kv_heads][rows][D]
   float* part_ml;        // [items][num_kv_heads][rows][2]

@@ -16,6 +16,23 @@
 // (short items among them would only add their fixed cost late), then the
 // shorter ones largest first (a counting sort by blocks), so the last units
 // the CTAs pick up are short and the step ends evenly.
+//
+// Tensor-core prefill units (query tile x kv head) are scheduled one of three
+// ways, by what the step holds (each measured best for its kind of step):
+//   * fewer units than SMs (a short chunk after a long prompt): each unit's
+//     KV is cut into pieces sized for one round, one piece per SM;
+//   * long units, a few per SM (a long chunk): McNaughton's wrap-around rule
+//     for identical machines with preemption -- the units are laid end to
+//     end on a line (each its KV tiles plus a fixed cost), the line is cut
+//     into equal chunks, one per SM, and a unit a cut falls inside becomes
+//     pieces (a cut that would leave a piece under kMinPrefillSplitTiles KV
+//     tiles moves to the unit's edge), so every CTA streams the same number
+//     of KV tiles instead of some SMs running one unit more than the rest;
+//   * otherwise whole units, handed out last first (within a chunk later
+//     query tiles see more keys, and later chunks carry more prior context),
+//     whose dynamic fetch already evens out many short units.
+// The pieces of a cut unit keep partial softmax states that the last one to
+// finish merges.
 #include <climits>
 
 #include "pa_device.cuh"
@@ -38,9 +55,10 @@ constexpr int kShortItems = 2048;  // short decode items listed in shared memory
 #define PA_SPLIT_MIN 16  // smallest decode split (blocks)
 #endif
 
-// decode items, decode tiles, small items, small tiles, prefill items, long decode items,
-// prefill query tiles, prefill partial slots
+// decode items, decode tiles, small items, small tiles, prefill line length, long decode
+// items, prefill query tiles, (unused)
 constexpr int kLists = 8;
+
 
 // Exclusive scan of kLists ints per thread across the CTA, all lists at once;
 // `total` receives each list's CTA total.
@@ -106,8 +124,6 @@ __global__ void __launch_bounds__(kPlanThreads, 1) plan_kernel(PlanParams p) {
   __shared__ int size_hist[kMaxUnitBlocks + 1];  // short decode items per size (blocks)
   __shared__ unsigned long long s_blocks;        // KV blocks of the requests that split
   __shared__ unsigned long long s_blocks_d;      // ... of the decode requests among them
-  __shared__ unsigned long long s_pf_tiles;      // prefill query tiles of the step
-  __shared__ unsigned long long s_pf_kv;         // KV tiles those query tiles see, summed
   __shared__ int2 s_short[kShortItems];          // short decode items: (item, blocks)
   __shared__ int s_nshort;
   static_assert(kMaxUnitBlocks == 8 * 32, "the dispatch-order scan gives each lane 8 sizes");
@@ -132,7 +148,9 @@ __global__ void __launch_bounds__(kPlanThreads, 1) plan_kernel(PlanParams p) {
   UnitRec* recs_s = reinterpret_cast<UnitRec*>(ws + p.lay.recs_s);
   int* cnt_d = reinterpret_cast<int*>(ws + p.lay.cnt_d);
   int* cnt_s = reinterpret_cast<int*>(ws + p.lay.cnt_s);
+  PfTile* tiles_p = reinterpret_cast<PfTile*>(ws + p.lay.tiles_p);
   PfItem* items_p = reinterpret_cast<PfItem*>(ws + p.lay.items_p);
+  int* starts_p = reinterpret_cast<int*>(ws + p.lay.starts_p);
   int* cnt_p = reinterpret_cast<int*>(ws + p.lay.cnt_p);
   int* order_d = reinterpret_cast<int*>(ws + p.lay.order_d);
 
@@ -141,8 +159,6 @@ __global__ void __launch_bounds__(kPlanThreads, 1) plan_kernel(PlanParams p) {
     err = 0;
     s_blocks = 0;
     s_blocks_d = 0;
-    s_pf_tiles = 0;
-    s_pf_kv = 0;
     s_nshort = 0;
     for (int i = 0; i < kLists; ++i) carry[i] = 0;
   }
@@ -154,8 +170,7 @@ __global__ void __launch_bounds__(kPlanThreads, 1) plan_kernel(PlanParams p) {
   // there are enough of them), up to kMaxUnitBlocks.
   // Out-of-range lengths are left out here (they are flagged below).
   {
-    unsigned long long mine = 0, mine_d = 0, pf_tiles = 0, pf_kv = 0;
-    const int pm = p.prefill_rows / p.group;  // positions per prefill query tile
+    unsigned long long mine = 0, mine_d = 0;
     for (int r = threadIdx.x; r < B; r += kPlanThreads) {
       const int S = __ldg(p.seq_lens + r);
       const int qa = __ldg(p.qsl + r), qb = __ldg(p.qsl + r + 1);
@@ -166,24 +181,15 @@ __global__ void __launch_bounds__(kPlanThreads, 1) plan_kernel(PlanParams p) {
       if (L < p.prefill_min_qlen) {
         mine += static_cast<unsigned long long>(ceil_div(S, kBlockSize));
         if (L == 1) mine_d += static_cast<unsigned long long>(ceil_div(S, kBlockSize));
-      } else if (L <= p.max_query_len) {
-        const int nt = ceil_div(L, pm);
-        pf_tiles += nt;
-        for (int m = 0; m < nt; ++m)
-          pf_kv += static_cast<unsigned long long>(ceil_div(S - L + min(L, (m + 1) * pm), kPrefillKeys));
       }
     }
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) {
       mine += __shfl_down_sync(0xffffffffu, mine, o);
       mine_d += __shfl_down_sync(0xffffffffu, mine_d, o);
-      pf_tiles += __shfl_down_sync(0xffffffffu, pf_tiles, o);
-      pf_kv += __shfl_down_sync(0xffffffffu, pf_kv, o);
     }
     if ((threadIdx.x & 31) == 0 && mine) atomicAdd(&s_blocks, mine);
     if ((threadIdx.x & 31) == 0 && mine_d) atomicAdd(&s_blocks_d, mine_d);
-    if ((threadIdx.x & 31) == 0 && pf_tiles) atomicAdd(&s_pf_tiles, pf_tiles);
-    if ((threadIdx.x & 31) == 0 && pf_kv) atomicAdd(&s_pf_kv, pf_kv);
   }
   __syncthreads();
   const int num_ctas = max(1, p.num_ctas);
@@ -207,31 +213,6 @@ __global__ void __launch_bounds__(kPlanThreads, 1) plan_kernel(PlanParams p) {
                                        : static_cast<long long>(p.bps);
       bps_d = static_cast<int>(min(static_cast<long long>(p.bps),
                                    max(max(want, need), static_cast<long long>(PA_SPLIT_MIN))));
-    }
-  }
-
-  // KV tiles per prefill unit.  With fewer prefill units (query tiles x kv
-  // heads) than SMs, a unit streams all the KV its rows see and most SMs idle
-  // (a short chunk after a long prompt: every later chunk reads all earlier
-  // ones from the cache), so each query tile's KV is split into pieces sized
-  // for one piece per SM, at least kMinPrefillSplitTiles, whose partial
-  // softmax states the last piece merges.  Pieces with a partial state must
-  // fit the capacity: they number at most query tiles + KV tiles / split (and
-  // the items then fit as well).
-  int tps = INT_MAX;
-  {
-    const long long nt = static_cast<long long>(s_pf_tiles);
-    const long long units = nt * p.num_kv_heads;
-    const long long room = p.cap.prefill_slots - nt;
-    if (units > 0 && units < p.num_sms && room > 0) {
-      // pieces x heads <= units + kv x heads / tps <= num_sms: one round of
-      // pieces, every SM streaming at most one
-      const long long kv = static_cast<long long>(s_pf_kv);
-      const long long spare = p.num_sms - units;
-      const long long want = (kv * p.num_kv_heads + spare - 1) / spare;
-      const long long need = (kv + room - 1) / room;
-      tps = static_cast<int>(min(static_cast<long long>(INT_MAX),
-                                 max(max(want, need), static_cast<long long>(kMinPrefillSplitTiles))));
     }
   }
 
@@ -267,12 +248,10 @@ __global__ void __launch_bounds__(kPlanThreads, 1) plan_kernel(PlanParams p) {
         c = kClassPrefill;
         const int pm = p.prefill_rows / p.group;
         cnt[6] = ceil_div(L, pm);
-        for (int m = 0; m < cnt[6]; ++m) {
-          const int nkv = ceil_div(S - L + min(L, (m + 1) * pm), kPrefillKeys);
-          const int ns = nkv > tps ? ceil_div(nkv, tps) : 1;
-          cnt[4] += ns;
-          if (ns > 1) cnt[7] += ns;
-        }
+        // line length of the request's units (query tiles x kv heads)
+        for (int m = 0; m < cnt[6]; ++m)
+          cnt[4] += ceil_div(S - L + min(L, (m + 1) * pm), kPrefillKeys) + kPrefillUnitCost;
+        cnt[4] *= p.num_kv_heads;
       } else {
         c = kClassSmall;
         cnt[3] = ceil_div(L, p.small_positions);
@@ -337,22 +316,14 @@ __global__ void __launch_bounds__(kPlanThreads, 1) plan_kernel(PlanParams p) {
       }
     } else if (c == kClassPrefill) {
       // tensor-core query tiles of prefill_rows rows (positions x grouped
-      // heads), each as one item or as pieces of its KV tiles
+      // heads), laid on the line from the request's offset
       const int pm = p.prefill_rows / p.group;
-      int item = off[4], slot = off[7];
+      int x = off[4];
       for (int m = 0; m < cnt[6]; ++m) {
-        const int tile = off[6] + m;
+        const int q = off[6] + m;
         const int nkv = ceil_div(S - L + min(L, (m + 1) * pm), kPrefillKeys);
-        const int ns = nkv > tps ? ceil_div(nkv, tps) : 1;
-        const int per = ceil_div(nkv, ns);
-        for (int sp = 0; sp < ns; ++sp, ++item) {
-          if (item >= p.cap.prefill_items) break;
-          PfItem it;
-          it.a = make_int4(r, m, sp * per, min(nkv, (sp + 1) * per));
-          it.b = make_int4(tile, sp, ns, ns > 1 ? slot : -1);
-          items_p[item] = it;
-        }
-        if (ns > 1) slot += ns;
+        if (q < p.cap.prefill_tiles) tiles_p[q] = PfTile{r, m, nkv, x};
+        x += (nkv + kPrefillUnitCost) * p.num_kv_heads;
       }
     }
 #pragma unroll
@@ -366,8 +337,7 @@ __global__ void __launch_bounds__(kPlanThreads, 1) plan_kernel(PlanParams p) {
   if (threadIdx.x == 0) {
     if (carry[0] > p.cap.decode_items || carry[1] > p.cap.decode_tiles ||
         carry[2] > p.cap.small_items || carry[3] > p.cap.small_tiles ||
-        carry[4] > p.cap.prefill_items || carry[6] > p.cap.prefill_tiles ||
-        carry[7] > p.cap.prefill_slots)
+        carry[6] > p.cap.prefill_tiles)
       err |= PA_DEV_CAPACITY;
   }
   __syncthreads();
@@ -381,7 +351,113 @@ __global__ void __launch_bounds__(kPlanThreads, 1) plan_kernel(PlanParams p) {
     return;
   }
   const int n_di = carry[0], n_dt = carry[1], n_si = carry[2], n_st = carry[3];
-  const int n_pi = carry[4], n_pt = carry[6];
+  const int n_pt = carry[6];
+
+  // Prefill pieces (see the file comment), one thread per unit u = q x Hkv + g.
+  const int Hkv = p.num_kv_heads;
+  const int line = carry[4];
+  const int n_units = n_pt * Hkv;
+  const int kv_tiles = line / Hkv - kPrefillUnitCost * n_pt;  // KV tiles of all query tiles
+  const int P = max(1, p.num_sms);
+  bool chunked = false;
+  int tps = INT_MAX, n_ch = 0, clen = 1;
+  if (n_units > 0 && n_units < P) {
+    // one round: pieces x heads <= units + KV tiles x heads / tps <= SMs, and
+    // the pieces with a partial state (<= that sum) within the slots
+    const long long kvh = static_cast<long long>(kv_tiles) * Hkv;
+    const long long room = p.cap.prefill_slots - n_units;
+    if (room > 0) {
+      const long long want = (kvh + (P - n_units) - 1) / (P - n_units);
+      const long long need = (kvh + room - 1) / room;
+      tps = static_cast<int>(min(static_cast<long long>(INT_MAX),
+                                 max(max(want, need), static_cast<long long>(kMinPrefillSplitTiles))));
+    }
+  } else if (n_units >= P && n_units <= kPrefillChunkMaxWaves * P &&
+             kv_tiles >= kPrefillChunkMinTiles * n_pt && p.cap.prefill_slots >= 2) {
+    // chunks of clen line positions, clen >= the unit cost + two minimum
+    // pieces, so the cut-or-snap rule keeps chunk starts in order; fewer than
+    // half the slots, since the pieces of cut units number at most 2 x cuts
+    chunked = true;
+    const int want = static_cast<int>(min(static_cast<long long>(min(kPrefillMaxChunks, P)),
+                                          p.cap.prefill_slots / 2));
+    clen = max(ceil_div(line, want), kPrefillUnitCost + 2 * kMinPrefillSplitTiles);
+    n_ch = ceil_div(line, clen);
+  }
+  int n_rec = 0, n_slot = 0;
+  for (int base = 0; base < n_units; base += kPlanThreads) {
+    const int u = base + threadIdx.x;
+    int v[kLists] = {0, 0, 0, 0, 0, 0, 0, 0}, tot[kLists];
+    PfTile t{0, 0, 0, 0};
+    int g = 0, s0 = 0, e0 = 0, c0 = 0, nrec = 0;
+    if (u < n_units) {
+      t = tiles_p[u / Hkv];  // written above by this CTA
+      g = u % Hkv;
+      s0 = t.x + g * (t.nkv + kPrefillUnitCost);
+      e0 = s0 + t.nkv + kPrefillUnitCost;
+      if (chunked) {
+        // cuts: the chunk starts c x clen in [s0 + cost + min piece, e0 - min piece]
+        c0 = ceil_div(s0 + kPrefillUnitCost + kMinPrefillSplitTiles, clen);
+        nrec = max(0, (e0 - kMinPrefillSplitTiles) / clen - c0 + 1) + 1;
+      } else {
+        nrec = t.nkv > tps ? ceil_div(t.nkv, tps) : 1;
+      }
+      v[0] = nrec;
+      v[1] = nrec > 1 ? nrec : 0;
+    }
+    block_exclusive_scan(v, warp_sums, tot);
+    if (u < n_units) {
+      const int rec0 = n_rec + v[0];
+      const int slot0 = nrec > 1 ? n_slot + v[1] : -1;
+      const int per = ceil_div(t.nkv, nrec);
+      for (int k = 0; k < nrec; ++k) {
+        int kt0, kt1;
+        if (chunked) {
+          kt0 = k == 0 ? 0 : (c0 + k - 1) * clen - s0 - kPrefillUnitCost;
+          kt1 = k == nrec - 1 ? t.nkv : (c0 + k) * clen - s0 - kPrefillUnitCost;
+        } else {
+          kt0 = k * per;
+          kt1 = min(t.nkv, (k + 1) * per);
+        }
+        // whole units are handed out last first
+        const int idx = (!chunked && tps == INT_MAX) ? n_units - 1 - u : rec0 + k;
+        if (idx < p.cap.prefill_pieces) {
+          PfItem it;
+          it.a = make_int4(u / Hkv, g, kt0, kt1);
+          it.b = make_int4(k, nrec, slot0, 0);
+          items_p[idx] = it;
+        }
+      }
+      if (chunked) {
+        // the chunk starts falling in this unit: cut, or moved to an edge
+        for (int c = max(1, ceil_div(s0, clen)); c < n_ch && c * clen < e0; ++c) {
+          const int b = c * clen;
+          starts_p[c] = b - s0 < kPrefillUnitCost + kMinPrefillSplitTiles ? rec0
+                        : e0 - b < kMinPrefillSplitTiles                 ? rec0 + nrec
+                                                                         : rec0 + c - c0 + 1;
+        }
+      }
+    }
+    n_rec += tot[0];
+    n_slot += tot[1];
+  }
+  if (threadIdx.x == 0) {
+    if (chunked) {
+      starts_p[0] = 0;
+      starts_p[n_ch] = n_rec;
+    } else {
+      n_ch = n_rec;
+    }
+    if (n_rec > p.cap.prefill_pieces || n_slot > p.cap.prefill_slots) err |= PA_DEV_CAPACITY;
+  }
+  __syncthreads();
+  if (err & PA_DEV_CAPACITY) {
+    if (threadIdx.x == 0) {
+      for (int i = 0; i < kHdrWords; ++i) hdr[i] = 0;
+      flag_error(p.status, err);
+    }
+    wait_prior_grid();
+    return;
+  }
   // dispatch order (it does not change results: partial states are stored
   // and merged by item, in split order).  The long items took the first
   // n_long slots above; short items: exclusive scan of the size histogram
@@ -431,8 +507,10 @@ __global__ void __launch_bounds__(kPlanThreads, 1) plan_kernel(PlanParams p) {
     hdr[kHdrSmallItems] = n_si;
     hdr[kHdrSmallTiles] = n_st;
     hdr[kHdrSmallNext] = 0;
-    hdr[kHdrPrefillItems] = n_pi;
+    hdr[kHdrPrefillItems] = n_pt;
     hdr[kHdrPrefillNext] = 0;
+    hdr[kHdrPrefillChunks] = n_ch;
+    hdr[kHdrPrefillChunked] = chunked ? 1 : 0;
     if (err) flag_error(p.status, err);
   }
   wait_prior_grid();

@@ -71,12 +71,22 @@ struct PfCfg {
   static constexpr int kVBlockBytes = kBlockSize * 128 * (D / 64);
   static constexpr int kKGroupBytes = 8 * 128 * (D / 64);
   static constexpr int kSmemBytes = kVOff + 2 * kTileBytes + 1024;  // + alignment slack
+  // FP8 cache: a tile's codes are staged by TMA, [block][16 rows][D bytes],
+  // and widened from there into the K / V buffers above: two staging buffers
+  // for K, one for V at D = 128 (two at D = 64), so the copies run ahead
+  static constexpr int kCodeBytes = kTileN * D;
+  static constexpr int kVStages = D == 64 ? 2 : 1;
+  static constexpr int kKCodeOff = kVOff + 2 * kTileBytes;
+  static constexpr int kVCodeOff = kKCodeOff + 2 * kCodeBytes;
+  static constexpr int kSmemBytesF8 = kVCodeOff + kVStages * kCodeBytes + 1024;
   // S0, S1 (consecutive tiles) at 0 / 128, each tile's P (bf16 pairs) over the
   // first 64 columns of its S once read; O at 256
   static constexpr int kTmemCols = 512;
   static_assert(D == 64 || D == 128, "head size 64 or 128");
   static_assert(kTileN == kTileM, "K and V tiles share the Q tile geometry");
   static_assert(kSmemBytes <= 227 * 1024, "shared memory per CTA exceeds 227 KB");
+  // (4 KB: the kernel's static shared memory)
+  static_assert(kSmemBytesF8 + 4096 <= 227 * 1024, "shared memory per CTA exceeds 227 KB");
 };
 
 // mbarriers.  [2] = one per buffer parity (tile t uses buffers t & 1 of S,
@@ -92,7 +102,8 @@ enum Bar : int {
   kSFull = 8,       // [2] S = Q K^T done (MMA commit); also frees the K buffer
   kGo = 10,         // [2] tile t: P written and S read (8 softmax warps), V of t landed
                     //     (V loader), K of t + 2 landed or none due (K loader)
-  kVLand = 12,      // [2] V tile landed, for a tile whose last block the V loader trims
+  kVLand = 12,      // [2] V tile landed, for a tile whose last block the V loader trims;
+                    //     FP8 cache: codes landed in V staging buffer 0 / 1
   kPVDone = 14,     // [2] O += P V done (MMA commit); frees the V buffer
   kMx = 16,         // [2] both halves of each row published their maximum (8 warps)
   kMlFull = 18,     // row sums of both halves published (8 warps)
@@ -102,7 +113,7 @@ enum Bar : int {
   kPieceDone = 22,  // a split piece's partial state stored (8 softmax warps)
   kPieceLast = 23,  // ... and whether it was the tile's last piece decided (warp 0)
   kQLand = 24,      // FP8 cache: the bf16 Q tile landed (TMA), before its f16 conversion
-  kKLand = 25,      // [2] FP8 cache: a K tile's codes landed (TMA), before widening
+  kKLand = 25,      // [2] FP8 cache: codes landed in K staging buffer 0 / 1 (TMA)
   kNumBars = 27
 };
 
@@ -110,7 +121,8 @@ struct UnitInfo {
   int r, g, a, j0, npos, pos0, kv_end, n_kv;  // r < 0: no more units
   int kt0;                                    // first KV tile (n_kv tiles from there)
   int rot;                                    // KV tile processed first (from kt0)
-  int ptile, piece, nsplit, slot0;            // split pieces of the query tile (PfItem::b)
+  int ptile;                                  // query tile index in the step
+  int piece, nsplit, slot0;                   // piece of the unit, pieces, slot of piece 0
 };
 
 // KV tile processed s-th in unit u (tiles are visited in rotated order).
@@ -226,11 +238,12 @@ __device__ __forceinline__ uint32_t e4m3x2_f16x2(uint32_t codes16) {
 
 }  // namespace
 
-// F8: the cache holds E4M3 codes.  They are copied by TMA into the upper half
-// of each K / V tile buffer and widened there to f16 (exactly) by the loader
-// warp, Q is converted from bf16 to f16 in place once per unit, and the two
-// products run as kind::f16 with f16 operands (P in f16).  The K scale is
-// folded into the softmax scale and the V scale into the normalisation.
+// F8: the cache holds E4M3 codes.  They are copied by TMA into staging
+// buffers, up to two tiles ahead, and widened from there to f16 (exactly) in
+// the K / V tile buffers by the loader warps; Q is converted from bf16 to f16
+// in place once per unit, and the two products run as kind::f16 with f16
+// operands (P in f16).  The K scale is folded into the softmax scale and the
+// V scale into the normalisation.
 template <int D, int G, bool F8>
 __global__ void __launch_bounds__(kPfThreads, 1)
     prefill_tc_kernel(const AttnParams p, const __grid_constant__ PfMaps maps) {
@@ -283,13 +296,13 @@ __global__ void __launch_bounds__(kPfThreads, 1)
       ph = -1;
     }
     if constexpr (F8) {
-      // the codes, [block][16 rows][D bytes], into the buffer's upper half
-      if (lane == 0) mbar_arrive_expect_tx(full, C::kTileBytes / 2);
+      // the codes, [block][16 rows][D bytes], into the staging buffer at dst
+      if (lane == 0) mbar_arrive_expect_tx(full, C::kCodeBytes);
       __syncwarp();
       if (lane < kTileN / kBlockSize) {
         const int coord = ph < 0 ? p.num_blocks : ph;
-        tma_load_3d(dst + C::kTileBytes / 2 + lane * kBlockSize * D, is_v ? &maps.v : &maps.k, 0,
-                    0, coord * kBlockSize * p.num_kv_heads + u.g, full);
+        tma_load_3d(dst + lane * kBlockSize * D, is_v ? &maps.v : &maps.k, 0, 0,
+                    coord * kBlockSize * p.num_kv_heads + u.g, full);
       }
       return;
     }
@@ -304,56 +317,75 @@ __global__ void __launch_bounds__(kPfThreads, 1)
                     coord * kBlockSize * p.num_kv_heads + u.g, full);
     }
   };
-  // FP8: widen the codes of a landed tile to f16 in the layout the bf16 TMA
-  // copy would have produced (K: [block][8-row group][64-column half][8 rows]
-  // [128 B]; V: [block][64-column half][16 rows][128 B]; 16-byte chunks
-  // XOR-swizzled by row), in place, block by block.  Block b's f16 rows cover
-  // the codes of blocks 2b - 8 and 2b - 7 only, each read at an earlier block
-  // except block 7's own codes, which the warp reads into registers before it
-  // writes.  Rows from tile row zero_from on are written as zeros.
-  auto widen_tile = [&](uint32_t buf, bool is_v, int zero_from) {
-    constexpr int kRowChunks = D / 16;                        // 16-code chunks per row
-    constexpr int kPerLane = kBlockSize * kRowChunks / 32;    // chunks per lane per block
-    const uint32_t codes = buf + C::kTileBytes / 2;
-#pragma unroll 1
-    for (int b = 0; b < kTileN / kBlockSize; ++b) {
-      uint4 cv[kPerLane];
-#pragma unroll
-      for (int j = 0; j < kPerLane; ++j)
-        asm volatile("ld.shared.v4.b32 {%0,%1,%2,%3}, [%4];\n"
-                     : "=r"(cv[j].x), "=r"(cv[j].y), "=r"(cv[j].z), "=r"(cv[j].w)
-                     : "r"(codes + b * kBlockSize * D + (lane + 32 * j) * 16)
-                     : "memory");
-      __syncwarp();
-#pragma unroll
-      for (int j = 0; j < kPerLane; ++j) {
-        const int q = lane + 32 * j;
-        const int t = q / kRowChunks, c0 = (q % kRowChunks) * 16;
-        const bool zero = b * kBlockSize + t >= zero_from;
-        const uint32_t wd[4] = {cv[j].x, cv[j].y, cv[j].z, cv[j].w};
-        uint32_t h[8];
-#pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          h[2 * e] = zero ? 0u : e4m3x2_f16x2(wd[e] & 0xffffu);
-          h[2 * e + 1] = zero ? 0u : e4m3x2_f16x2(wd[e] >> 16);
-        }
-#pragma unroll
-        for (int o = 0; o < 2; ++o) {
-          const int col = c0 + 8 * o, half = col >> 6, ch = (col & 63) >> 3;
-          const uint32_t sw = static_cast<uint32_t>((ch ^ (t & 7)) << 4);
-          const uint32_t addr =
-              is_v ? buf + b * C::kVBlockBytes + half * (kBlockSize * 128) + t * 128 + sw
-                   : buf + b * C::kVBlockBytes + (t >> 3) * C::kKGroupBytes + half * 1024 +
-                         (t & 7) * 128 + sw;
-          asm volatile("st.shared.v4.b32 [%0], {%1,%2,%3,%4};\n" ::"r"(addr), "r"(h[4 * o]),
-                       "r"(h[4 * o + 1]), "r"(h[4 * o + 2]), "r"(h[4 * o + 3])
-                       : "memory");
-        }
-      }
-      __syncwarp();
+  // Rows r0 .. r1 - 1 of the V tile buffer at vb to zeros (all D columns).
+  auto zero_v_rows = [&](uint32_t vb, int r0, int r1) {
+    constexpr int per_row = (D / 64) * 8;  // 16-byte chunks per row
+    for (int idx = lane; idx < (r1 - r0) * per_row; idx += 32) {
+      const int row = r0 + idx / per_row, c = idx % per_row;
+      asm volatile("st.shared.v4.b32 [%0], {%1,%1,%1,%1};\n" ::"r"(
+                       vb + (row >> 4) * C::kVBlockBytes + (c >> 3) * (kBlockSize * 128) +
+                       (row & 15) * 128 + (c & 7) * 16),
+                   "r"(0u)
+                   : "memory");
     }
-    fence_proxy_async_smem();  // the generic-proxy writes, before the tensor cores read them
-    __syncwarp();
+  };
+  // FP8: widen a staged tile of codes at src to f16 at dst, in the layout the
+  // bf16 TMA copy produces (K: [block][8-row group][64-column half][8 rows]
+  // [128 B]; V: [block][64-column half][16 rows][128 B]; 16-byte chunks
+  // XOR-swizzled by row).  A lane converts 16-code chunks (two 16-byte f16
+  // chunks); at D = 128 the lanes with the second column half take the
+  // neighbouring row (parity flipped), so each 8 lanes' loads and stores hit
+  // 8 distinct 16-byte bank groups.  Two blocks per step, for overlap.
+  auto widen_tile = [&](uint32_t src, uint32_t dst, bool is_v) {
+    constexpr int kRowChunks = D / 16;                 // 16-code chunks per row: 8 or 4
+    constexpr int kRowsPerStep = 32 / kRowChunks;      // rows a warp covers per step: 4 or 8
+    constexpr int kSteps = kBlockSize / kRowsPerStep;  // steps per block: 4 or 2
+    const int c = lane % kRowChunks;
+    const int rr = (lane / kRowChunks) ^ (D == 128 ? (c >> 2) & 1 : 0);
+    const int half = (c * 16) >> 6;
+    uint32_t soff[kSteps][2];  // store offsets within a block
+#pragma unroll
+    for (int j = 0; j < kSteps; ++j) {
+      const int t = j * kRowsPerStep + rr;
+#pragma unroll
+      for (int o = 0; o < 2; ++o) {
+        const int ch = (2 * c + o) & 7;
+        const uint32_t sw = static_cast<uint32_t>((ch ^ (t & 7)) << 4);
+        soff[j][o] = is_v ? half * (kBlockSize * 128) + t * 128 + sw
+                          : (t >> 3) * C::kKGroupBytes + half * 1024 + (t & 7) * 128 + sw;
+      }
+    }
+    const uint32_t lsrc = src + rr * D + c * 16;
+#pragma unroll 1
+    for (int b = 0; b < kTileN / kBlockSize; b += 2) {
+      uint4 cv[2][kSteps];
+#pragma unroll
+      for (int bb = 0; bb < 2; ++bb)
+#pragma unroll
+        for (int j = 0; j < kSteps; ++j)
+          asm volatile("ld.shared.v4.b32 {%0,%1,%2,%3}, [%4];\n"
+                       : "=r"(cv[bb][j].x), "=r"(cv[bb][j].y), "=r"(cv[bb][j].z), "=r"(cv[bb][j].w)
+                       : "r"(lsrc + (b + bb) * kBlockSize * D + j * kRowsPerStep * D)
+                       : "memory");
+#pragma unroll
+      for (int bb = 0; bb < 2; ++bb)
+#pragma unroll
+        for (int j = 0; j < kSteps; ++j) {
+          const uint32_t wd[4] = {cv[bb][j].x, cv[bb][j].y, cv[bb][j].z, cv[bb][j].w};
+          uint32_t h[8];
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            h[2 * e] = e4m3x2_f16x2(wd[e] & 0xffffu);
+            h[2 * e + 1] = e4m3x2_f16x2(wd[e] >> 16);
+          }
+          const uint32_t base = dst + (b + bb) * C::kVBlockBytes;
+#pragma unroll
+          for (int o = 0; o < 2; ++o)
+            asm volatile("st.shared.v4.b32 [%0], {%1,%2,%3,%4};\n" ::"r"(base + soff[j][o]),
+                         "r"(h[4 * o]), "r"(h[4 * o + 1]), "r"(h[4 * o + 2]), "r"(h[4 * o + 3])
+                         : "memory");
+        }
+    }
   };
   // FP8: the landed bf16 Q tile to f16, in place (an element keeps its slot)
   auto q_to_f16 = [&]() {
@@ -380,43 +412,67 @@ __global__ void __launch_bounds__(kPfThreads, 1)
 
   if (warp == kKLoadWarp) {
     // ------------------------------------------------------------ units, Q, K
-    const int Hkv = p.num_kv_heads;
-    const int n_units = __ldg(p.n_items) * Hkv;
+    // Work comes in chunks of pieces (PfItem), fetched from a counter: chunk
+    // c is pieces starts[c] .. starts[c + 1] - 1 when the plan cut the unit
+    // line into chunks, else piece c alone.  A chunk's last piece, when it is
+    // the first piece of a unit the next chunk continues, runs first, so that
+    // both pieces finish early and their merge is off the CTA's critical path.
+    const int n_chunks = __ldg(p.n_items + (kHdrPrefillChunks - kHdrPrefillItems));
+    const bool chunked = __ldg(p.n_items + (kHdrPrefillChunked - kHdrPrefillItems)) != 0;
+    const PfItem* pieces = reinterpret_cast<const PfItem*>(p.items);
+    const PfTile* qtiles = reinterpret_cast<const PfTile*>(p.tiles);
+    int ra = 0, rn = 0, rk = 0;  // the chunk's first piece, its pieces, pieces taken
+    bool last_first = false;
     // per buffer parity w: nf: first-K copies; sw: S phases waited; ga: kGo
     // arrivals (one per tile of that parity), gk: the last one that carried
     // a copy, plus one
     uint32_t nf[2] = {0, 0}, sw[2] = {0, 0}, ga[2] = {0, 0}, gk[2] = {0, 0}, nq = 0;
-    uint32_t nkl[2] = {0, 0};     // FP8: K code copies per buffer parity
-    bool kl_wait[2] = {false, false}, q_wait = false;  // FP8: copies not yet waited for
+    // FP8: code copies issued / waited (copy i: staging buffer i & 1, phase i >> 1)
+    uint32_t kc = 0, kw = 0;
+    bool q_wait = false;  // FP8: the Q copy not yet waited for
     for (int uc = 0;; ++uc) {
-      int unit = 0;
-      if (lane == 0) unit = atomicAdd(p.next, 1);
-      unit = __shfl_sync(0xffffffffu, unit, 0);
+      int pc = -1;
+      while (true) {
+        if (rk < rn) {
+          pc = last_first ? (rk == 0 ? ra + rn - 1 : ra + rk - 1) : ra + rk;
+          ++rk;
+          break;
+        }
+        int c = 0;
+        if (lane == 0) c = atomicAdd(p.next, 1);
+        c = __shfl_sync(0xffffffffu, c, 0);
+        if (c >= n_chunks) break;
+        ra = chunked ? __ldg(p.order + c) : c;
+        rn = (chunked ? __ldg(p.order + c + 1) : c + 1) - ra;
+        rk = 0;
+        last_first = false;
+        if (rn > 1) {
+          const int4 lb = __ldg(&pieces[ra + rn - 1].b);
+          last_first = lb.x == 0 && lb.y > 1;
+        }
+      }
       UnitInfo u;
       u.r = -1;
-      if (unit < n_units) {
-        // last item first: within a chunk later query tiles see more keys, and
-        // later chunks of the step carry more prior context
-        const PfItem* it = reinterpret_cast<const PfItem*>(p.items) +
-                           (__ldg(p.n_items) - 1 - unit / Hkv);
-        const int4 ta = __ldg(&it->a), tb = __ldg(&it->b);
-        const int S = __ldg(p.seq_lens + ta.x);
-        const int a = __ldg(p.qsl + ta.x);
-        const int L = __ldg(p.qsl + ta.x + 1) - a;
-        u.r = ta.x;
-        u.g = unit % Hkv;
+      if (pc >= 0) {
+        const int4 ta = __ldg(&pieces[pc].a), tb = __ldg(&pieces[pc].b);
+        const int4 qt = __ldg(reinterpret_cast<const int4*>(qtiles + ta.x));  // PfTile
+        const int S = __ldg(p.seq_lens + qt.x);
+        const int a = __ldg(p.qsl + qt.x);
+        const int L = __ldg(p.qsl + qt.x + 1) - a;
+        u.r = qt.x;
+        u.g = ta.y;
         u.a = a;
-        u.j0 = ta.y * PM;
+        u.j0 = qt.y * PM;
         u.npos = min(PM, L - u.j0);
         u.pos0 = S - L + u.j0;
         u.kt0 = ta.z;
         u.n_kv = ta.w - ta.z;
         u.kv_end = min(u.pos0 + u.npos, ta.w * kTileN);  // this piece's keys end here
-        u.rot = ta.y % u.n_kv;
-        u.ptile = tb.x;
-        u.piece = tb.y;
-        u.nsplit = tb.z;
-        u.slot0 = tb.w;
+        u.rot = qt.y % u.n_kv;
+        u.ptile = ta.x;
+        u.piece = tb.x;
+        u.nsplit = tb.y;
+        u.slot0 = tb.z;
       }
       const int slot = uc & 1;
       if (uc >= 2 && !wait_bar(bar(kUnitEmpty + slot), ((uc >> 1) - 1) & 1, abort, p.status)) break;
@@ -427,6 +483,18 @@ __global__ void __launch_bounds__(kPfThreads, 1)
       if (u.r < 0) break;
 
       int ph = tile_phys(u, tile_of(u, 0));
+      // FP8: the codes of the unit's first two tiles into the staging buffers
+      // (free: every copy issued before has been widened), ahead of Q
+      auto copy_codes = [&](int sq) {
+        copy_kv_tile(u, tile_of(u, sq), ph, false, sbase + C::kKCodeOff + (kc & 1) * C::kCodeBytes,
+                     bar(kKLand + (kc & 1)));
+        ++kc;
+        if (sq + 1 < u.n_kv) ph = tile_phys(u, tile_of(u, sq + 1));
+      };
+      if constexpr (F8) {
+        copy_codes(0);
+        if (u.n_kv > 1) copy_codes(1);
+      }
       // Q tile: rows (position, head) of 128/G tokens x G heads, one box per 64 columns
       if (uc > 0 && !wait_bar(bar(kQEmpty), (uc - 1) & 1, abort, p.status)) break;
       const uint32_t q_bar = F8 ? bar(kQLand) : bar(kQFull);
@@ -440,11 +508,20 @@ __global__ void __launch_bounds__(kPfThreads, 1)
       ++nq;
       q_wait = F8;
       bool ok = true;
+      if constexpr (F8) {  // Q to f16 while the codes are on their way
+        if (!wait_bar(bar(kQLand), (nq - 1) & 1, abort, p.status)) {
+          ok = false;
+        } else {
+          q_wait = false;
+          q_to_f16();
+          if (lane == 0) mbar_arrive(bar(kQFull));
+        }
+      }
       // K of tile sq goes into buffer w = sq & 1.  The first two were freed
       // by the previous unit (its last S of each parity was waited below);
       // later ones wait for S of tile sq - 2 and then count as that tile's
-      // kGo arrival (bytes included)
-      for (int sq = 0; sq < u.n_kv; ++sq) {
+      // kGo arrival (bytes included; FP8: a plain arrival after widening)
+      for (int sq = 0; ok && sq < u.n_kv; ++sq) {
         const int w = sq & 1;
         uint32_t full = bar(kKFirst + w);
         if (sq >= 2) {
@@ -457,20 +534,14 @@ __global__ void __launch_bounds__(kPfThreads, 1)
         }
         const uint32_t kbuf = sbase + C::kKOff + w * C::kTileBytes;
         if constexpr (F8) {
-          copy_kv_tile(u, tile_of(u, sq), ph, false, kbuf, bar(kKLand + w));
-          ++nkl[w];
-          kl_wait[w] = true;
-          if (sq + 1 < u.n_kv) ph = tile_phys(u, tile_of(u, sq + 1));
-          if (q_wait) {  // Q to f16 while K(0)'s codes are on their way
-            if (!wait_bar(bar(kQLand), (nq - 1) & 1, abort, p.status)) { ok = false; break; }
-            q_wait = false;
-            q_to_f16();
-            if (lane == 0) mbar_arrive(bar(kQFull));
-          }
-          if (!wait_bar(bar(kKLand + w), (nkl[w] - 1) & 1, abort, p.status)) { ok = false; break; }
-          kl_wait[w] = false;
-          widen_tile(kbuf, false, 0x7fffffff);
+          const uint32_t b = kw & 1;
+          if (!wait_bar(bar(kKLand + b), (kw >> 1) & 1, abort, p.status)) { ok = false; break; }
+          ++kw;
+          widen_tile(sbase + C::kKCodeOff + b * C::kCodeBytes, kbuf, false);
+          fence_proxy_async_smem();  // the generic-proxy writes, before the tensor cores read them
+          __syncwarp();
           if (lane == 0) mbar_arrive(full);
+          if (sq + 2 < u.n_kv) copy_codes(sq + 2);  // into the staging buffer just read
           continue;
         }
         copy_kv_tile(u, tile_of(u, sq), ph, false, kbuf, full);
@@ -489,8 +560,7 @@ __global__ void __launch_bounds__(kPfThreads, 1)
     if (*abort) {  // let every copy issued land before the CTA ends
       if constexpr (F8) {
         if (q_wait) drain_wait(bar(kQLand), (nq - 1) & 1);
-        for (int w = 0; w < 2; ++w)
-          if (kl_wait[w]) drain_wait(bar(kKLand + w), (nkl[w] - 1) & 1);
+        for (uint32_t i = kw; i < kc; ++i) drain_wait(bar(kKLand + (i & 1)), (i >> 1) & 1);
       } else {
         if (nq > 0) drain_wait(bar(kQFull), (nq - 1) & 1);
         for (int w = 0; w < 2; ++w) {
@@ -507,6 +577,9 @@ __global__ void __launch_bounds__(kPfThreads, 1)
     uint32_t nv[2] = {0, 0}, gv[2] = {0, 0}, nl[2] = {0, 0};
     bool landing = false;  // a kVLand copy not yet waited for
     int land_w = 0;
+    // FP8: code copies issued / waited (copy i: staging buffer i % kVStages)
+    constexpr uint32_t NS = C::kVStages;
+    uint32_t vc = 0, vw = 0;
     for (int uc = 0;; ++uc) {
       const int slot = uc & 1;
       if (!wait_bar(bar(kUnitFull + slot), (uc >> 1) & 1, abort, p.status)) break;
@@ -514,6 +587,14 @@ __global__ void __launch_bounds__(kPfThreads, 1)
       warp_arrive(bar(kUnitEmpty + slot));
       if (u.r < 0) break;
       int ph = tile_phys(u, tile_of(u, 0));
+      auto copy_codes = [&](int sq) {  // FP8: into staging buffer vc % NS
+        copy_kv_tile(u, tile_of(u, sq), ph, true, sbase + C::kVCodeOff + (vc % NS) * C::kCodeBytes,
+                     bar(kVLand + vc % NS));
+        ++vc;
+        if (sq + 1 < u.n_kv) ph = tile_phys(u, tile_of(u, sq + 1));
+      };
+      if constexpr (F8)
+        for (int sq = 0; sq < min(static_cast<int>(NS), u.n_kv); ++sq) copy_codes(sq);
       bool ok = true;
       for (int sq = 0; sq < u.n_kv; ++sq) {
         const int w = sq & 1;
@@ -525,16 +606,22 @@ __global__ void __launch_bounds__(kPfThreads, 1)
         }
         const uint32_t vb = sbase + C::kVOff + w * C::kTileBytes;
         if constexpr (F8) {
-          // codes -> kVLand, widened to f16 here; rows past the unit's last
+          // widened to f16 from the staging buffer; rows past the unit's last
           // key (unwritten slots) become zeros, so p = 0 never meets a NaN
-          copy_kv_tile(u, kt, ph, true, vb, bar(kVLand + w));
-          landing = true;
-          land_w = w;
-          if (!wait_bar(bar(kVLand + w), nl[w] & 1, abort, p.status)) { ok = false; break; }
-          landing = false;
-          ++nl[w];
-          widen_tile(vb, true, u.kv_end - kt * kTileN);
+          const uint32_t b = vw % NS;
+          if (!wait_bar(bar(kVLand + b), (vw / NS) & 1, abort, p.status)) { ok = false; break; }
+          ++vw;
+          widen_tile(sbase + C::kVCodeOff + b * C::kCodeBytes, vb, true);
+          const int r0 = u.kv_end - kt * kTileN;
+          if (r0 < kTileN) {
+            __syncwarp();
+            zero_v_rows(vb, r0, (r0 + kBlockSize - 1) & ~(kBlockSize - 1));
+          }
+          fence_proxy_async_smem();
           warp_arrive(bar(kGo + w));
+          if (sq + static_cast<int>(NS) < u.n_kv) copy_codes(sq + NS);
+          ++nv[w];
+          continue;
         } else if (kt != u.kt0 + u.n_kv - 1 || (u.kv_end & (kBlockSize - 1)) == 0) {
           copy_kv_tile(u, kt, ph, true, vb, bar(kGo + w));  // this tile's kGo arrival
           gv[w] = nv[w] + 1;
@@ -548,18 +635,8 @@ __global__ void __launch_bounds__(kPfThreads, 1)
           if (!wait_bar(bar(kVLand + w), nl[w] & 1, abort, p.status)) { ok = false; break; }
           landing = false;
           ++nl[w];
-          const int tok0 = kt * kTileN;
-          const int r0 = u.kv_end - tok0;
-          const int r1 = ((u.kv_end + kBlockSize - 1) & ~(kBlockSize - 1)) - tok0;
-          constexpr int per_row = (D / 64) * 8;  // 16-byte chunks per row
-          for (int idx = lane; idx < (r1 - r0) * per_row; idx += 32) {
-            const int row = r0 + idx / per_row, c = idx % per_row;
-            asm volatile("st.shared.v4.b32 [%0], {%1,%1,%1,%1};\n" ::"r"(
-                             vb + (row >> 4) * C::kVBlockBytes + (c >> 3) * (kBlockSize * 128) +
-                             (row & 15) * 128 + (c & 7) * 16),
-                         "r"(0u)
-                         : "memory");
-          }
+          const int r0 = u.kv_end - kt * kTileN;
+          zero_v_rows(vb, r0, (r0 + kBlockSize - 1) & ~(kBlockSize - 1));
           fence_proxy_async_smem();
           warp_arrive(bar(kGo + w));
         }
@@ -570,6 +647,7 @@ __global__ void __launch_bounds__(kPfThreads, 1)
     }
     if (*abort) {
       if (landing) drain_wait(bar(kVLand + land_w), nl[land_w] & 1);
+      for (uint32_t i = vw; i < vc; ++i) drain_wait(bar(kVLand + i % NS), (i / NS) & 1);
       for (int w = 0; w < 2; ++w)
         if (gv[w] > 0) drain_wait(bar(kGo + w), (gv[w] - 1) & 1, kGoDrainLimit);
     }
@@ -686,14 +764,14 @@ __global__ void __launch_bounds__(kPfThreads, 1)
     uint32_t nb0 = 0, nb1 = 0;  // tiles per buffer parity so far (all units)
     uint32_t npieces = 0;       // split pieces finished so far
     const int Hkv = p.num_kv_heads;
-    // Merge of a split query tile, by its last piece: this thread's row i and
-    // its warpgroup's half of the columns, from every piece's (max, sum) and
-    // unnormalised O (fp32, in L2).
+    // Merge of a split unit, by its last piece: this thread's row i and its
+    // warpgroup's half of the columns, from every piece's (max, sum) and
+    // unnormalised O (fp32, in L2); piece sp's state is in slot slot0 + sp.
     auto merge_row = [&](const UnitInfo& u, long long tok, int hh) {
-      const long long rbase = static_cast<long long>(u.slot0) * Hkv + u.g;
+      const long long rbase = u.slot0;
       auto ml_of = [&](int sp) {
         return __ldcg(reinterpret_cast<const float2*>(p.part_ml) +
-                      ((rbase + static_cast<long long>(sp) * Hkv) * kTileM + i));
+                      ((rbase + sp) * kTileM + i));
       };
       float M = -CUDART_INF_F;
       for (int sp = 0; sp < u.nsplit; ++sp) M = fmaxf(M, ml_of(sp).x);
@@ -712,7 +790,7 @@ __global__ void __launch_bounds__(kPfThreads, 1)
         for (int sp = 0; sp < u.nsplit; ++sp) {
           const float f = ex2(ml_of(sp).x - M);
           const float4* src = reinterpret_cast<const float4*>(
-              p.part_acc + ((rbase + static_cast<long long>(sp) * Hkv) * kTileM + i) * D + c0);
+              p.part_acc + ((rbase + sp) * kTileM + i) * D + c0);
           float4 v[8];
 #pragma unroll
           for (int j = 0; j < 8; ++j) v[j] = __ldcg(src + j);
@@ -863,8 +941,7 @@ __global__ void __launch_bounds__(kPfThreads, 1)
       // a piece of a split query tile keeps its state: unnormalised O and
       // the row's (maximum used, sum) go to its partial slot
       const bool split = u.nsplit > 1;
-      const long long prow =
-          (static_cast<long long>(u.slot0 + u.piece) * Hkv + u.g) * kTileM + i;
+      const long long prow = static_cast<long long>(u.slot0 + u.piece) * kTileM + i;
 #pragma unroll
       for (int c0 = w * kOCols; c0 < (w + 1) * kOCols; c0 += 32) {
         uint32_t o[32];
@@ -970,6 +1047,7 @@ bool encode_map_u8(CUtensorMap* m, const void* base, int rank, const cuuint64_t*
 template <int D, int G, bool F8>
 cudaError_t launch_pf(const AttnParams& p, int num_sms, cudaStream_t stream) {
   using C = PfCfg<D>;
+  constexpr int kSmem = F8 ? C::kSmemBytesF8 : C::kSmemBytes;
   static bool configured[64] = {false};
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
@@ -977,7 +1055,7 @@ cudaError_t launch_pf(const AttnParams& p, int num_sms, cudaStream_t stream) {
   if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
   if (!configured[dev]) {
     e = cudaFuncSetAttribute(prefill_tc_kernel<D, G, F8>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             C::kSmemBytes);
+                             kSmem);
     if (e != cudaSuccess) return e;
     configured[dev] = true;
   }
@@ -1024,7 +1102,7 @@ cudaError_t launch_pf(const AttnParams& p, int num_sms, cudaStream_t stream) {
                                 static_cast<cuuint32_t>(D / 64), 1, 1};
     if (!encode_map(&maps.v, p.v_cache, 5, vdims, vstrides, vbox)) return cudaErrorInvalidValue;
   }
-  prefill_tc_kernel<D, G, F8><<<num_sms, kPfThreads, C::kSmemBytes, stream>>>(p, maps);
+  prefill_tc_kernel<D, G, F8><<<num_sms, kPfThreads, kSmem, stream>>>(p, maps);
   return cudaGetLastError();
 }
 

@@ -92,3 +92,14 @@ def test_fp8_mixed_step():
     over an 8-bit cache: decode and few-token kernels read codes, the chunks
     run on the tensor cores."""
     _run(W.spec_mixed_step(), 0.01, 0.01)
+
+
+@pytest.mark.parametrize("D,G", [(64, 8), (64, 2), (128, 1)])
+def test_fp8_long_chunks(D, G):
+    """Chunks of 40-300 tokens over 1000-3000 keys (up to 24 KV tiles a unit,
+    several units per CTA) over an 8-bit cache: the staged code copies run
+    ahead across tiles and units (two V staging buffers at D = 64, one at
+    D = 128), and the last tile's ragged block is zeroed."""
+    spec = W.custom_spec(f"fp8-long-{D}-{G}", "bf16", 2 * G, 2, D, [300, 1, 129, 40],
+                         [3000, 77, 1001, 1500], seed=90 + D + G)
+    _run(spec, 0.01, 0.02)
