@@ -182,6 +182,30 @@ def test_random_shapes(dtype, D, G, shape):
     _full_parity(W.make_step(spec))
 
 
+def test_many_requests_plan_passes():
+    """700 requests, more than the plan kernel's CTA holds at once: its passes
+    over the requests carry every list's offsets, the decode dispatch order
+    (long splits in request order, short ones in the shared short-item list)
+    and the prefill query tiles across passes.  Decodes (some split: longer
+    than 2048 keys), few-token queries (2-15) and chunks of 16-40 tokens."""
+    rng = np.random.default_rng(321)
+    q_lens, seq_lens = [], []
+    for i in range(700):
+        kind = rng.random()
+        if kind < 0.8:
+            q, s = 1, int(rng.integers(1, 2600))
+        elif kind < 0.95:
+            q = int(rng.integers(2, 16))
+            s = q + int(rng.integers(0, 2400))
+        else:
+            q = int(rng.integers(16, 41))
+            s = q + int(rng.integers(0, 600))
+        q_lens.append(q)
+        seq_lens.append(s)
+    spec = W.custom_spec("many-requests", "bf16", 8, 2, 64, q_lens, seq_lens, seed=322)
+    _full_parity(W.make_step(spec))
+
+
 def test_prefix_sharing_and_permutation_invariance():
     """Outputs are bit-identical when the physical blocks are renumbered (data
     moved with them), including blocks shared by several tables."""
