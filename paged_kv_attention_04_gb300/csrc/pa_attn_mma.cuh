@@ -123,6 +123,16 @@ __device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint32_t codes16) {
   return r;
 }
 
+// Four E4M3 codes (one 32-bit word, low byte first) -> two f16x2, exactly:
+// codes 0-1 into lo, codes 2-3 into hi.  The word is unpacked into its 16-bit
+// halves in PTX, which measured faster than shifting the high half down.
+__device__ __forceinline__ void e4m3x4_to_f16x2x2(uint32_t w, uint32_t& lo, uint32_t& hi) {
+  asm("{\n .reg .b16 l16, h16;\n mov.b32 {l16, h16}, %2;\n"
+      " cvt.rn.f16x2.e4m3x2 %0, l16;\n cvt.rn.f16x2.e4m3x2 %1, h16;\n}\n"
+      : "=r"(lo), "=r"(hi)
+      : "r"(w));
+}
+
 // SW (decode tiles only, P = 1): the keys are the MMA's M dimension and the
 // G <= 8 query rows its N; otherwise the query rows are M, padded to 16.
 template <int D, int G, int P, int NW, int NS, bool F8, bool SW>
@@ -607,8 +617,9 @@ __global__ void __launch_bounds__(MmaCfg<D, G, P, NW, NS, F8, SW>::kThreads,
             }
 #pragma unroll
             for (int kk = 0; kk < C::kKSteps; ++kk) {
-              const uint32_t a[4] = {e4m3x2_to_f16x2(kw[0][kk]), e4m3x2_to_f16x2(kw[1][kk]),
-                                     e4m3x2_to_f16x2(kw[0][kk] >> 16), e4m3x2_to_f16x2(kw[1][kk] >> 16)};
+              uint32_t a[4];
+              e4m3x4_to_f16x2x2(kw[0][kk], a[0], a[2]);
+              e4m3x4_to_f16x2x2(kw[1][kk], a[1], a[3]);
               mma_f16((kk & 1) ? sb : sa, a, qb[kk][0], qb[kk][1]);
             }
           } else {
@@ -698,12 +709,11 @@ __global__ void __launch_bounds__(MmaCfg<D, G, P, NW, NS, F8, SW>::kThreads,
 #pragma unroll
             for (int mt = 0; mt < C::kKSteps; ++mt) {
               const int w = mt >> 1;
-              const uint32_t sel0 = (mt & 1) ? 0x62u : 0x40u;  // byte of dim 2mt, two keys
-              const uint32_t sel1 = (mt & 1) ? 0x73u : 0x51u;  // byte of dim 2mt + 1
-              const uint32_t a[4] = {e4m3x2_to_f16x2(__byte_perm(vw[0][w], vw[1][w], sel0)),
-                                     e4m3x2_to_f16x2(__byte_perm(vw[0][w], vw[1][w], sel1)),
-                                     e4m3x2_to_f16x2(__byte_perm(vw[2][w], vw[3][w], sel0)),
-                                     e4m3x2_to_f16x2(__byte_perm(vw[2][w], vw[3][w], sel1))};
+              // dims 2mt and 2mt + 1 of two keys: one permute builds both pairs
+              const uint32_t sel = (mt & 1) ? 0x7362u : 0x5140u;
+              uint32_t a[4];
+              e4m3x4_to_f16x2x2(__byte_perm(vw[0][w], vw[1][w], sel), a[0], a[1]);
+              e4m3x4_to_f16x2x2(__byte_perm(vw[2][w], vw[3][w], sel), a[2], a[3]);
               mma_f16(o[mt], a, pb0, pb1);
             }
           } else {
@@ -798,8 +808,11 @@ __global__ void __launch_bounds__(MmaCfg<D, G, P, NW, NS, F8, SW>::kThreads,
           for (int kk = 0; kk < C::kKSteps; ++kk) {
             float* d0 = (PA_QK_SPLIT_ACC && (kk & 1)) ? s2[0] : s[0];
             float* d1 = (PA_QK_SPLIT_ACC && (kk & 1)) ? s2[1] : s[1];
-            mma_f16(d0, qa[kk], e4m3x2_to_f16x2(kw[0][kk]), e4m3x2_to_f16x2(kw[0][kk] >> 16));
-            mma_f16(d1, qa[kk], e4m3x2_to_f16x2(kw[1][kk]), e4m3x2_to_f16x2(kw[1][kk] >> 16));
+            uint32_t b0[2], b1[2];
+            e4m3x4_to_f16x2x2(kw[0][kk], b0[0], b0[1]);
+            e4m3x4_to_f16x2x2(kw[1][kk], b1[0], b1[1]);
+            mma_f16(d0, qa[kk], b0[0], b0[1]);
+            mma_f16(d1, qa[kk], b1[0], b1[1]);
           }
 #pragma unroll
           for (int e = 0; e < 4; ++e) {
@@ -938,14 +951,15 @@ __global__ void __launch_bounds__(MmaCfg<D, G, P, NW, NS, F8, SW>::kThreads,
           }
 #pragma unroll
           for (int w = 0; w < D / 32; ++w) {
-            const uint32_t lo0 = __byte_perm(vw[0][w], vw[1][w], 0x5140);
-            const uint32_t hi0 = __byte_perm(vw[0][w], vw[1][w], 0x7362);
-            const uint32_t lo1 = __byte_perm(vw[2][w], vw[3][w], 0x5140);
-            const uint32_t hi1 = __byte_perm(vw[2][w], vw[3][w], 0x7362);
-            mma_f16(o[4 * w + 0], pa, e4m3x2_to_f16x2(lo0), e4m3x2_to_f16x2(lo1));
-            mma_f16(o[4 * w + 1], pa, e4m3x2_to_f16x2(lo0 >> 16), e4m3x2_to_f16x2(lo1 >> 16));
-            mma_f16(o[4 * w + 2], pa, e4m3x2_to_f16x2(hi0), e4m3x2_to_f16x2(hi1));
-            mma_f16(o[4 * w + 3], pa, e4m3x2_to_f16x2(hi0 >> 16), e4m3x2_to_f16x2(hi1 >> 16));
+            uint32_t l0[2], h0[2], l1[2], h1[2];
+            e4m3x4_to_f16x2x2(__byte_perm(vw[0][w], vw[1][w], 0x5140), l0[0], l0[1]);
+            e4m3x4_to_f16x2x2(__byte_perm(vw[0][w], vw[1][w], 0x7362), h0[0], h0[1]);
+            e4m3x4_to_f16x2x2(__byte_perm(vw[2][w], vw[3][w], 0x5140), l1[0], l1[1]);
+            e4m3x4_to_f16x2x2(__byte_perm(vw[2][w], vw[3][w], 0x7362), h1[0], h1[1]);
+            mma_f16(o[4 * w + 0], pa, l0[0], l1[0]);
+            mma_f16(o[4 * w + 1], pa, l0[1], l1[1]);
+            mma_f16(o[4 * w + 2], pa, h0[0], h1[0]);
+            mma_f16(o[4 * w + 3], pa, h0[1], h1[1]);
           }
         } else {
           const int mi = lane >> 3;
