@@ -115,6 +115,16 @@ __device__ __forceinline__ uint32_t movm_trans(uint32_t x) {
   asm volatile("movmatrix.sync.aligned.m8n8.trans.b16 %0, %1;\n" : "=r"(r) : "r"(x));
   return r;
 }
+// 2^x by the hardware approximation (ex2.approx.ftz: relative error about
+// 2^-22, 0 for -inf), in place of the library exp2f: the softmax and the
+// merges take 2^x of base-2 logits, and the shorter instruction sequence
+// measured faster on the latency-bound FP8 and small decodes (FP8
+// Llama-3-8B 139.3 -> 135.2 us, FP8 TinyLlama 24.6 -> 22.5 us).
+__device__ __forceinline__ float ex2_approx(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;\n" : "=f"(y) : "f"(x));
+  return y;
+}
 // Two E4M3 codes (low byte first) -> two f16 values, exactly.
 __device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint32_t codes16) {
   uint32_t r;
@@ -459,7 +469,7 @@ __global__ void __launch_bounds__(MmaCfg<D, G, P, NW, NS, F8, SW>::kThreads,
       if (M != -CUDART_INF_F) {
 #pragma unroll
         for (int w = 0; w < NW; ++w) {
-          const float f = exp2f(cm[(w * R + row) * 2] - M);
+          const float f = ex2_approx(cm[(w * R + row) * 2] - M);
           const float4 c4 = *reinterpret_cast<const float4*>(cb + (w * R + row) * D + d);
           num.x = fmaf(c4.x, f, num.x); num.y = fmaf(c4.y, f, num.y);
           num.z = fmaf(c4.z, f, num.z); num.w = fmaf(c4.w, f, num.w);
@@ -514,13 +524,13 @@ __global__ void __launch_bounds__(MmaCfg<D, G, P, NW, NS, F8, SW>::kThreads,
             for (int j = 0; j < kMergeChunk; ++j) mc = fmaxf(mc, ml[j].x);
             if (mc == -CUDART_INF_F) continue;
             if (mc > M) {  // rescale the running sums to the new maximum
-              const float sc = exp2f(M - mc);  // 0 while nothing was visible
+              const float sc = ex2_approx(M - mc);  // 0 while nothing was visible
               num.x *= sc; num.y *= sc; num.z *= sc; num.w *= sc; den *= sc;
               M = mc;
             }
 #pragma unroll
             for (int j = 0; j < kMergeChunk; ++j) {
-              const float f = exp2f(ml[j].x - M);  // 0 for an empty split
+              const float f = ex2_approx(ml[j].x - M);  // 0 for an empty split
               num.x = fmaf(a4[j].x, f, num.x); num.y = fmaf(a4[j].y, f, num.y);
               num.z = fmaf(a4[j].z, f, num.z); num.w = fmaf(a4[j].w, f, num.w);
               den = fmaf(ml[j].y, f, den);
@@ -653,16 +663,16 @@ __global__ void __launch_bounds__(MmaCfg<D, G, P, NW, NS, F8, SW>::kThreads,
           const float mn0 = fmaxf(m0, mx0), mn1 = fmaxf(m1, mx1);
           float corr0 = 1.f, corr1 = 1.f, pr[4];
           if (mn0 != -CUDART_INF_F) {
-            corr0 = exp2f(m0 - mn0);
-            pr[0] = exp2f(s[0] - mn0);
-            pr[2] = exp2f(s[2] - mn0);
+            corr0 = ex2_approx(m0 - mn0);
+            pr[0] = ex2_approx(s[0] - mn0);
+            pr[2] = ex2_approx(s[2] - mn0);
           } else {
             pr[0] = pr[2] = 0.f;
           }
           if (mn1 != -CUDART_INF_F) {
-            corr1 = exp2f(m1 - mn1);
-            pr[1] = exp2f(s[1] - mn1);
-            pr[3] = exp2f(s[3] - mn1);
+            corr1 = ex2_approx(m1 - mn1);
+            pr[1] = ex2_approx(s[1] - mn1);
+            pr[3] = ex2_approx(s[3] - mn1);
           } else {
             pr[1] = pr[3] = 0.f;
           }
@@ -858,11 +868,11 @@ __global__ void __launch_bounds__(MmaCfg<D, G, P, NW, NS, F8, SW>::kThreads,
           const float mn = fmaxf(mA, mx);
           float corr = 1.f;
           if (mn != -CUDART_INF_F) {
-            corr = exp2f(mA - mn);
+            corr = ex2_approx(mA - mn);
 #pragma unroll
             for (int j = 0; j < 2; ++j)
 #pragma unroll
-              for (int e = 0; e < 2; ++e) pA[j * 2 + e] = exp2f(s[j][e] - mn);
+              for (int e = 0; e < 2; ++e) pA[j * 2 + e] = ex2_approx(s[j][e] - mn);
           } else {
 #pragma unroll
             for (int e = 0; e < 4; ++e) pA[e] = 0.f;
@@ -886,11 +896,11 @@ __global__ void __launch_bounds__(MmaCfg<D, G, P, NW, NS, F8, SW>::kThreads,
             mxb = fmaxf(mxb, __shfl_xor_sync(0xffffffffu, mxb, 2));
             const float mnb = fmaxf(mB, mxb);
             if (mnb != -CUDART_INF_F) {
-              corrB = exp2f(mB - mnb);
+              corrB = ex2_approx(mB - mnb);
 #pragma unroll
               for (int j = 0; j < 2; ++j)
 #pragma unroll
-                for (int e = 0; e < 2; ++e) pB[j * 2 + e] = exp2f(s[j][2 + e] - mnb);
+                for (int e = 0; e < 2; ++e) pB[j * 2 + e] = ex2_approx(s[j][2 + e] - mnb);
             } else {
 #pragma unroll
               for (int e = 0; e < 4; ++e) pB[e] = 0.f;
