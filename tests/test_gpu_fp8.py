@@ -103,3 +103,36 @@ def test_fp8_long_chunks(D, G):
     spec = W.custom_spec(f"fp8-long-{D}-{G}", "bf16", 2 * G, 2, D, [300, 1, 129, 40],
                          [3000, 77, 1001, 1500], seed=90 + D + G)
     _run(spec, 0.01, 0.02)
+
+
+def test_fp8_chunked_schedule_sampled():
+    """The chunked schedule (152 units of ~30 KV tiles cut into equal chunks)
+    over an 8-bit cache: the quantising write bit for bit, attention on
+    sampled rows against the oracle over the dequantised cache."""
+    L, prior, Hkv, D = 19 * 128, 3000, 8, 128
+    spec = W.custom_spec("fp8-chunked", "bf16", Hkv, Hkv, D, [L], [prior + L], seed=451)
+    cpu = W.make_step(spec)
+    ks, vs = 0.01, 0.02
+    kc0, vc0 = _pool_codes(cpu.k_cache, ks), _pool_codes(cpu.v_cache, vs)
+    st = cpu.to("cuda")
+    kc, vc = kc0.cuda(), vc0.cuda()
+    lay = P.layout_of(kc, spec.num_q_heads, k_scale=ks, v_scale=vs)
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    P.pa_cache_write(st.k, st.v, st.slot_mapping, kc, vc, lay, status)
+    ws = P.alloc_workspace(lay, spec.num_seqs, spec.num_tokens, st.max_seq_len)
+    out = torch.full_like(st.q, float("nan"))
+    P.pa_forward(st.q, kc, vc, st.block_tables, st.seq_lens, st.query_start_loc,
+                 st.max_query_len, st.max_seq_len, st.scale, out, ws, lay, status)
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0
+    rk, rv = fp8.cache_write_fp8(oracle.widen(bits(cpu.k)), oracle.widen(bits(cpu.v)),
+                                 cpu.slot_mapping.numpy(), kc0.numpy(), vc0.numpy(), ks, vs)
+    assert np.array_equal(kc.cpu().numpy(), rk) and np.array_equal(vc.cpu().numpy(), rv)
+    nb = oracle.blocks_needed(prior + L)
+    bt = cpu.block_tables.numpy()[0, :nb]
+    rows = [(j, g) for g in range(Hkv) for j in (0, 127, 128, L // 2, L - 1)]
+    ref = oracle.paged_attention_rows(bits(cpu.q), fp8.dequantize(rk, ks)[bt], fp8.dequantize(rv, vs)[bt],
+                                      np.arange(nb)[None, :], spec.seq_lens, np.array([0, L]),
+                                      cpu.scale, Hkv, rows)
+    got = torch.stack([out[t, h] for t, h in rows])
+    assert_close(got, ref, "bf16", spec.name)

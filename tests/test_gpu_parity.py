@@ -138,6 +138,31 @@ def test_long_prior_chunks_sampled_parity():
         assert_close(got, ref, "bf16", f"long prior chunk r={r}")
 
 
+@pytest.mark.parametrize("D,G", [(64, 1), (128, 1), (64, 2), (128, 2)])
+def test_chunked_schedule_sampled_parity(D, G):
+    """One chunk of 19 query tiles over 3000 prior keys with 8 kv heads: 152
+    units of ~30 KV tiles, which the plan cuts into equal chunks of a unit
+    line (units cut at chunk boundaries become pieces merged by the last).
+    The whole cache write is checked bit for bit, attention on sampled rows
+    (query-tile edges and the middle, every kv head)."""
+    pm = 128 // G
+    L, prior, Hkv = 19 * pm, 3000, 8
+    spec = W.custom_spec(f"chunked-{D}-{G}", "bf16", Hkv * G, Hkv, D, [L], [prior + L], seed=400 + D + G)
+    step = W.make_step(spec, device="cuda")
+    out, kc, vc, status = run_gpu(step)
+    assert status == 0
+    mk, mv = oracle.cache_write(bits(step.k), bits(step.v), step.slot_mapping.cpu().numpy(),
+                                bits(step.k_cache), bits(step.v_cache))
+    assert np.array_equal(bits(kc), mk) and np.array_equal(bits(vc), mv)
+    nb = oracle.blocks_needed(prior + L)
+    bt = step.block_tables.cpu().numpy()[0, :nb]
+    rows = [(j, g * G + (j + g) % G) for g in range(Hkv) for j in (0, pm - 1, pm, L // 2, L - 1)]
+    ref = oracle.paged_attention_rows(bits(step.q), mk[bt], mv[bt], np.arange(nb)[None, :],
+                                      spec.seq_lens, np.array([0, L]), step.scale, Hkv, rows)
+    got = torch.stack([out[t, h] for t, h in rows])
+    assert_close(got, ref, "bf16", spec.name)
+
+
 def test_prefill_runs_are_bit_identical():
     """Chunks of 16 to 1000 tokens over contexts up to 3000 keys: ~450 tensor-core
     units, several per CTA, so every hand-off between the kernel's roles is
