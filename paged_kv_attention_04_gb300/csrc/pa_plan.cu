@@ -399,6 +399,30 @@ __global__ void __launch_bounds__(kPlanThreads, 1) plan_kernel(PlanParams p) {
       tps = static_cast<int>(min(static_cast<long long>(INT_MAX),
                                  max(max(want, need), static_cast<long long>(kMinPrefillSplitTiles))));
     }
+    // tps bounds the pieces from the mean; the longest piece decides the
+    // round, so take the smallest size that still fits: thread i tries
+    // tps - i, counting its pieces (and partial slots) over the query tiles
+    // (64 tokens after 32768 and 16 after 98304: pieces of at most 70 KV
+    // tiles instead of 77, 120.4 -> 119.0 us)
+    __shared__ int s_nkv[kPlanThreads];
+    __shared__ int s_tps;
+    if (tps != INT_MAX && n_pt <= kPlanThreads) {
+      if (threadIdx.x < n_pt) s_nkv[threadIdx.x] = max(1, tiles_p[threadIdx.x].nkv);
+      if (threadIdx.x == 0) s_tps = tps;
+      __syncthreads();
+      const int T = tps - static_cast<int>(threadIdx.x);
+      if (T >= kMinPrefillSplitTiles) {
+        long long pieces = 0, slots = 0;
+        for (int q = 0; q < n_pt; ++q) {
+          const int k = ceil_div(s_nkv[q], T);
+          pieces += k;
+          slots += k > 1 ? k : 0;
+        }
+        if (pieces * Hkv <= P && slots * Hkv <= p.cap.prefill_slots) atomicMin(&s_tps, T);
+      }
+      __syncthreads();
+      tps = s_tps;
+    }
   } else if (n_units >= P && n_units <= kPrefillChunkMaxWaves * P &&
              kv_tiles >= kPrefillChunkMinTiles * n_pt && p.cap.prefill_slots >= 2) {
     // chunks of clen line positions, clen >= the unit cost + two minimum

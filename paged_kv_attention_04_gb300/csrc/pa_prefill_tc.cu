@@ -429,7 +429,14 @@ __global__ void __launch_bounds__(kPfThreads, 1)
     // FP8: code copies issued / waited (copy i: staging buffer i & 1, phase i >> 1)
     uint32_t kc = 0, kw = 0;
     bool q_wait = false;  // FP8: the Q copy not yet waited for
-    for (int uc = 0;; ++uc) {
+    // The next unit is claimed and published while the current one's last
+    // tiles run (before its trailing kGo arrivals), so its metadata loads,
+    // Q copy and first K copies are not a serial gap between units; a CTA's
+    // first claim is its own index (no atomic), later ones count on from the
+    // grid size.  (The mixed step's two 512-token chunks, 256 units of 1-16
+    // KV tiles: 30.4 -> 28.8 us.)
+    bool first_claim = true;
+    auto claim = [&](int ucn, UnitInfo& u) -> bool {
       int pc = -1;
       while (true) {
         if (rk < rn) {
@@ -437,14 +444,18 @@ __global__ void __launch_bounds__(kPfThreads, 1)
           break;
         }
         int c = 0;
-        if (lane == 0) c = atomicAdd(p.next, 1);
-        c = __shfl_sync(0xffffffffu, c, 0);
+        if (first_claim) {
+          c = blockIdx.x;
+          first_claim = false;
+        } else {
+          if (lane == 0) c = static_cast<int>(gridDim.x) + atomicAdd(p.next, 1);
+          c = __shfl_sync(0xffffffffu, c, 0);
+        }
         if (c >= n_chunks) break;
         ra = chunked ? __ldg(p.order + c) : c;
         rn = (chunked ? __ldg(p.order + c + 1) : c + 1) - ra;
         rk = 0;
       }
-      UnitInfo u;
       u.r = -1;
       if (pc >= 0) {
         const int4 ta = __ldg(&pieces[pc].a), tb = __ldg(&pieces[pc].b);
@@ -467,14 +478,18 @@ __global__ void __launch_bounds__(kPfThreads, 1)
         u.nsplit = tb.y;
         u.slot0 = tb.z;
       }
-      const int slot = uc & 1;
-      if (uc >= 2 && !wait_bar(bar(kUnitEmpty + slot), ((uc >> 1) - 1) & 1, abort, p.status)) break;
+      const int slot = ucn & 1;
+      if (ucn >= 2 && !wait_bar(bar(kUnitEmpty + slot), ((ucn >> 1) - 1) & 1, abort, p.status))
+        return false;
       if (lane == 0) {
         s_units[slot] = u;
         mbar_arrive(bar(kUnitFull + slot));
       }
+      return true;
+    };
+    UnitInfo u;
+    if (claim(0, u)) for (int uc = 0;; ++uc) {
       if (u.r < 0) break;
-
       int ph = tile_phys(u, tile_of(u, 0));
       // FP8: the codes of the unit's first two tiles into the staging buffers
       // (free: every copy issued before has been widened), ahead of Q
@@ -540,6 +555,8 @@ __global__ void __launch_bounds__(kPfThreads, 1)
         copy_kv_tile(u, tile_of(u, sq), ph, false, kbuf, full);
         if (sq + 1 < u.n_kv) ph = tile_phys(u, tile_of(u, sq + 1));
       }
+      UnitInfo nu;
+      if (ok) ok = claim(uc + 1, nu);
       // tiles with no K two places on: a plain kGo arrival once their S is done
       for (int t = max(0, u.n_kv - 2); ok && t < u.n_kv; ++t) {
         const int w = t & 1;
@@ -549,6 +566,7 @@ __global__ void __launch_bounds__(kPfThreads, 1)
         warp_arrive(bar(kGo + w));
       }
       if (!ok) break;
+      u = nu;
     }
     if (*abort) {  // let every copy issued land before the CTA ends
       if constexpr (F8) {
@@ -916,18 +934,19 @@ __global__ void __launch_bounds__(kPfThreads, 1)
       }
       if (!ok) break;
 
-      // ---- both halves' row sums, then this group's half of the O columns
+      // ---- both halves' row sums (traded while the last PV runs), then
+      // this group's half of the O columns
+      s_ml[w][i] = l_part;
+      warp_arrive(bar(kMlFull));
+      if (!wait_bar(bar(kMlFull), uc & 1, abort, p.status)) break;
+      const float l_sum = l_part + s_ml[w ^ 1][i];
+      warp_arrive(bar(kMlRead));
       {
         const int lb = (u.n_kv - 1) & 1;  // buffer of the last tile: its PV covers all
         const uint32_t npv = (lb ? nb1 : nb0) - 1;
         if (!wait_bar(bar(kPVDone + lb), npv & 1, abort, p.status)) break;
       }
       tc_fence_after();
-      s_ml[w][i] = l_part;
-      warp_arrive(bar(kMlFull));
-      if (!wait_bar(bar(kMlFull), uc & 1, abort, p.status)) break;
-      const float l_sum = l_part + s_ml[w ^ 1][i];
-      warp_arrive(bar(kMlRead));
       const float inv = p.out_scale / l_sum;
       const long long tok = u.a + u.j0 + jj;
       __nv_bfloat16* orow = out + (tok * Hq + u.g * G + (i - jj * G)) * D;
