@@ -452,7 +452,7 @@ class StepRunner:
         self._flush.view(self.torch.int32).sum()
 
     def time_device(self, steps: int, warmup: int, world: int, clocks: ClockSampler | None = None,
-                    flush: bool = False):
+                    flush: bool = False, serial_kernels: bool = False):
         """Inputs resident in HBM; returns (ms per step, decode-kernel ms per launch,
         prefill-kernel ms per launch or None), the kernel times being medians over
         the launches.  The steps are timed in one loop with no events inside a
@@ -505,7 +505,15 @@ class StepRunner:
         step_ms = loop(False)
         if clocks:
             clocks.mark("timed_end")
-        dec_ms, pf_ms = loop(True)
+        if serial_kernels and has_prefill:
+            # the prefill kernel on the caller's stream: its events then time it
+            # alone, not also the wait for SMs that the decode kernel's CTAs
+            # (resident early, with no work in a prefill-only step) hold
+            P.pa_set_prefill_overlap(False)
+        try:
+            dec_ms, pf_ms = loop(True)
+        finally:
+            P.pa_set_prefill_overlap(True)
         return step_ms, dec_ms, pf_ms
 
     def time_graph(self, steps: int, warmup: int, world: int, flush: bool = False) -> float:
@@ -704,7 +712,7 @@ def run_gpu_arm(args):
 
     # ---- the mixed step's two prefill chunks alone: the tensor-core kernel's own rate
     pf = StepRunner(MIXED, seed_offset=seed_off, requests=slice(-2, None))
-    pms, _, ppf = pf.time_device(half, args.warmup, world, flush=True)
+    pms, _, ppf = pf.time_device(half, args.warmup, world, flush=True, serial_kernels=True)
     pms, ppf = dist_max(pms, world), dist_max(ppf, world)
     _check_status(pf, "prefill chunks")
     pf_tflops = pf.work["chunk_flops"] / (ppf * 1e-3) / 1e12
@@ -719,8 +727,10 @@ def run_gpu_arm(args):
         "step_tflops": pf.work["chunk_flops"] / (pms * 1e-3) / 1e12,
         "peak_tflops": bf16_peak[0], "peak_source": bf16_peak[1],
         "flops": pf.work["chunk_flops"],
-        "timed": "tflops: flops / median event time of the tensor-core prefill kernel; "
-                 "ms_per_step: pa_cache_write + pa_forward (plan, prefill kernel); L2 "
+        "timed": "tflops: flops / median event time of the tensor-core prefill kernel, timed "
+                 "in a second loop with the prefill kernel on the caller's stream; "
+                 "ms_per_step: pa_cache_write + pa_forward (plan, prefill kernel; default "
+                 "side-stream schedule); L2 "
                  + StepRunner.FLUSH_TEXT + "; flops = 4 x D x Hq x visible (query, key) pairs",
     }
     del pf
@@ -728,7 +738,7 @@ def run_gpu_arm(args):
 
     # ---- one long chunk: the tensor-core kernel in its steady state (56 KV tiles a unit)
     pl = StepRunner("long_prefill_chunk", seed_offset=seed_off)
-    lms, _, lpf = pl.time_device(half, args.warmup, world, flush=True)
+    lms, _, lpf = pl.time_device(half, args.warmup, world, flush=True, serial_kernels=True)
     lms, lpf = dist_max(lms, world), dist_max(lpf, world)
     _check_status(pl, "long prefill")
     pl_tflops = pl.work["chunk_flops"] / (lpf * 1e-3) / 1e12
@@ -748,7 +758,7 @@ def run_gpu_arm(args):
     del pl
     torch.cuda.empty_cache()
     plf = StepRunner("long_prefill_chunk", seed_offset=seed_off, fp8_scales=(0.01, 0.01))
-    lfms, _, lfpf = plf.time_device(half, args.warmup, world, flush=True)
+    lfms, _, lfpf = plf.time_device(half, args.warmup, world, flush=True, serial_kernels=True)
     lfms, lfpf = dist_max(lfms, world), dist_max(lfpf, world)
     _check_status(plf, "long prefill, fp8")
     prefill_long_info["fp8_kv"] = {
@@ -764,7 +774,7 @@ def run_gpu_arm(args):
 
     # ---- short chunks after long prompts: prefill units split over their KV
     lp = StepRunner("long_prior_chunks", seed_offset=seed_off)
-    pps, _, ppk = lp.time_device(half, args.warmup, world, flush=True)
+    pps, _, ppk = lp.time_device(half, args.warmup, world, flush=True, serial_kernels=True)
     pps, ppk = dist_max(pps, world), dist_max(ppk, world)
     _check_status(lp, "long-prior chunks")
     lpw = lp.work
@@ -780,6 +790,8 @@ def run_gpu_arm(args):
                  "read + q + out + block tables)",
         "algorithmic_bytes": lpw["chunk_bytes"], "flops": lpw["chunk_flops"],
         "l2": StepRunner.FLUSH_TEXT,
+        "timed": "prefill kernel: median event time in a second loop with the prefill kernel on "
+                 "the caller's stream",
     }
     del lp
     torch.cuda.empty_cache()
