@@ -71,14 +71,15 @@ struct PfCfg {
   static constexpr int kVBlockBytes = kBlockSize * 128 * (D / 64);
   static constexpr int kKGroupBytes = 8 * 128 * (D / 64);
   static constexpr int kSmemBytes = kVOff + 2 * kTileBytes + 1024;  // + alignment slack
-  // FP8 cache: a tile's codes are staged by TMA, [block][16 rows][D bytes],
-  // and widened from there into the K / V buffers above: two staging buffers
-  // for K, one for V at D = 128 (two at D = 64), so the copies run ahead
+  // FP8 cache: a tile's codes are copied by TMA, [16 rows][D bytes] per
+  // block, and widened to f16 in the layouts above.  K codes go to two
+  // staging buffers ([block][16 rows][D bytes]), so a copy runs two tiles
+  // ahead of its widening; V codes go into the upper half of each block's
+  // region of the V buffer they are widened into (one warp widens a block in
+  // place), so a V copy starts as soon as PV has read that buffer.
   static constexpr int kCodeBytes = kTileN * D;
-  static constexpr int kVStages = D == 64 ? 2 : 1;
   static constexpr int kKCodeOff = kVOff + 2 * kTileBytes;
-  static constexpr int kVCodeOff = kKCodeOff + 2 * kCodeBytes;
-  static constexpr int kSmemBytesF8 = kVCodeOff + kVStages * kCodeBytes + 1024;
+  static constexpr int kSmemBytesF8 = kKCodeOff + 2 * kCodeBytes + 1024;
   // S0, S1 (consecutive tiles) at 0 / 128, each tile's P (bf16 pairs) over the
   // first 64 columns of its S once read; O at 256
   static constexpr int kTmemCols = 512;
@@ -101,9 +102,10 @@ enum Bar : int {
   kKFirst = 6,      // [2] the unit's first two K tiles landed (TMA)
   kSFull = 8,       // [2] S = Q K^T done (MMA commit); also frees the K buffer
   kGo = 10,         // [2] tile t: P written and S read (8 softmax warps), V of t landed
-                    //     (V loader), K of t + 2 landed or none due (K loader)
+                    //     (V loader), K of t + 2 landed or none due (K loader); FP8 cache:
+                    //     the softmax warps alone, who also widen K of t + 2 and V of t
   kVLand = 12,      // [2] V tile landed, for a tile whose last block the V loader trims;
-                    //     FP8 cache: codes landed in V staging buffer 0 / 1
+                    //     FP8 cache: V codes landed in V buffer 0 / 1
   kPVDone = 14,     // [2] O += P V done (MMA commit); frees the V buffer
   kMx = 16,         // [2] both halves of each row published their maximum (8 warps)
   kMlFull = 18,     // row sums of both halves published (8 warps)
@@ -114,7 +116,8 @@ enum Bar : int {
   kPieceLast = 23,  // ... and whether it was the tile's last piece decided (warp 0)
   kQLand = 24,      // FP8 cache: the bf16 Q tile landed (TMA), before its f16 conversion
   kKLand = 25,      // [2] FP8 cache: codes landed in K staging buffer 0 / 1 (TMA)
-  kNumBars = 27
+  kKStFree = 27,    // [2] FP8 cache: K staging buffer 0 / 1 widened by the 8 softmax warps
+  kNumBars = 29
 };
 
 struct UnitInfo {
@@ -191,11 +194,12 @@ __device__ __forceinline__ bool wait_bar(uint32_t bar, uint32_t parity, volatile
 }
 
 // Arrivals that complete a phase of each barrier.
+template <bool F8>
 __device__ __forceinline__ uint32_t bar_count(int i) {
   if (i == kUnitEmpty || i == kUnitEmpty + 1) return 10;  // 8 softmax warps, MMA, V loader
-  if (i == kGo || i == kGo + 1) return 10;  // 8 softmax warps, V loader, K loader
+  if (i == kGo || i == kGo + 1) return F8 ? 8 : 10;  // 8 softmax warps (+ V and K loaders)
   if (i == kMx || i == kMx + 1 || i == kMlFull || i == kMlRead || i == kOFree ||
-      i == kPieceDone)
+      i == kPieceDone || i == kKStFree || i == kKStFree + 1)
     return 8;
   // kQLand, kKLand: TMA (arrive + bytes); kQFull, kKFirst also take the
   // loader's plain arrival after an FP8 conversion: one arrival either way
@@ -236,6 +240,68 @@ __device__ __forceinline__ uint32_t e4m3x2_f16x2(uint32_t codes16) {
   return r;
 }
 
+// FP8: widen blocks b .. b + NB - 1 of a tile of codes at src ([16 rows][D
+// bytes] per block, blocks src_stride bytes apart) to f16 at dst, in the
+// layout the bf16 TMA copy produces (K: [block][8-row group][64-column half][8 rows][128 B]; V:
+// [block][64-column half][16 rows][128 B]; 16-byte chunks XOR-swizzled by
+// row); one warp.  A lane converts 16-code chunks (two 16-byte f16 chunks);
+// at D = 128 the lanes with the second column half take the neighbouring row
+// (parity flipped), so each 8 lanes' loads and stores hit 8 distinct 16-byte
+// bank groups.  NB = 2 overlaps two blocks' loads.  Every code is loaded
+// before any store, so a block's codes may sit inside its own output.
+template <int D, int NB>
+__device__ __forceinline__ void widen_blocks(uint32_t src, uint32_t src_stride, uint32_t dst,
+                                             bool is_v, int b, int lane) {
+  using C = PfCfg<D>;
+  constexpr int kRowChunks = D / 16;                 // 16-code chunks per row: 8 or 4
+  constexpr int kRowsPerStep = 32 / kRowChunks;      // rows a warp covers per step: 4 or 8
+  constexpr int kSteps = kBlockSize / kRowsPerStep;  // steps per block: 4 or 2
+  const int c = lane % kRowChunks;
+  const int rr = (lane / kRowChunks) ^ (D == 128 ? (c >> 2) & 1 : 0);
+  const int half = (c * 16) >> 6;
+  uint32_t soff[kSteps][2];  // store offsets within a block
+#pragma unroll
+  for (int j = 0; j < kSteps; ++j) {
+    const int t = j * kRowsPerStep + rr;
+#pragma unroll
+    for (int o = 0; o < 2; ++o) {
+      const int ch = (2 * c + o) & 7;
+      const uint32_t sw = static_cast<uint32_t>((ch ^ (t & 7)) << 4);
+      soff[j][o] = is_v ? half * (kBlockSize * 128) + t * 128 + sw
+                        : (t >> 3) * C::kKGroupBytes + half * 1024 + (t & 7) * 128 + sw;
+    }
+  }
+  const uint32_t lsrc = src + rr * D + c * 16;
+  uint4 cv[NB][kSteps];
+#pragma unroll
+  for (int bb = 0; bb < NB; ++bb)
+#pragma unroll
+    for (int j = 0; j < kSteps; ++j)
+      asm volatile("ld.shared.v4.b32 {%0,%1,%2,%3}, [%4];\n"
+                   : "=r"(cv[bb][j].x), "=r"(cv[bb][j].y), "=r"(cv[bb][j].z), "=r"(cv[bb][j].w)
+                   : "r"(lsrc + (b + bb) * src_stride + j * kRowsPerStep * D)
+                   : "memory");
+  __syncwarp();
+#pragma unroll
+  for (int bb = 0; bb < NB; ++bb)
+#pragma unroll
+    for (int j = 0; j < kSteps; ++j) {
+      const uint32_t wd[4] = {cv[bb][j].x, cv[bb][j].y, cv[bb][j].z, cv[bb][j].w};
+      uint32_t h[8];
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        h[2 * e] = e4m3x2_f16x2(wd[e] & 0xffffu);
+        h[2 * e + 1] = e4m3x2_f16x2(wd[e] >> 16);
+      }
+      const uint32_t base = dst + (b + bb) * C::kVBlockBytes;
+#pragma unroll
+      for (int o = 0; o < 2; ++o)
+        asm volatile("st.shared.v4.b32 [%0], {%1,%2,%3,%4};\n" ::"r"(base + soff[j][o]),
+                     "r"(h[4 * o]), "r"(h[4 * o + 1]), "r"(h[4 * o + 2]), "r"(h[4 * o + 3])
+                     : "memory");
+    }
+}
+
 }  // namespace
 
 // F8: the cache holds E4M3 codes.  They are copied by TMA into staging
@@ -267,7 +333,7 @@ __global__ void __launch_bounds__(kPfThreads, 1)
   auto bar = [&](int i) { return smem_u32(&bars[i]); };
 
   if (tid == 0) {
-    for (int i = 0; i < kNumBars; ++i) mbar_init(bar(i), bar_count(i));
+    for (int i = 0; i < kNumBars; ++i) mbar_init(bar(i), bar_count<F8>(i));
     s_abort = 0;
     mbar_fence_init();
   }
@@ -296,12 +362,16 @@ __global__ void __launch_bounds__(kPfThreads, 1)
       ph = -1;
     }
     if constexpr (F8) {
-      // the codes, [block][16 rows][D bytes], into the staging buffer at dst
+      // the codes, [16 rows][D bytes] per block: K into the staging buffer
+      // at dst, V into the upper half of each block's region of the V
+      // buffer at dst
       if (lane == 0) mbar_arrive_expect_tx(full, C::kCodeBytes);
       __syncwarp();
       if (lane < kTileN / kBlockSize) {
         const int coord = ph < 0 ? p.num_blocks : ph;
-        tma_load_3d(dst + lane * kBlockSize * D, is_v ? &maps.v : &maps.k, 0, 0,
+        const uint32_t d = is_v ? dst + lane * C::kVBlockBytes + C::kVBlockBytes / 2
+                                : dst + lane * kBlockSize * D;
+        tma_load_3d(d, is_v ? &maps.v : &maps.k, 0, 0,
                     coord * kBlockSize * p.num_kv_heads + u.g, full);
       }
       return;
@@ -329,63 +399,12 @@ __global__ void __launch_bounds__(kPfThreads, 1)
                    : "memory");
     }
   };
-  // FP8: widen a staged tile of codes at src to f16 at dst, in the layout the
-  // bf16 TMA copy produces (K: [block][8-row group][64-column half][8 rows]
-  // [128 B]; V: [block][64-column half][16 rows][128 B]; 16-byte chunks
-  // XOR-swizzled by row).  A lane converts 16-code chunks (two 16-byte f16
-  // chunks); at D = 128 the lanes with the second column half take the
-  // neighbouring row (parity flipped), so each 8 lanes' loads and stores hit
-  // 8 distinct 16-byte bank groups.  Two blocks per step, for overlap.
-  auto widen_tile = [&](uint32_t src, uint32_t dst, bool is_v) {
-    constexpr int kRowChunks = D / 16;                 // 16-code chunks per row: 8 or 4
-    constexpr int kRowsPerStep = 32 / kRowChunks;      // rows a warp covers per step: 4 or 8
-    constexpr int kSteps = kBlockSize / kRowsPerStep;  // steps per block: 4 or 2
-    const int c = lane % kRowChunks;
-    const int rr = (lane / kRowChunks) ^ (D == 128 ? (c >> 2) & 1 : 0);
-    const int half = (c * 16) >> 6;
-    uint32_t soff[kSteps][2];  // store offsets within a block
-#pragma unroll
-    for (int j = 0; j < kSteps; ++j) {
-      const int t = j * kRowsPerStep + rr;
-#pragma unroll
-      for (int o = 0; o < 2; ++o) {
-        const int ch = (2 * c + o) & 7;
-        const uint32_t sw = static_cast<uint32_t>((ch ^ (t & 7)) << 4);
-        soff[j][o] = is_v ? half * (kBlockSize * 128) + t * 128 + sw
-                          : (t >> 3) * C::kKGroupBytes + half * 1024 + (t & 7) * 128 + sw;
-      }
-    }
-    const uint32_t lsrc = src + rr * D + c * 16;
+  // FP8: widen a tile of codes at src (blocks src_stride bytes apart) to f16
+  // at dst (one warp)
+  auto widen_tile = [&](uint32_t src, uint32_t src_stride, uint32_t dst, bool is_v) {
 #pragma unroll 1
-    for (int b = 0; b < kTileN / kBlockSize; b += 2) {
-      uint4 cv[2][kSteps];
-#pragma unroll
-      for (int bb = 0; bb < 2; ++bb)
-#pragma unroll
-        for (int j = 0; j < kSteps; ++j)
-          asm volatile("ld.shared.v4.b32 {%0,%1,%2,%3}, [%4];\n"
-                       : "=r"(cv[bb][j].x), "=r"(cv[bb][j].y), "=r"(cv[bb][j].z), "=r"(cv[bb][j].w)
-                       : "r"(lsrc + (b + bb) * kBlockSize * D + j * kRowsPerStep * D)
-                       : "memory");
-#pragma unroll
-      for (int bb = 0; bb < 2; ++bb)
-#pragma unroll
-        for (int j = 0; j < kSteps; ++j) {
-          const uint32_t wd[4] = {cv[bb][j].x, cv[bb][j].y, cv[bb][j].z, cv[bb][j].w};
-          uint32_t h[8];
-#pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            h[2 * e] = e4m3x2_f16x2(wd[e] & 0xffffu);
-            h[2 * e + 1] = e4m3x2_f16x2(wd[e] >> 16);
-          }
-          const uint32_t base = dst + (b + bb) * C::kVBlockBytes;
-#pragma unroll
-          for (int o = 0; o < 2; ++o)
-            asm volatile("st.shared.v4.b32 [%0], {%1,%2,%3,%4};\n" ::"r"(base + soff[j][o]),
-                         "r"(h[4 * o]), "r"(h[4 * o + 1]), "r"(h[4 * o + 2]), "r"(h[4 * o + 3])
-                         : "memory");
-        }
-    }
+    for (int b = 0; b < kTileN / kBlockSize; b += 2)
+      widen_blocks<D, 2>(src, src_stride, dst, is_v, b, lane);
   };
   // FP8: the landed bf16 Q tile to f16, in place (an element keeps its slot)
   auto q_to_f16 = [&]() {
@@ -426,8 +445,11 @@ __global__ void __launch_bounds__(kPfThreads, 1)
     // arrivals (one per tile of that parity), gk: the last one that carried
     // a copy, plus one
     uint32_t nf[2] = {0, 0}, sw[2] = {0, 0}, ga[2] = {0, 0}, gk[2] = {0, 0}, nq = 0;
-    // FP8: code copies issued / waited (copy i: staging buffer i & 1, phase i >> 1)
-    uint32_t kc = 0, kw = 0;
+    // FP8: code copies issued (copy i: staging buffer i & 1, phase i >> 1); per
+    // staging buffer, softmax widenings so far (kStFree phases) and whether
+    // its current codes are one of them, not yet waited for
+    uint32_t kc = 0, ks0 = 0, ks1 = 0;
+    bool kp0 = false, kp1 = false;
     bool q_wait = false;  // FP8: the Q copy not yet waited for
     // The next unit is claimed and published while the current one's last
     // tiles run (before its trailing kGo arrivals), so its metadata loads,
@@ -491,18 +513,33 @@ __global__ void __launch_bounds__(kPfThreads, 1)
     if (claim(0, u)) for (int uc = 0;; ++uc) {
       if (u.r < 0) break;
       int ph = tile_phys(u, tile_of(u, 0));
-      // FP8: the codes of the unit's first two tiles into the staging buffers
-      // (free: every copy issued before has been widened), ahead of Q
-      auto copy_codes = [&](int sq) {
-        copy_kv_tile(u, tile_of(u, sq), ph, false, sbase + C::kKCodeOff + (kc & 1) * C::kCodeBytes,
-                     bar(kKLand + (kc & 1)));
+      // FP8: K codes of tile sq (tiles in order) into staging buffer kc & 1,
+      // once the softmax warps have widened what it held, if theirs.  The
+      // loader widens a unit's first two tiles itself (they start the unit);
+      // the softmax warps widen tile sq >= 2 while they work on tile sq - 2.
+      const uint32_t c0 = kc;
+      auto copy_codes = [&](int sq) -> bool {
+        const uint32_t b = kc & 1;
+        if ((b ? kp1 : kp0) &&
+            !wait_bar(bar(kKStFree + b), ((b ? ks1 : ks0) - 1) & 1, abort, p.status))
+          return false;
+        copy_kv_tile(u, tile_of(u, sq), ph, false, sbase + C::kKCodeOff + b * C::kCodeBytes,
+                     bar(kKLand + b));
+        const bool soft = sq >= 2;
+        if (b) {
+          kp1 = soft;
+          ks1 += soft;
+        } else {
+          kp0 = soft;
+          ks0 += soft;
+        }
         ++kc;
         if (sq + 1 < u.n_kv) ph = tile_phys(u, tile_of(u, sq + 1));
+        return true;
       };
-      if constexpr (F8) {
-        copy_codes(0);
-        if (u.n_kv > 1) copy_codes(1);
-      }
+      bool ok = true;
+      if constexpr (F8) ok = copy_codes(0) && (u.n_kv < 2 || copy_codes(1));  // ahead of Q
+      if (!ok) break;
       // Q tile: rows (position, head) of 128/G tokens x G heads, one box per 64 columns
       if (uc > 0 && !wait_bar(bar(kQEmpty), (uc - 1) & 1, abort, p.status)) break;
       const uint32_t q_bar = F8 ? bar(kQLand) : bar(kQFull);
@@ -515,7 +552,6 @@ __global__ void __launch_bounds__(kPfThreads, 1)
       }
       ++nq;
       q_wait = F8;
-      bool ok = true;
       if constexpr (F8) {  // Q to f16 while the codes are on their way
         if (!wait_bar(bar(kQLand), (nq - 1) & 1, abort, p.status)) {
           ok = false;
@@ -525,45 +561,56 @@ __global__ void __launch_bounds__(kPfThreads, 1)
           if (lane == 0) mbar_arrive(bar(kQFull));
         }
       }
-      // K of tile sq goes into buffer w = sq & 1.  The first two were freed
-      // by the previous unit (its last S of each parity was waited below);
-      // later ones wait for S of tile sq - 2 and then count as that tile's
-      // kGo arrival (bytes included; FP8: a plain arrival after widening)
-      for (int sq = 0; ok && sq < u.n_kv; ++sq) {
-        const int w = sq & 1;
-        uint32_t full = bar(kKFirst + w);
-        if (sq >= 2) {
-          if (!wait_bar(bar(kSFull + w), sw[w] & 1, abort, p.status)) { ok = false; break; }
-          ++sw[w];
-          full = bar(kGo + w);
-          gk[w] = ++ga[w];
-        } else {
-          ++nf[w];
-        }
-        const uint32_t kbuf = sbase + C::kKOff + w * C::kTileBytes;
-        if constexpr (F8) {
-          const uint32_t b = kw & 1;
-          if (!wait_bar(bar(kKLand + b), (kw >> 1) & 1, abort, p.status)) { ok = false; break; }
-          ++kw;
-          widen_tile(sbase + C::kKCodeOff + b * C::kCodeBytes, kbuf, false);
+      if constexpr (F8) {
+        // the first two tiles into K buffers 0 / 1 (freed by the previous
+        // unit: its last S of each parity was waited below), then every
+        // later tile's codes as their staging buffer frees up
+        for (int sq = 0; ok && sq < min(2, u.n_kv); ++sq) {
+          const uint32_t i = c0 + sq;
+          ++nf[sq];
+          if (!wait_bar(bar(kKLand + (i & 1)), (i >> 1) & 1, abort, p.status)) { ok = false; break; }
+          widen_tile(sbase + C::kKCodeOff + (i & 1) * C::kCodeBytes, kBlockSize * D,
+                     sbase + C::kKOff + sq * C::kTileBytes, false);
           fence_proxy_async_smem();  // the generic-proxy writes, before the tensor cores read them
           __syncwarp();
-          if (lane == 0) mbar_arrive(full);
-          if (sq + 2 < u.n_kv) copy_codes(sq + 2);  // into the staging buffer just read
-          continue;
+          if (lane == 0) mbar_arrive(bar(kKFirst + sq));
+          if (sq + 2 < u.n_kv && !copy_codes(sq + 2)) ok = false;  // into the buffer just read
         }
-        copy_kv_tile(u, tile_of(u, sq), ph, false, kbuf, full);
-        if (sq + 1 < u.n_kv) ph = tile_phys(u, tile_of(u, sq + 1));
+        for (int sq = 4; ok && sq < u.n_kv; ++sq)
+          if (!copy_codes(sq)) ok = false;
+        for (int t = 0; t < u.n_kv - 2; ++t) ++sw[t & 1];  // S phases not waited for
+      } else {
+        // K of tile sq goes into buffer w = sq & 1.  The first two were freed
+        // by the previous unit (its last S of each parity was waited below);
+        // later ones wait for S of tile sq - 2 and then count as that tile's
+        // kGo arrival (bytes included)
+        for (int sq = 0; ok && sq < u.n_kv; ++sq) {
+          const int w = sq & 1;
+          uint32_t full = bar(kKFirst + w);
+          if (sq >= 2) {
+            if (!wait_bar(bar(kSFull + w), sw[w] & 1, abort, p.status)) { ok = false; break; }
+            ++sw[w];
+            full = bar(kGo + w);
+            gk[w] = ++ga[w];
+          } else {
+            ++nf[w];
+          }
+          copy_kv_tile(u, tile_of(u, sq), ph, false, sbase + C::kKOff + w * C::kTileBytes, full);
+          if (sq + 1 < u.n_kv) ph = tile_phys(u, tile_of(u, sq + 1));
+        }
       }
       UnitInfo nu;
       if (ok) ok = claim(uc + 1, nu);
-      // tiles with no K two places on: a plain kGo arrival once their S is done
+      // the unit's last two S done (K buffers free for the next unit); bf16:
+      // tiles with no K two places on make a plain kGo arrival then
       for (int t = max(0, u.n_kv - 2); ok && t < u.n_kv; ++t) {
         const int w = t & 1;
         if (!wait_bar(bar(kSFull + w), sw[w] & 1, abort, p.status)) { ok = false; break; }
         ++sw[w];
-        ++ga[w];
-        warp_arrive(bar(kGo + w));
+        if constexpr (!F8) {
+          ++ga[w];
+          warp_arrive(bar(kGo + w));
+        }
       }
       if (!ok) break;
       u = nu;
@@ -571,7 +618,9 @@ __global__ void __launch_bounds__(kPfThreads, 1)
     if (*abort) {  // let every copy issued land before the CTA ends
       if constexpr (F8) {
         if (q_wait) drain_wait(bar(kQLand), (nq - 1) & 1);
-        for (uint32_t i = kw; i < kc; ++i) drain_wait(bar(kKLand + (i & 1)), (i >> 1) & 1);
+        // the last copy into each staging buffer (one at most is in flight per buffer)
+        for (uint32_t i = kc > 2 ? kc - 2 : 0; i < kc; ++i)
+          drain_wait(bar(kKLand + (i & 1)), (i >> 1) & 1);
       } else {
         if (nq > 0) drain_wait(bar(kQFull), (nq - 1) & 1);
         for (int w = 0; w < 2; ++w) {
@@ -588,9 +637,8 @@ __global__ void __launch_bounds__(kPfThreads, 1)
     uint32_t nv[2] = {0, 0}, gv[2] = {0, 0}, nl[2] = {0, 0};
     bool landing = false;  // a kVLand copy not yet waited for
     int land_w = 0;
-    // FP8: code copies issued / waited (copy i: staging buffer i % kVStages)
-    constexpr uint32_t NS = C::kVStages;
-    uint32_t vc = 0, vw = 0;
+    bool vland = false;  // FP8: a code copy into V buffer vland_w not yet drained
+    int vland_w = 0;
     for (int uc = 0;; ++uc) {
       const int slot = uc & 1;
       if (!wait_bar(bar(kUnitFull + slot), (uc >> 1) & 1, abort, p.status)) break;
@@ -598,67 +646,64 @@ __global__ void __launch_bounds__(kPfThreads, 1)
       warp_arrive(bar(kUnitEmpty + slot));
       if (u.r < 0) break;
       int ph = tile_phys(u, tile_of(u, 0));
-      auto copy_codes = [&](int sq) {  // FP8: into staging buffer vc % NS
-        copy_kv_tile(u, tile_of(u, sq), ph, true, sbase + C::kVCodeOff + (vc % NS) * C::kCodeBytes,
-                     bar(kVLand + vc % NS));
-        ++vc;
-        if (sq + 1 < u.n_kv) ph = tile_phys(u, tile_of(u, sq + 1));
-      };
-      if constexpr (F8)
-        for (int sq = 0; sq < min(static_cast<int>(NS), u.n_kv); ++sq) copy_codes(sq);
       bool ok = true;
-      for (int sq = 0; sq < u.n_kv; ++sq) {
-        const int w = sq & 1;
-        const int kt = tile_of(u, sq);
-        // V buffer w is free once PV of the previous tile of that parity is done
-        if (nv[w] > 0 && !wait_bar(bar(kPVDone + w), (nv[w] - 1) & 1, abort, p.status)) {
-          ok = false;
-          break;
-        }
-        const uint32_t vb = sbase + C::kVOff + w * C::kTileBytes;
-        if constexpr (F8) {
-          // widened to f16 from the staging buffer; rows past the unit's last
-          // key (unwritten slots) become zeros, so p = 0 never meets a NaN
-          const uint32_t b = vw % NS;
-          if (!wait_bar(bar(kVLand + b), (vw / NS) & 1, abort, p.status)) { ok = false; break; }
-          ++vw;
-          widen_tile(sbase + C::kVCodeOff + b * C::kCodeBytes, vb, true);
-          const int r0 = u.kv_end - kt * kTileN;
-          if (r0 < kTileN) {
-            __syncwarp();
-            zero_v_rows(vb, r0, (r0 + kBlockSize - 1) & ~(kBlockSize - 1));
+      if constexpr (F8) {
+        // each tile's codes into V buffer w = sq & 1 once PV of the previous
+        // tile of that parity is done; the softmax warps widen them there
+        for (int sq = 0; sq < u.n_kv; ++sq) {
+          const int w = sq & 1;
+          if (nv[w] > 0 && !wait_bar(bar(kPVDone + w), (nv[w] - 1) & 1, abort, p.status)) {
+            ok = false;
+            break;
           }
-          fence_proxy_async_smem();
-          warp_arrive(bar(kGo + w));
-          if (sq + static_cast<int>(NS) < u.n_kv) copy_codes(sq + NS);
+          copy_kv_tile(u, tile_of(u, sq), ph, true, sbase + C::kVOff + w * C::kTileBytes,
+                       bar(kVLand + w));
           ++nv[w];
-          continue;
-        } else if (kt != u.kt0 + u.n_kv - 1 || (u.kv_end & (kBlockSize - 1)) == 0) {
-          copy_kv_tile(u, kt, ph, true, vb, bar(kGo + w));  // this tile's kGo arrival
-          gv[w] = nv[w] + 1;
-        } else {
-          // the unit's last block is partial: its rows past the last key
-          // (unwritten slots) are zeroed once the tile has landed, so that
-          // p = 0 never meets a NaN there; then the kGo arrival
-          copy_kv_tile(u, kt, ph, true, vb, bar(kVLand + w));
-          landing = true;
-          land_w = w;
-          if (!wait_bar(bar(kVLand + w), nl[w] & 1, abort, p.status)) { ok = false; break; }
-          landing = false;
-          ++nl[w];
-          const int r0 = u.kv_end - kt * kTileN;
-          zero_v_rows(vb, r0, (r0 + kBlockSize - 1) & ~(kBlockSize - 1));
-          fence_proxy_async_smem();
-          warp_arrive(bar(kGo + w));
+          vland = true;
+          vland_w = w;
+          if (sq + 1 < u.n_kv) ph = tile_phys(u, tile_of(u, sq + 1));
         }
-        ++nv[w];
-        if (sq + 1 < u.n_kv) ph = tile_phys(u, tile_of(u, sq + 1));
+      } else {
+        for (int sq = 0; sq < u.n_kv; ++sq) {
+          const int w = sq & 1;
+          const int kt = tile_of(u, sq);
+          // V buffer w is free once PV of the previous tile of that parity is done
+          if (nv[w] > 0 && !wait_bar(bar(kPVDone + w), (nv[w] - 1) & 1, abort, p.status)) {
+            ok = false;
+            break;
+          }
+          const uint32_t vb = sbase + C::kVOff + w * C::kTileBytes;
+          if (kt != u.kt0 + u.n_kv - 1 || (u.kv_end & (kBlockSize - 1)) == 0) {
+            copy_kv_tile(u, kt, ph, true, vb, bar(kGo + w));  // this tile's kGo arrival
+            gv[w] = nv[w] + 1;
+          } else {
+            // the unit's last block is partial: its rows past the last key
+            // (unwritten slots) are zeroed once the tile has landed, so that
+            // p = 0 never meets a NaN there; then the kGo arrival
+            copy_kv_tile(u, kt, ph, true, vb, bar(kVLand + w));
+            landing = true;
+            land_w = w;
+            if (!wait_bar(bar(kVLand + w), nl[w] & 1, abort, p.status)) { ok = false; break; }
+            landing = false;
+            ++nl[w];
+            const int r0 = u.kv_end - kt * kTileN;
+            zero_v_rows(vb, r0, (r0 + kBlockSize - 1) & ~(kBlockSize - 1));
+            fence_proxy_async_smem();
+            warp_arrive(bar(kGo + w));
+          }
+          ++nv[w];
+          if (sq + 1 < u.n_kv) ph = tile_phys(u, tile_of(u, sq + 1));
+        }
       }
       if (!ok) break;
     }
     if (*abort) {
       if (landing) drain_wait(bar(kVLand + land_w), nl[land_w] & 1);
-      for (uint32_t i = vw; i < vc; ++i) drain_wait(bar(kVLand + i % NS), (i / NS) & 1);
+      // FP8: the last code copy into each V buffer
+      if (vland) {
+        drain_wait(bar(kVLand + vland_w), (nv[vland_w] - 1) & 1);
+        if (nv[vland_w ^ 1] > 0) drain_wait(bar(kVLand + (vland_w ^ 1)), (nv[vland_w ^ 1] - 1) & 1);
+      }
       for (int w = 0; w < 2; ++w)
         if (gv[w] > 0) drain_wait(bar(kGo + w), (gv[w] - 1) & 1, kGoDrainLimit);
     }
@@ -773,6 +818,7 @@ __global__ void __launch_bounds__(kPfThreads, 1)
     const int Hq = p.num_q_heads;
     __nv_bfloat16* out = static_cast<__nv_bfloat16*>(p.out);
     uint32_t nb0 = 0, nb1 = 0;  // tiles per buffer parity so far (all units)
+    uint32_t cb = 0;            // FP8: tiles of earlier units (the code copy index of tile 0)
     uint32_t npieces = 0;       // split pieces finished so far
     const int Hkv = p.num_kv_heads;
     // Merge of a split unit, by its last piece: this thread's row i and its
@@ -909,6 +955,34 @@ __global__ void __launch_bounds__(kPfThreads, 1)
           PA_TMEM_ST32(tmem_s + w * 32, pw);
           l_part += (ps4[0] + ps4[1]) + (ps4[2] + ps4[3]);
         }
+        if constexpr (F8) {
+          // this warp's 16-token block of K(t + 2), from its staging buffer
+          // into K buffer b (S(t), its last reader, is done), and of V(t), in
+          // place in V buffer b (PV(t - 2), its last reader, finished before
+          // S(t)); V rows past the unit's last key (unwritten slots) become
+          // zeros, so p = 0 never meets a NaN there
+          if (t + 2 < u.n_kv) {
+            const uint32_t ci = cb + t + 2;
+            if (!wait_bar(bar(kKLand + (ci & 1)), (ci >> 1) & 1, abort, p.status)) {
+              ok = false;
+              break;
+            }
+            widen_blocks<D, 1>(sbase + C::kKCodeOff + (ci & 1) * C::kCodeBytes, kBlockSize * D,
+                               sbase + C::kKOff + b * C::kTileBytes, false, warp, lane);
+            warp_arrive(bar(kKStFree + (ci & 1)));
+          }
+          {
+            if (!wait_bar(bar(kVLand + b), nb & 1, abort, p.status)) { ok = false; break; }
+            const uint32_t vb = sbase + C::kVOff + b * C::kTileBytes;
+            widen_blocks<D, 1>(vb + C::kVBlockBytes / 2, C::kVBlockBytes, vb, true, warp, lane);
+            const int r0 = u.kv_end - kt * kTileN;
+            if (r0 < kTileN && (r0 >> 4) == warp) {
+              __syncwarp();
+              zero_v_rows(vb, r0, (r0 + kBlockSize - 1) & ~(kBlockSize - 1));
+            }
+          }
+          fence_proxy_async_smem();  // generic-proxy writes, before the tensor cores read them
+        }
         // rescale this group's O columns in rows whose maximum moved, once
         // PV(t - 1) is done (not on the unit's first tile: PV(0) overwrites O)
         if (t > 0 && __any_sync(0xffffffffu, f != 1.f)) {
@@ -933,6 +1007,7 @@ __global__ void __launch_bounds__(kPfThreads, 1)
         if (b) ++nb1; else ++nb0;
       }
       if (!ok) break;
+      cb += u.n_kv;
 
       // ---- both halves' row sums (traded while the last PV runs), then
       // this group's half of the O columns
