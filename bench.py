@@ -454,12 +454,14 @@ class StepRunner:
     def time_device(self, steps: int, warmup: int, world: int, clocks: ClockSampler | None = None,
                     flush: bool = False, serial_kernels: bool = False):
         """Inputs resident in HBM; returns (ms per step, decode-kernel ms per launch,
-        prefill-kernel ms per launch or None), the kernel times being medians over
-        the launches.  The steps are timed in one loop with no events inside a
-        step; the kernels are timed in a second loop with events around each
-        (events between the plan and the decode kernel would cost the step their
-        launch overlap).  With flush, L2 is flushed before every step, outside
-        the timed events."""
+        prefill-kernel ms per launch or None), the kernel times being means over
+        the launches (the event clock ticks in ~2 us steps; a launch starts at a
+        random phase of the tick, so the mean of many launches resolves what
+        one reading, or a median of them, rounds away).  The steps are timed in
+        one loop with no events inside a step; the kernels are timed in a second
+        loop with events around each (events between the plan and the decode
+        kernel would cost the step their launch overlap).  With flush, L2 is
+        flushed before every step, outside the timed events."""
         torch, P = self.torch, self.P
         for _ in range(warmup):
             self.step()
@@ -495,8 +497,8 @@ class StepRunner:
             P.pa_set_profile_events(None, None)
             P.pa_set_prefill_profile_events(None, None)
             if kernel_events:
-                dec = statistics.median(a.elapsed_time(b) for a, b in evs)
-                pf = statistics.median(a.elapsed_time(b) for a, b in pevs) if has_prefill else None
+                dec = statistics.fmean(a.elapsed_time(b) for a, b in evs)
+                pf = statistics.fmean(a.elapsed_time(b) for a, b in pevs) if has_prefill else None
                 return dec, pf
             return sum(a.elapsed_time(b) for a, b in steps_ev) / steps
 
@@ -686,7 +688,7 @@ def run_gpu_arm(args):
         "timed": "ms_per_step: pa_cache_write + pa_forward back to back with no events inside a "
                  "step (prefill kernel on the library side stream beside the decode kernel); "
                  "serial_ms_per_step: the same with pa_set_prefill_overlap(0) (prefill kernel "
-                 "on the caller's stream before the decode kernel); kernel times: medians of "
+                 "on the caller's stream before the decode kernel); kernel times: means of "
                  "events around each kernel in a second loop (overlapped, the prefill kernel's "
                  "stop event waits for CTAs that only start when decode CTAs leave, so only the "
                  "serial prefill time is reported); decode_alone: the 192 decode requests as a "
@@ -727,7 +729,7 @@ def run_gpu_arm(args):
         "step_tflops": pf.work["chunk_flops"] / (pms * 1e-3) / 1e12,
         "peak_tflops": bf16_peak[0], "peak_source": bf16_peak[1],
         "flops": pf.work["chunk_flops"],
-        "timed": "tflops: flops / median event time of the tensor-core prefill kernel, timed "
+        "timed": "tflops: flops / mean event time of the tensor-core prefill kernel, timed "
                  "in a second loop with the prefill kernel on the caller's stream; "
                  "ms_per_step: pa_cache_write + pa_forward (plan, prefill kernel; default "
                  "side-stream schedule); L2 "
@@ -790,7 +792,7 @@ def run_gpu_arm(args):
                  "read + q + out + block tables)",
         "algorithmic_bytes": lpw["chunk_bytes"], "flops": lpw["chunk_flops"],
         "l2": StepRunner.FLUSH_TEXT,
-        "timed": "prefill kernel: median event time in a second loop with the prefill kernel on "
+        "timed": "prefill kernel: mean event time in a second loop with the prefill kernel on "
                  "the caller's stream",
     }
     del lp

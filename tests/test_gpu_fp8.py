@@ -77,13 +77,22 @@ def test_fp8_layout_checks():
         P.pa_forward_workspace_size(P.layout_of(kc, 4, k_scale=0.0), 1, 1, 16)
 
 
-def test_fp8_chunks_on_tensor_cores():
+@pytest.mark.parametrize("D", [64, 128])
+def test_fp8_chunks_on_tensor_cores(D):
     """Chunks of 17-300 tokens over an 8-bit cache take the tensor-core prefill
     kernel (codes widened to f16 in shared memory); with fewer units than SMs
     their KV is split into pieces that are merged.  Checked against the oracle
     over the dequantised cache."""
-    spec = W.custom_spec("fp8-chunks", "bf16", 8, 2, 128, [1, 300, 1, 64, 17],
-                         [700, 2300, 40, 64, 900], seed=77)
+    spec = W.custom_spec(f"fp8-chunks-{D}", "bf16", 8, 2, D, [1, 300, 1, 64, 17],
+                         [700, 2300, 40, 64, 900], seed=77 + D)
+    _run(spec, 0.01, 0.02)
+
+
+def test_fp8_short_chunk_long_prior():
+    """A 16-token chunk after ~6000 tokens of context over an 8-bit cache: one
+    unit per kv head, cut into many pieces (one round over the SMs), each
+    piece's tiles widened by the softmax warps, merged by the last piece."""
+    spec = W.custom_spec("fp8-long-prior", "bf16", 8, 2, 128, [16, 1], [6016, 300], seed=71)
     _run(spec, 0.01, 0.02)
 
 
@@ -97,9 +106,9 @@ def test_fp8_mixed_step():
 @pytest.mark.parametrize("D,G", [(64, 8), (64, 2), (128, 1)])
 def test_fp8_long_chunks(D, G):
     """Chunks of 40-300 tokens over 1000-3000 keys (up to 24 KV tiles a unit,
-    several units per CTA) over an 8-bit cache: the staged code copies run
-    ahead across tiles and units (two V staging buffers at D = 64, one at
-    D = 128), and the last tile's ragged block is zeroed."""
+    several units per CTA) over an 8-bit cache: K codes run two tiles ahead
+    in staging buffers, V codes land in place in the V buffers, across tiles
+    and units, and the last tile's ragged block is zeroed."""
     spec = W.custom_spec(f"fp8-long-{D}-{G}", "bf16", 2 * G, 2, D, [300, 1, 129, 40],
                          [3000, 77, 1001, 1500], seed=90 + D + G)
     _run(spec, 0.01, 0.02)
