@@ -30,6 +30,10 @@
 //     Each writes its half of P (bf16) over the first half of the tile's S,
 //     which both have read by then.  At the end of the unit the two halves'
 //     row sums are added and each warpgroup writes half of O's columns.
+// An FP8 (E4M3) cache: the loaders copy codes (K to staging buffers, V into
+// the V buffers themselves) and the softmax warps widen them to f16, one
+// 16-token block per warp, while they work on the tile before; the products
+// run as kind::f16.
 // Hand-offs are mbarriers; every wait is bounded and a timeout makes the whole
 // CTA stop (status PA_DEV_TIMEOUT), drain its copies and MMAs, and free TMEM.
 #include <cuda.h>
@@ -304,12 +308,14 @@ __device__ __forceinline__ void widen_blocks(uint32_t src, uint32_t src_stride, 
 
 }  // namespace
 
-// F8: the cache holds E4M3 codes.  They are copied by TMA into staging
-// buffers, up to two tiles ahead, and widened from there to f16 (exactly) in
-// the K / V tile buffers by the loader warps; Q is converted from bf16 to f16
-// in place once per unit, and the two products run as kind::f16 with f16
-// operands (P in f16).  The K scale is folded into the softmax scale and the
-// V scale into the normalisation.
+// F8: the cache holds E4M3 codes.  K codes are copied by TMA into two
+// staging buffers, two tiles ahead, V codes into the V tile buffers they are
+// widened in; both are widened to f16 (exactly) in the K / V tile buffers, a
+// unit's first two K tiles by the K loader and every other tile by the
+// softmax warps, one block each.  Q is converted from bf16 to f16 in place
+// once per unit, and the two products run as kind::f16 with f16 operands (P
+// in f16).  The K scale is folded into the softmax scale and the V scale
+// into the normalisation.
 template <int D, int G, bool F8>
 __global__ void __launch_bounds__(kPfThreads, 1)
     prefill_tc_kernel(const AttnParams p, const __grid_constant__ PfMaps maps) {
