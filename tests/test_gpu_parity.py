@@ -329,6 +329,9 @@ PREFILL_SHAPES = [
     # G = 1, 128 positions per tile: a piece boundary (key 4096) falls inside
     # the first query tile, so its early rows see no key in the last piece
     ("bf16", 128, 1, [150], [4150]),
+    # units of 157, 16 and 6 KV tiles, fewer than SMs: the plan takes the
+    # smallest piece size that fits one round, cutting them unevenly
+    ("bf16", 128, 4, [16, 16, 48], [20000, 2000, 700]),
 ]
 
 
